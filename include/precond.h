@@ -1,0 +1,150 @@
+/*
+ * libprecond: per-layer matrix-preconditioner step of EMA-Gram / KL-Shampoo
+ * style optimizers, on one NVIDIA GB300 (sm_103a).
+ *
+ * For every weight gradient G (m x n, row-major) one step computes
+ *
+ *   L <- beta L + (1 - beta) G G^T,   R <- beta R + (1 - beta) G^T G
+ *   A_hat = L / tr(L) + eps I          (same for R)
+ *   X_L = A_hat(L)^power, X_R = A_hat(R)^power,  power in {-1/4, -1/2}
+ *   U = X_L G X_R
+ *
+ * "Sharding EMA-Gram eigensolves" (Marin research note), section Background,
+ * defines the step (EMA of G G^T and G^T G, rescale, regularise the
+ * eigenvalues, raise to -1/4, reconstruct, shape the update).  The root is
+ * computed here without any eigensolver, by the coupled Newton-Schulz
+ * iteration of "Online KL Shampoo" (Tilde Research), section 2.2 and the
+ * Appendix D algorithm box, generalised to the inverse p-th root
+ * (T = ((p+1) I - M) / p, X <- X T, M <- T^p M, X_0 = I, M_0 = A_hat / c,
+ * c = 1.01 x the Appendix D upper bound on the largest eigenvalue), and it
+ * stops when ||M - I||_F <= tol * sqrt(d) (M equals X^p A_hat / c in exact
+ * arithmetic, so this is the residual of the inverse-root equation that
+ * Appendix E calls explicit and measurable).
+ *
+ * Conventions for every entry point:
+ *  - All matrix pointers are DEVICE pointers (cuda_device's memory), owned by
+ *    the caller, row-major, densely packed (leading dimension = columns).
+ *  - Pointer arrays (grads[], L[], ...) and shape arrays are HOST arrays,
+ *    read during the call only.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *    enqueued asynchronously on it; the call returns before it completes.
+ *  - The library owns a workspace cached in the handle: it grows on demand
+ *    (cudaMalloc, synchronising) and is freed by precond_destroy.
+ *  - Return value: PRECOND_OK (0) or a negative PRECOND_E* code.  Argument
+ *    errors are detected on the host before anything is enqueued.
+ *  - Per-root outcomes found on the device (non-convergence, non-finite
+ *    input) are reported by precond_get_stats, not by the return value.
+ *  - A handle is not thread-safe: use one handle per host thread.
+ */
+#ifndef LIBPRECOND_PRECOND_H
+#define LIBPRECOND_PRECOND_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct precond_ctx* precond_t;
+
+/* status codes */
+#define PRECOND_OK          0
+#define PRECOND_EINVAL     -1  /* bad argument (null pointer, bad size, bad power/eps/beta, aliasing) */
+#define PRECOND_ENOMEM     -2  /* workspace could not be allocated (or exceeds the set limit) */
+#define PRECOND_ECUDA      -3  /* a CUDA runtime/driver call failed */
+#define PRECOND_ENODEV     -4  /* host-only handle (created with cuda_device = -1): no GPU work possible */
+#define PRECOND_ENOTCONV   -5  /* per root: residual above tolerance after the iteration cap; output written */
+#define PRECOND_ENONFINITE -6  /* per root: NaN/Inf in the input or the Gram; output not written */
+
+/* gradient storage types */
+#define PRECOND_F32   0
+#define PRECOND_BF16  1
+
+/* option keys for precond_set_option */
+#define PRECOND_OPT_TOL            1  /* stop when ||M - I||_F <= tol*sqrt(d); default 1e-5 */
+#define PRECOND_OPT_MAX_ITER       2  /* iteration cap; 0 = derived from the scalar model (default) */
+#define PRECOND_OPT_MIN_ITER       3  /* stagnation test only after this many iterations; default 4 */
+#define PRECOND_OPT_ENGINE         4  /* 0 auto (default), 1 fp64 SIMT engine, 2 tcgen05 engine */
+#define PRECOND_OPT_SMALL_DIM      5  /* auto engine: max(m,n) <= this -> fp64 SIMT engine; default 512 */
+#define PRECOND_OPT_WORKSPACE_MAX  6  /* workspace limit in bytes; 0 = unlimited (default) */
+#define PRECOND_OPT_TIMING         7  /* 1 = record per-stage CUDA events (read by precond_get_timing) */
+#define PRECOND_OPT_USE_GRAPH      8  /* 1 = capture the step as a CUDA graph and replay it (default 0) */
+
+/*
+ * Create a handle bound to `cuda_device` (>= 0).  cuda_device = -1 creates a
+ * host-only handle that validates arguments and plans workspaces but enqueues
+ * nothing (every GPU call then returns PRECOND_ENODEV after validation).
+ * Errors: EINVAL (out == NULL or cuda_device < -1), ECUDA (device unusable).
+ */
+int precond_create(precond_t* out, int cuda_device);
+
+/* Free the workspace and the handle.  NULL is accepted (no-op). */
+int precond_destroy(precond_t h);
+
+/*
+ * One preconditioner step for `count` (>= 1) weight matrices.
+ *   grads[i]     : m_i x n_i gradient, PRECOND_F32 (float*) or PRECOND_BF16
+ *                  (16-bit bfloat16 words), per `grad_dtype`.  Read; and, when
+ *                  out_f32 == NULL, overwritten with U_i (rounded to bf16 for
+ *                  bf16 grads).
+ *   shapes       : 2*count int64: m_0, n_0, m_1, n_1, ...  (each >= 1)
+ *   L[i], R[i]   : fp32 EMA state, m_i x m_i and n_i x n_i, read and updated
+ *                  in place (start from zeros for the first step).  L[i] and
+ *                  R[i] must not alias each other or any other state.
+ *   beta         : EMA coefficient in [0, 1)
+ *   eps          : regulariser added to the eigenvalues of the unit-trace
+ *                  Gram, > 0
+ *   power        : -0.25f or -0.5f
+ *   out_f32      : NULL (write U in place into grads) or an array of count
+ *                  device pointers to fp32 m_i x n_i outputs
+ * Roots are numbered 2i (left, L) and 2i+1 (right, R) in precond_get_stats.
+ */
+int precond_step(precond_t h, int count, void* const grads[], int grad_dtype,
+                 const int64_t shapes[], float* const L[], float* const R[],
+                 float beta, float eps, float power, float* const out_f32[],
+                 void* stream);
+
+/*
+ * Inverse root of given SPD matrices (no EMA, no gradient):
+ *   X_i = (A_i / tr(A_i) + eps I)^power,  A_i and X_i fp32 d_i x d_i.
+ * eps is therefore relative to the trace.  A_i is read only; X_i may not
+ * alias A_i.  Roots are numbered i in precond_get_stats.
+ */
+int precond_inv_root(precond_t h, int count, const float* const A[], const int64_t dims[],
+                     float eps, float power, float* const X[], void* stream);
+
+/*
+ * Per-root results of the last precond_step / precond_inv_root on this
+ * handle.  Synchronises with that call's stream.  `nroots` must equal the
+ * number of roots of that call (2*count for a step, count for inv_root).
+ * Every output array may be NULL (skipped):
+ *   iters[r]  : Newton-Schulz iterations executed
+ *   resid[r]  : final ||M - I||_F / sqrt(d)
+ *   status[r] : PRECOND_OK, PRECOND_ENOTCONV or PRECOND_ENONFINITE
+ *   scale[r]  : c = 1.01 x the largest-eigenvalue bound of A_hat
+ */
+int precond_get_stats(precond_t h, int nroots, int iters[], float resid[], int status[],
+                      float scale[]);
+
+/* Set an option (PRECOND_OPT_*).  EINVAL for an unknown key or a bad value. */
+int precond_set_option(precond_t h, int key, double value);
+
+/*
+ * Milliseconds spent by stage in the last call when PRECOND_OPT_TIMING is on
+ * (synchronises): ms[0] input preparation + Gram EMA, ms[1] bound + start,
+ * ms[2] Newton-Schulz iterations, ms[3] finish + apply.  Also the number of
+ * GEMM launches of the iteration stage and its algorithmic FLOPs.
+ */
+int precond_get_timing(precond_t h, double ms[4], int64_t* ns_gemm_launches, double* ns_flops);
+
+/* Kernel launches this handle has issued since creation (every library kernel). */
+int64_t precond_launch_count(precond_t h);
+
+/* Static text for a status code. */
+const char* precond_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBPRECOND_PRECOND_H */
