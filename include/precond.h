@@ -140,6 +140,34 @@ int precond_get_timing(precond_t h, double ms[4], int64_t* ns_gemm_launches, dou
 /* Kernel launches this handle has issued since creation (every library kernel). */
 int64_t precond_launch_count(precond_t h);
 
+/*
+ * Read back the fp32 root of root `r` of the last precond_step on this handle
+ * (X_L of matrix i for r = 2i, X_R for r = 2i+1) into `dst`, a d x d device
+ * buffer owned by the caller.  Enqueued on `stream`.  For tests and
+ * diagnostics; the step itself never materialises fp32 roots.  After a
+ * precond_inv_root call it reads the root's last iterate instead.
+ */
+int precond_get_root(precond_t h, int r, float* dst, void* stream);
+
+/*
+ * Self-test of the GEMM core (no counterpart in the method: it checks the
+ * library's building block).  C = A . B^T with A (M x K), B (N x K), C (M x N)
+ * fp32 device buffers, through engine 1 (fp64 SIMT) or 2 (tcgen05, operands
+ * split into per-row-scaled bf16 digits); `passes` = digits used per operand
+ * (3 or 4; ignored by engine 1).  Synchronises `stream`.
+ */
+int precond_gemm_selftest(precond_t h, int engine, int M, int N, int K, const float* A, const float* B,
+                          float* C, int passes, void* stream);
+
+/*
+ * Diagnostic read-back (no counterpart in the method) of a work matrix of
+ * root `r` of the last call into a d x d fp32 device buffer:
+ * which = 0/1 X buffers, 2/3 M buffers, 4/5 T buffers, 6 T^2, 7 T^4, 8 the
+ * final root (step calls).  Iteration k reads buffers k & 1 and writes
+ * (k + 1) & 1.  Enqueued on `stream`.
+ */
+int precond_debug_plane(precond_t h, int r, int which, float* dst, void* stream);
+
 /* Static text for a status code. */
 const char* precond_error_string(int code);
 

@@ -1,0 +1,308 @@
+// tcgen05 batched GEMM of the large-matrix engine (sm_103a):  C_b = A_b . B_b^T
+//
+// Exact-digit split.  Each operand row is held as S bf16 "digit planes":
+//   x = sigma * 2^-b * (P_1 + P_2 + ... + P_S),   P_s = d_s * 2^(-b (s-1)),
+// with sigma a power of two >= max |x| of the row (a per-row scale, or one
+// bound for the whole matrix), b = 7 and integer digits |d_1| <= 2^b,
+// |d_s| <= 2^(b-1).  Digit products are exact in bf16 x bf16 -> fp32, and the
+// two leading product levels are sums of integers (level 2: P_1 Q_1; level 3:
+// P_1 Q_2 + P_2 Q_1 in units of 2^-b) below 2^24 for K <= 1024 (and for
+// non-coherent rows well beyond), so their fp32 tensor-memory accumulation is
+// EXACT: no rounding, and none of the truncation bias of a long fp32 chain.
+// The remaining levels (s + t >= 4) go to a third accumulator whose rounding
+// is 2^-14 below the result.  Products with s + t > S + 1 are dropped.
+//   S = 4: 10 MMAs per K step, ~2^-29 relative to the row scales;
+//   S = 3:  6 MMAs per K step, ~2^-22.
+// The epilogue forms C_ij = 2^-2b sigma_A(i) sigma_B(j) (acc0 + acc1 + acc2).
+//
+// Pipeline: TMA (3-D tensor maps {K, rows, batch}, 64-byte swizzle, K block
+// 32) into a 3-4 stage shared-memory ring; one elected thread issues
+// tcgen05.mma (kind::f16, bf16, M = 128, N = 128, K = 16) into three fp32
+// accumulators in tensor memory; four epilogue warps read them back with
+// tcgen05.ld.  Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM
+// owner and MMA issuer, warps 2..5 epilogue.  Every mbarrier wait is
+// bounded; on time-out the kernel records an error word and leaves the tile.
+#pragma once
+
+#include <cuda.h>
+#include "engine.cuh"
+
+namespace precond {
+
+constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 32;
+constexpr int TC_THREADS = 192;
+constexpr int DIGIT_BITS = 7;
+constexpr unsigned long long TC_WAIT_CYCLES = 4000000000ull;   // ~2 s at 2 GHz
+
+struct TcGemmArgs {
+  int M, N, K;
+  const int* a_index;    // batch entry -> z coordinate of A (null: b)
+  const int* b_index;    // batch entry -> z coordinate of B (null: b)
+  // operand scales: per-row arrays [z][rows] (A rows = output rows, B rows = output cols) or constants
+  const float* a_rowscale; long long a_rs_stride; float a_scale;
+  const float* b_rowscale; long long b_rs_stride; float b_scale;
+  unsigned int* err;     // error word (bit 0: a wait timed out)
+};
+
+template <int S>
+struct TcSmem {
+  static constexpr int A_BYTES = TC_BM * TC_BK * 2;            // 8 KB per digit plane
+  static constexpr int B_BYTES = TC_BN * TC_BK * 2;            // 8 KB
+  static constexpr int STAGE_BYTES = S * (A_BYTES + B_BYTES);
+  static constexpr int STAGES = (S == 4) ? 3 : 4;
+  static constexpr int TMEM_COLS = 512;                        // 3 x 128 used
+  static constexpr int BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+// ----------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded wait; returns false (and flags `err`) on time-out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > TC_WAIT_CYCLES) {
+      if (err) atomicOr(err, 1u);
+      return false;
+    }
+  }
+  return true;
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Shared-memory matrix descriptor: K-major, 64-byte swizzle (rows of 64 B),
+// 8-row groups 512 B apart.
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);          // start address
+  d |= (uint64_t)1 << 16;                           // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(512 >> 4) << 32;                  // stride byte offset
+  d |= (uint64_t)1 << 46;                           // descriptor version (tcgen05)
+  d |= (uint64_t)4 << 61;                           // swizzle mode: 64 B
+  return d;
+}
+// Instruction descriptor, kind::f16 with bf16 A and B: fp32 accumulate,
+// K-major A and B, M = 128, N = 128.
+__host__ __device__ constexpr uint32_t tc_idesc() {
+  return (1u << 4)                                  // D format f32
+       | (1u << 7) | (1u << 10)                     // A, B format bf16
+       | ((uint32_t)(TC_BN >> 3) << 17)             // N / 8
+       | ((uint32_t)(TC_BM >> 4) << 24);            // M / 16
+}
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+      ::"r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+      " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Digit-pair schedule (0-based digit indices), ordered by level s + t; the
+// first 6 pairs are the S = 3 schedule.  Accumulator: level 0 -> 0, level 1 -> 1,
+// level >= 2 -> 2.
+__host__ __device__ constexpr int pair_a(int i) {
+  return i == 0 ? 0 : i == 1 ? 0 : i == 2 ? 1 : i == 3 ? 0 : i == 4 ? 1 : i == 5 ? 2 : i == 6 ? 0 : i == 7 ? 1 : i == 8 ? 2 : 3;
+}
+__host__ __device__ constexpr int pair_b(int i) {
+  return i == 0 ? 0 : i == 1 ? 1 : i == 2 ? 0 : i == 3 ? 2 : i == 4 ? 1 : i == 5 ? 0 : i == 6 ? 3 : i == 7 ? 2 : i == 8 ? 1 : 0;
+}
+template <int S>
+struct Pairs { static constexpr int N = (S == 4) ? 10 : 6; };
+__host__ __device__ constexpr int pair_acc(int s, int t) { return (s + t) >= 2 ? 2 : (s + t); }
+
+// ----------------------------------------------------------------- kernel
+// Tensor maps: digit plane s of A is map_a[s] (only the first S are used).
+struct TcMaps {
+  CUtensorMap a[4];
+  CUtensorMap b[4];
+};
+
+template <int S>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
+  using SM = TcSmem<S>;
+  const int b = blockIdx.z;
+  if (epi_skip(e, b)) return;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bars = base + SM::STAGES * SM::STAGE_BYTES;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (SM::STAGES + s); };
+  const uint32_t accum_bar = bars + 8u * (2 * SM::STAGES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + SM::STAGES * SM::STAGE_BYTES + 8 * (2 * SM::STAGES + 1));
+  __shared__ double red[4];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SM::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(accum_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(tmem_slot)), "r"((uint32_t)SM::TMEM_COLS) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int tile_m = blockIdx.y * TC_BM, tile_n = blockIdx.x * TC_BN;
+  const int za = g.a_index ? g.a_index[b] : b;
+  const int zb = g.b_index ? g.b_index[b] : b;
+  const int nk = (g.K + TC_BK - 1) / TC_BK;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % SM::STAGES;
+        const uint32_t round = kb / SM::STAGES;
+        if (kb >= SM::STAGES && !mbar_wait(empty_bar(s), (round - 1) & 1, g.err)) break;
+        const uint32_t st = base + s * SM::STAGE_BYTES;
+        mbar_expect_tx(full_bar(s), SM::STAGE_BYTES);
+        const int kx = kb * TC_BK;
+#pragma unroll
+        for (int q = 0; q < S; ++q) {
+          tma_load_3d(st + q * SM::A_BYTES, &maps.a[q], full_bar(s), kx, tile_m, za);
+          tma_load_3d(st + S * SM::A_BYTES + q * SM::B_BYTES, &maps.b[q], full_bar(s), kx, tile_n, zb);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc_idesc();
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % SM::STAGES;
+        const uint32_t round = kb / SM::STAGES;
+        if (!mbar_wait(full_bar(s), round & 1, g.err)) break;
+        tc_fence_after();
+        const uint32_t st = base + s * SM::STAGE_BYTES;
+#pragma unroll
+        for (int k = 0; k < TC_BK / 16; ++k) {
+          const uint32_t koff = k * 32;   // 16 bf16 = 32 bytes inside the 64 B swizzle row
+#pragma unroll
+          for (int i = 0; i < Pairs<S>::N; ++i) {
+            const int pa = pair_a(i), pb = pair_b(i);
+            const int acc_id = pair_acc(pa, pb);
+            // first contribution of each accumulator in this tile starts it fresh
+            const bool first = (kb == 0 && k == 0) && (i == 0 || i == 1 || i == 3);
+            tc_mma(tmem + 128u * acc_id, sw64_desc(st + pa * SM::A_BYTES + koff),
+                   sw64_desc(st + S * SM::A_BYTES + pb * SM::B_BYTES + koff), idesc, first ? 0u : 1u);
+          }
+        }
+        tc_commit(empty_bar(s));
+      }
+      tc_commit(accum_bar);
+    }
+  } else {
+    // ------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const bool ok = mbar_wait(accum_bar, 0, g.err);
+    tc_fence_after();
+    const long long gr = tile_m + row;
+    const double c0 = (double)e.inv_scale * epi_matrix_scale(e, b) * ldexp(1.0, -2 * DIGIT_BITS);
+    double sa = 0.0;
+    if (gr < g.M) sa = g.a_rowscale ? (double)g.a_rowscale[(long long)za * g.a_rs_stride + gr] : (double)g.a_scale;
+    double part = 0.0;
+    float rmax = 0.f;
+    const bool track = (e.kind == EPI_M) && e.C.rowmax != nullptr;
+    if (ok) {
+#pragma unroll 1
+      for (int ch = 0; ch < TC_BN / 32; ++ch) {
+        float v0[32], v1[32], v2[32];
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ch * 32);
+        tmem_ld32(taddr, v0);
+        tmem_ld32(taddr + 128, v1);
+        tmem_ld32(taddr + 256, v2);
+        if (gr < g.M) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const long long gc = tile_n + ch * 32 + j;
+            if (gc < g.N) {
+              const double sb = g.b_rowscale ? (double)g.b_rowscale[(long long)zb * g.b_rs_stride + gc]
+                                             : (double)g.b_scale;
+              const double acc = (((double)v0[j] + (double)v1[j]) + (double)v2[j]) * (c0 * sa * sb);
+              part += epi_apply<ENGINE_TC>(e, b, gr, gc, acc);
+              rmax = fmaxf(rmax, (float)fabs(acc));
+            }
+          }
+        }
+      }
+      if (track && gr < g.M) atomic_max_nonneg(&e.C.rowmax[(long long)b * e.C.rows + gr], rmax);
+    }
+    if (e.kind == EPI_M) {
+      part = warp_sum(part);
+      if (lane == 0) red[q] = part;
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (warp == 2) epi_m_finish(e, b, red[0] + red[1] + red[2] + red[3], g.M, blockIdx.y * gridDim.x + blockIdx.x);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                 ::"r"(tmem), "r"((uint32_t)SM::TMEM_COLS) : "memory");
+  }
+}
+
+}  // namespace precond

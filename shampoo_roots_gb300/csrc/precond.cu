@@ -1,0 +1,1129 @@
+// libprecond host side: the C ABI of include/precond.h.
+//
+// A call is planned into classes:
+//  * shape classes: weight matrices of the same (m, n) and engine, batched in
+//    the preparation, Gram and apply launches;
+//  * root classes: roots (left / right Grams, or given SPD matrices) of the
+//    same side d and engine, batched in the bound, start, iteration and finish
+//    launches.
+// Matrices with max(m, n) <= small_dim use the fp64 SIMT engine, the others
+// the tcgen05 engine (fp16 split operands, fp32 tensor-memory accumulators).
+// Everything is enqueued on the caller's stream; the only host <-> device
+// traffic of a call is one upload of its pointer / index tables.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "engine.cuh"
+#include "gemm_f64.cuh"
+#include "gemm_tc.cuh"
+#include "stages.cuh"
+
+using namespace precond;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr size_t ALIGN = 1024;
+inline size_t align_up(size_t x, size_t a = ALIGN) { return (x + a - 1) / a * a; }
+inline int ld16(int cols) { return (int)align_up((size_t)cols, 64); }   // 16-bit planes: rows padded to 128 B
+
+struct Slab {   // an engine-format matrix batch inside the workspace
+  size_t off = 0;        // double plane (fp64 engine) or first bf16 digit plane (tcgen05 engine)
+  int digits = 0;        // digit planes allocated
+  long long pstride = 0; // elements between digit planes
+  int rows = 0, cols = 0, ld = 0, batch = 0;
+  float scale = 1.f;     // fixed power-of-two digit scale (0: per-row scales in `rowscale`)
+  size_t f32 = 0, rowmax = 0, rowscale = 0;   // fp32 form + per-row max / scale (0: absent)
+};
+
+struct RootClass {
+  int d = 0, eng = 0;
+  std::vector<int> roots;              // global root ids
+  std::vector<const float*> src;       // per entry: source matrix (caller)
+  std::vector<float*> dst;             // per entry: caller output (inv_root)
+  Slab X[2], M[2], T[2], T2, T4, Xf;
+  size_t rowabs = 0, diag = 0, rowsq = 0, partials = 0;
+  long long tiles = 0;
+  size_t t_root = 0, t_src = 0, t_dst = 0, t_xscale = 0;   // device tables (offsets)
+  int kmax = 0;
+  std::vector<float> xscale;           // tcgen05 engine: digit scale of X_k, k = 0..kmax
+};
+
+struct ShapeClass {
+  int m = 0, n = 0, eng = 0;
+  std::vector<int> mats;
+  int lrc = -1, rrc = -1;
+  std::vector<int> lslot, rslot;
+  Slab Gd, GTd, VTd;                    // fp64 engine
+  Slab Gq, GTq, VTq;                    // tcgen05 engine: per-row-scaled digits (+ fp32 form)
+  size_t mstat = 0;
+  size_t t_g = 0, t_L = 0, t_R = 0, t_out = 0, t_roots2 = 0, t_lslot = 0, t_rslot = 0;
+};
+
+struct Plan {
+  bool step = true;
+  int count = 0, nroots = 0, p = 4, dtype = PRECOND_F32;
+  bool out_f32 = false;
+  std::vector<ShapeClass> sc;
+  std::vector<RootClass> rc;
+  size_t stats = 0, err = 0, partials = 0, meta = 0, meta_bytes = 0, total = 0;
+  long long max_tiles = 0;
+  std::vector<uint8_t> meta_host;
+};
+
+}  // namespace
+
+struct precond_ctx {
+  int device = -1;
+  double tol = 1e-5;
+  int max_iter = 0, min_iter = 4, engine = 0, small_dim = 512, timing = 0, use_graph = 0;
+  double ws_max = 0;
+  void* ws = nullptr;
+  size_t ws_cap = 0;
+  void* pinned = nullptr;
+  size_t pinned_cap = 0;
+  cudaEvent_t upload_done = nullptr;
+  bool upload_pending = false;
+  cudaEvent_t ev[5] = {};
+  bool events = false;
+  cudaStream_t last_stream = nullptr;
+  int last_nroots = 0;
+  int last_p = 4;
+  bool have_last = false;
+  std::vector<int> last_root_d;       // per root: d
+  std::vector<int> last_root_class, last_root_slot;
+  Plan last_plan;
+  int64_t launches = 0;
+  int64_t ns_launches = 0;
+  EncodeTiledFn encode = nullptr;
+  bool tc_attr_set = false;
+};
+
+namespace {
+
+#define CK(call)                                                                 \
+  do {                                                                           \
+    cudaError_t e_ = (call);                                                     \
+    if (e_ != cudaSuccess) {                                                     \
+      fprintf(stderr, "libprecond: %s failed: %s\n", #call, cudaGetErrorString(e_)); \
+      return PRECOND_ECUDA;                                                      \
+    }                                                                            \
+  } while (0)
+
+int iter_cap(double eps, int d, int p, double tol, int user_max) {
+  if (user_max > 0) return user_max;
+  // scalar model of the iteration on the smallest scaled eigenvalue
+  double m = eps / (1.01 * (1.0 + d * eps));
+  int k = 0;
+  while (std::fabs(m - 1.0) >= tol * 0.1 && k < 200) {
+    m = m * std::pow((p + 1 - m) / p, p);
+    ++k;
+  }
+  return std::min(k + 3, 60);
+}
+
+
+struct Layout {
+  size_t top = 0;
+  size_t take(size_t bytes) {
+    size_t o = top;
+    top = align_up(top + std::max<size_t>(bytes, 1));
+    return o;
+  }
+};
+
+Slab make_slab(Layout& L, int eng, int batch, int rows, int cols, int digits = 4, bool per_row = false) {
+  Slab s;
+  s.rows = rows;
+  s.cols = cols;
+  s.batch = batch;
+  if (eng == ENGINE_F64) {
+    s.ld = cols;
+    s.off = L.take((size_t)batch * rows * cols * sizeof(double));
+  } else {
+    s.ld = ld16(cols);
+    s.digits = digits;
+    s.pstride = (long long)batch * rows * s.ld;
+    s.off = L.take((size_t)s.pstride * 2 * digits);
+    if (per_row) {
+      s.scale = 0.f;
+      s.f32 = L.take((size_t)s.pstride * sizeof(float));
+      s.rowmax = L.take((size_t)batch * rows * sizeof(float));
+      s.rowscale = L.take((size_t)batch * rows * sizeof(float));
+    }
+  }
+  return s;
+}
+
+float pow2_ceil_host(double x) {
+  if (!(x > 0)) return 1.f;
+  int e;
+  const double f = std::frexp(x, &e);
+  return f == 0.5 ? (float)x : std::ldexp(1.0f, e);
+}
+
+struct MetaWriter {
+  std::vector<uint8_t>& buf;
+  size_t base;   // workspace offset of the meta region
+  explicit MetaWriter(std::vector<uint8_t>& b, size_t base_) : buf(b), base(base_) {}
+  template <typename T>
+  size_t put(const std::vector<T>& v) {
+    size_t o = align_up(buf.size(), 16);
+    buf.resize(o + std::max<size_t>(v.size() * sizeof(T), 16));
+    if (!v.empty()) memcpy(buf.data() + o, v.data(), v.size() * sizeof(T));
+    return base + o;
+  }
+};
+
+int check_power(float power, int* p) {
+  if (power == -0.25f) { *p = 4; return PRECOND_OK; }
+  if (power == -0.5f) { *p = 2; return PRECOND_OK; }
+  return PRECOND_EINVAL;
+}
+
+int pick_engine(const precond_ctx* h, int64_t maxdim) {
+  if (h->engine == 1) return ENGINE_F64;
+  if (h->engine == 2) return ENGINE_TC;
+  return maxdim <= h->small_dim ? ENGINE_F64 : ENGINE_TC;
+}
+
+// Root-class planes and scales.
+void layout_root_class(Layout& L, RootClass& r, int p, double eps) {
+  const int nb = (int)r.roots.size(), d = r.d, e = r.eng;
+  for (int i = 0; i < 2; ++i) {
+    r.X[i] = make_slab(L, e, nb, d, d);
+    r.M[i] = make_slab(L, e, nb, d, d, 4, true);
+    r.T[i] = make_slab(L, e, nb, d, d);
+  }
+  r.T2 = make_slab(L, e, nb, d, d);
+  if (p == 4) r.T4 = make_slab(L, e, nb, d, d);
+  r.Xf = make_slab(L, e, nb, d, d);
+  r.rowabs = L.take((size_t)nb * d * sizeof(double));
+  r.diag = L.take((size_t)nb * d * sizeof(double));
+  r.rowsq = L.take((size_t)nb * d * sizeof(double));
+  if (e == ENGINE_TC) {
+    // entry bounds from the spectra (|a_ij| <= ||A||_2 for symmetric A):
+    // T in [1, (p+1)/p], T^2, T^4 accordingly, X_k <= m0^(-1/p), final X <= eps^(-1/p).
+    const double tmax = (p + 1.0) / p;
+    const double m0 = eps / (1.01 * (1.0 + d * eps));
+    const double xmax = std::pow(m0, -1.0 / p);
+    const double xf = std::pow(eps, -1.0 / p);
+    for (int i = 0; i < 2; ++i) {
+      r.T[i].scale = pow2_ceil_host(tmax * 1.001);
+      r.X[i].scale = pow2_ceil_host(xmax * 1.001);
+    }
+    r.T2.scale = pow2_ceil_host(tmax * tmax * 1.001);
+    r.T4.scale = pow2_ceil_host(std::pow(tmax, 4) * 1.001);
+    r.Xf.scale = pow2_ceil_host(xf * 1.001);
+  }
+}
+
+int build_plan(precond_ctx* h, Plan& P, bool step, int count, const int64_t* dims2, int dtype, float eps,
+               int p, void* const* grads, float* const* Ls, float* const* Rs, float* const* outs,
+               const float* const* As, float* const* Xs) {
+  P = Plan();
+  P.step = step;
+  P.count = count;
+  P.p = p;
+  P.dtype = dtype;
+  P.out_f32 = outs != nullptr;
+  std::map<std::pair<int, int>, int> rc_index;
+  auto root_class = [&](int d, int eng) {
+    auto key = std::make_pair(d, eng);
+    auto it = rc_index.find(key);
+    if (it != rc_index.end()) return it->second;
+    RootClass r;
+    r.d = d;
+    r.eng = eng;
+    P.rc.push_back(r);
+    rc_index[key] = (int)P.rc.size() - 1;
+    return (int)P.rc.size() - 1;
+  };
+  if (step) {
+    std::map<std::pair<int, int>, int> sc_index;
+    P.nroots = 2 * count;
+    for (int i = 0; i < count; ++i) {
+      const int m = (int)dims2[2 * i], n = (int)dims2[2 * i + 1];
+      auto key = std::make_pair(m, n);
+      auto it = sc_index.find(key);
+      int s;
+      if (it == sc_index.end()) {
+        ShapeClass c;
+        c.m = m;
+        c.n = n;
+        c.eng = pick_engine(h, std::max(m, n));
+        P.sc.push_back(c);
+        s = (int)P.sc.size() - 1;
+        sc_index[key] = s;
+      } else {
+        s = it->second;
+      }
+      P.sc[s].mats.push_back(i);
+    }
+    for (auto& c : P.sc) {
+      c.lrc = root_class(c.m, c.eng);
+      c.rrc = root_class(c.n, c.eng);
+      for (int i : c.mats) {
+        RootClass& l = P.rc[c.lrc];
+        c.lslot.push_back((int)l.roots.size());
+        l.roots.push_back(2 * i);
+        l.src.push_back(Ls ? Ls[i] : nullptr);
+        l.dst.push_back(nullptr);
+        RootClass& r = P.rc[c.rrc];
+        c.rslot.push_back((int)r.roots.size());
+        r.roots.push_back(2 * i + 1);
+        r.src.push_back(Rs ? Rs[i] : nullptr);
+        r.dst.push_back(nullptr);
+      }
+    }
+  } else {
+    P.nroots = count;
+    for (int i = 0; i < count; ++i) {
+      const int d = (int)dims2[i];
+      const int r = root_class(d, pick_engine(h, d));
+      P.rc[r].roots.push_back(i);
+      P.rc[r].src.push_back(As ? As[i] : nullptr);
+      P.rc[r].dst.push_back(Xs ? Xs[i] : nullptr);
+    }
+  }
+
+  Layout L;
+  P.stats = L.take(sizeof(RootStat) * P.nroots);
+  P.err = L.take(64);
+  for (auto& r : P.rc) {
+    layout_root_class(L, r, p, eps);
+    r.kmax = iter_cap(eps, r.d, p, h->tol, h->max_iter);
+    // X_k = prod_j T_j; its largest eigenvalue follows the scalar model on the
+    // smallest scaled eigenvalue m0 = eps / (1.01 (1 + d eps)) <= lambda_min(M_0):
+    // x_k = (m_k / m0)^(1/p) with m_{k+1} = m_k ((p+1-m_k)/p)^p.
+    r.xscale.assign(r.kmax + 2, 1.f);
+    double m = eps / (1.01 * (1.0 + r.d * eps));
+    const double m0 = m;
+    for (int k = 0; k <= r.kmax + 1; ++k) {
+      r.xscale[k] = pow2_ceil_host(std::pow(m / m0, 1.0 / p) * 1.01);
+      m = m * std::pow((p + 1 - m) / p, p);
+    }
+    const long long t = r.eng == ENGINE_F64
+        ? (long long)((r.d + F64_BM - 1) / F64_BM) * ((r.d + F64_BN - 1) / F64_BN)
+        : (long long)((r.d + TC_BM - 1) / TC_BM) * ((r.d + TC_BN - 1) / TC_BN);
+    P.max_tiles = std::max(P.max_tiles, t);
+  }
+  P.partials = L.take(sizeof(double) * P.max_tiles * P.nroots);
+  for (auto& c : P.sc) {
+    const int nb = (int)c.mats.size();
+    if (c.eng == ENGINE_F64) {
+      c.Gd = make_slab(L, ENGINE_F64, nb, c.m, c.n);
+      c.GTd = make_slab(L, ENGINE_F64, nb, c.n, c.m);
+      c.VTd = make_slab(L, ENGINE_F64, nb, c.n, c.m);
+    } else {
+      c.Gq = make_slab(L, ENGINE_TC, nb, c.m, c.n, 4, true);
+      c.GTq = make_slab(L, ENGINE_TC, nb, c.n, c.m, 4, true);
+      c.VTq = make_slab(L, ENGINE_TC, nb, c.n, c.m, 4, true);
+    }
+    c.mstat = L.take(sizeof(MatStat) * nb);
+  }
+  // meta tables
+  P.meta = L.top;
+  MetaWriter W(P.meta_host, P.meta);
+  for (auto& r : P.rc) {
+    std::vector<int> ro(r.roots.begin(), r.roots.end());
+    r.t_root = W.put(ro);
+    r.t_src = W.put(r.src);
+    r.t_dst = W.put(r.dst);
+    r.t_xscale = W.put(r.xscale);
+  }
+  for (auto& c : P.sc) {
+    std::vector<const void*> g;
+    std::vector<float*> l, rr;
+    std::vector<void*> o;
+    std::vector<int> roots2;
+    for (int i : c.mats) {
+      g.push_back(grads ? grads[i] : nullptr);
+      l.push_back(Ls ? Ls[i] : nullptr);
+      rr.push_back(Rs ? Rs[i] : nullptr);
+      o.push_back(outs ? (void*)outs[i] : (grads ? grads[i] : nullptr));
+      roots2.push_back(2 * i);
+      roots2.push_back(2 * i + 1);
+    }
+    c.t_g = W.put(g);
+    c.t_L = W.put(l);
+    c.t_R = W.put(rr);
+    c.t_out = W.put(o);
+    c.t_roots2 = W.put(roots2);
+    c.t_lslot = W.put(c.lslot);
+    c.t_rslot = W.put(c.rslot);
+  }
+  P.meta_bytes = align_up(P.meta_host.size(), 16);
+  P.meta_host.resize(P.meta_bytes);
+  P.total = align_up(P.meta + P.meta_bytes);
+  return PRECOND_OK;
+}
+
+int ensure_workspace(precond_ctx* h, size_t bytes) {
+  if (h->ws_max > 0 && (double)bytes > h->ws_max) return PRECOND_ENOMEM;
+  if (bytes <= h->ws_cap) return PRECOND_OK;
+  CK(cudaDeviceSynchronize());
+  if (h->ws) cudaFree(h->ws);
+  h->ws = nullptr;
+  h->ws_cap = 0;
+  if (cudaMalloc(&h->ws, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return PRECOND_ENOMEM;
+  }
+  h->ws_cap = bytes;
+  return PRECOND_OK;
+}
+
+int upload_meta(precond_ctx* h, const Plan& P, cudaStream_t st) {
+  if (h->upload_pending) {
+    CK(cudaEventSynchronize(h->upload_done));
+    h->upload_pending = false;
+  }
+  if (P.meta_bytes > h->pinned_cap) {
+    if (h->pinned) cudaFreeHost(h->pinned);
+    h->pinned = nullptr;
+    h->pinned_cap = 0;
+    CK(cudaMallocHost(&h->pinned, P.meta_bytes));
+    h->pinned_cap = P.meta_bytes;
+  }
+  memcpy(h->pinned, P.meta_host.data(), P.meta_bytes);
+  CK(cudaMemcpyAsync((char*)h->ws + P.meta, h->pinned, P.meta_bytes, cudaMemcpyHostToDevice, st));
+  CK(cudaEventRecord(h->upload_done, st));
+  h->upload_pending = true;
+  return PRECOND_OK;
+}
+
+// --------------------------------------------------------------------------- launch helpers
+struct Ctx {
+  precond_ctx* h;
+  const Plan& P;
+  char* ws;
+  cudaStream_t st;
+  template <typename T>
+  T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
+  RootStat* stats() const { return at<RootStat>(P.stats); }
+  unsigned int* err() const { return at<unsigned int>(P.err); }
+  // Store target: the digit form, or the fp32 form for per-row-scaled slabs.
+  Plane plane(const Slab& s) const {
+    Plane p;
+    memset(&p, 0, sizeof(p));
+    p.hi = ws + s.off;
+    p.pstride = s.pstride;
+    p.bstride = (long long)s.rows * s.ld;
+    p.ld = s.ld;
+    p.scale = s.scale;
+    p.S = s.digits;
+    p.rows = s.rows;
+    if (s.f32) {
+      p.f32 = reinterpret_cast<float*>(ws + s.f32);
+      p.rowmax = reinterpret_cast<float*>(ws + s.rowmax);
+    }
+    return p;
+  }
+  // Load source: always the digit form (or the double plane).
+  Plane digits(const Slab& s) const {
+    Plane p = plane(s);
+    p.f32 = nullptr;
+    p.rowmax = nullptr;
+    return p;
+  }
+};
+
+Epi base_epi(const Ctx& c, int kind, int rows, int cols) {
+  Epi e;
+  memset(&e, 0, sizeof(e));
+  e.kind = kind;
+  e.rows = rows;
+  e.cols = cols;
+  e.stats = c.stats();
+  e.inv_scale = 1.f;
+  return e;
+}
+
+int encode_map(precond_ctx* h, CUtensorMap* map, void* base, const Slab& s, int box_rows) {
+  cuuint64_t dims[3] = {(cuuint64_t)s.cols, (cuuint64_t)s.rows, (cuuint64_t)s.batch};
+  cuuint64_t strides[2] = {(cuuint64_t)s.ld * 2, (cuuint64_t)s.ld * 2 * s.rows};
+  cuuint32_t box[3] = {(cuuint32_t)TC_BK, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    fprintf(stderr, "libprecond: cuTensorMapEncodeTiled failed (%d)\n", (int)r);
+    return PRECOND_ECUDA;
+  }
+  return PRECOND_OK;
+}
+
+// Batched product C_b = A_b B_b^T in the engine of the operands; the tcgen05
+// engine uses the first `S` digit planes of each operand (S = 3 or 4).
+int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int K, const int* aidx,
+         const int* bidx, int S, const Epi& e0, int batch) {
+  Epi e = e0;
+  if (eng == ENGINE_F64) {
+    GemmF64Args g;
+    g.A = c.at<double>(A.off);
+    g.a_bstride = (long long)A.rows * A.ld;
+    g.lda = A.ld;
+    g.B = c.at<double>(B.off);
+    g.b_bstride = (long long)B.rows * B.ld;
+    g.ldb = B.ld;
+    g.a_index = aidx;
+    g.b_index = bidx;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    dim3 grid((N + F64_BN - 1) / F64_BN, (M + F64_BM - 1) / F64_BM, batch);
+    e.tiles_per_entry = grid.x * grid.y;
+    gemm_f64_kernel<<<grid, 256, 0, c.st>>>(g, e);
+  } else {
+    if (S > A.digits || S > B.digits) return PRECOND_EINVAL;
+    TcMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    int rc;
+    for (int q = 0; q < S; ++q) {
+      if ((rc = encode_map(c.h, &maps.a[q], c.ws + A.off + (size_t)q * A.pstride * 2, A, TC_BM))) return rc;
+      if ((rc = encode_map(c.h, &maps.b[q], c.ws + B.off + (size_t)q * B.pstride * 2, B, TC_BN))) return rc;
+    }
+    TcGemmArgs g;
+    memset(&g, 0, sizeof(g));
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.a_index = aidx;
+    g.b_index = bidx;
+    g.a_rowscale = A.rowscale ? c.at<const float>(A.rowscale) : nullptr;
+    g.a_rs_stride = A.rows;
+    g.a_scale = A.scale;
+    g.b_rowscale = B.rowscale ? c.at<const float>(B.rowscale) : nullptr;
+    g.b_rs_stride = B.rows;
+    g.b_scale = B.scale;
+    g.err = c.err();
+    dim3 grid((N + TC_BN - 1) / TC_BN, (M + TC_BM - 1) / TC_BM, batch);
+    e.tiles_per_entry = grid.x * grid.y;
+    if (S == 4)
+      gemm_tc_kernel<4><<<grid, TC_THREADS, TcSmem<4>::BYTES, c.st>>>(maps, g, e);
+    else
+      gemm_tc_kernel<3><<<grid, TC_THREADS, TcSmem<3>::BYTES, c.st>>>(maps, g, e);
+  }
+  c.h->launches++;
+  CK(cudaGetLastError());
+  return PRECOND_OK;
+}
+
+// Per-row-scaled digits of a slab's fp32 form.
+int slice(const Ctx& c, const Slab& s) {
+  SliceArgs a;
+  a.src = c.at<const float>(s.f32);
+  a.src_bstride = (long long)s.rows * s.ld;
+  a.src_ld = s.ld;
+  a.rowmax = c.at<const float>(s.rowmax);
+  a.rowscale = c.at<float>(s.rowscale);
+  a.dst = c.digits(s);
+  a.rows = s.rows;
+  a.cols = s.cols;
+  const int rb = std::min((s.rows + 7) / 8, 1024);
+  slice_rows_kernel<<<dim3(rb, s.batch), 256, 0, c.st>>>(a);
+  c.h->launches++;
+  CK(cudaGetLastError());
+  return PRECOND_OK;
+}
+
+int clear_rowmax(const Ctx& c, const Slab& s) {
+  if (s.rowmax) CK(cudaMemsetAsync(c.ws + s.rowmax, 0, (size_t)s.batch * s.rows * sizeof(float), c.st));
+  return PRECOND_OK;
+}
+
+RootArgs root_args(const Ctx& c, const RootClass& r, float eps) {
+  RootArgs a;
+  memset(&a, 0, sizeof(a));
+  a.src = c.at<const float* const>(r.t_src);
+  a.root_of = c.at<const int>(r.t_root);
+  a.stats = c.stats();
+  a.rowabs = c.at<double>(r.rowabs);
+  a.diag = c.at<double>(r.diag);
+  a.rowsq = c.at<double>(r.rowsq);
+  a.d = r.d;
+  a.eps = eps;
+  a.ctl.p = c.P.p;
+  a.ctl.kmin = c.h->min_iter;
+  a.ctl.kmax = r.kmax;
+  a.ctl.tol = (float)c.h->tol;
+  a.M0 = c.plane(r.M[0]);     // fp32 form (tcgen05 engine), sliced after the start
+  a.T0 = c.plane(r.T[0]);
+  a.X1 = c.plane(r.X[1]);
+  if (r.eng == ENGINE_TC) a.X1.scale = r.xscale[1];
+  a.X[0] = c.digits(r.X[0]);
+  a.X[1] = c.digits(r.X[1]);
+  a.Xf = c.plane(r.Xf);
+  a.dst = c.P.step ? nullptr : c.at<float* const>(r.t_dst);
+  a.xscale = r.eng == ENGINE_TC ? c.at<const float>(r.t_xscale) : nullptr;
+  return a;
+}
+
+int launch_roots_start(const Ctx& c, float eps) {
+  for (const auto& r : c.P.rc) {
+    const int nb = (int)r.roots.size();
+    RootArgs a = root_args(c, r, eps);
+    const int rb = std::min((r.d + 7) / 8, 512);
+    root_stats_kernel<<<dim3(rb, nb), 256, 0, c.st>>>(a);
+    root_bound_kernel<<<dim3(rb, nb), 256, 0, c.st>>>(a);
+    dim3 g((r.d + 31) / 32, (r.d + 31) / 32, nb);
+    int rc;
+    if (r.eng == ENGINE_F64) {
+      root_init_kernel<ENGINE_F64><<<g, 256, 0, c.st>>>(a);
+    } else {
+      if ((rc = clear_rowmax(c, r.M[0]))) return rc;
+      root_init_kernel<ENGINE_TC><<<g, 256, 0, c.st>>>(a);
+    }
+    c.h->launches += 3;
+    CK(cudaGetLastError());
+    if (r.eng == ENGINE_TC && (rc = slice(c, r.M[0]))) return rc;
+  }
+  return PRECOND_OK;
+}
+
+int launch_iterations(const Ctx& c) {
+  const int p = c.P.p;
+  int kall = 0;
+  for (const auto& r : c.P.rc) kall = std::max(kall, r.kmax);
+  int64_t n = 0;
+  for (int k = 0; k < kall; ++k) {
+    for (const auto& r : c.P.rc) {
+      if (k >= r.kmax) continue;
+      const int nb = (int)r.roots.size(), d = r.d, eng = r.eng;
+      const int* root_of = c.at<const int>(r.t_root);
+      const int cur = k & 1, nxt = (k + 1) & 1;
+      int rcode;
+      Epi e = base_epi(c, EPI_STORE, d, d);
+      e.root_of = root_of;
+      e.partials = c.at<double>(c.P.partials);
+      e.partials_stride = c.P.max_tiles;
+      e.ctl.p = p;
+      e.ctl.kmin = c.h->min_iter;
+      e.ctl.kmax = r.kmax;
+      e.ctl.tol = (float)c.h->tol;
+      e.k = k;
+      const bool tc = eng == ENGINE_TC;
+      if (k >= 1) {   // X_{k+1} = X_k T_k   (X_1 = T_0 was written by the start)
+        Epi ex = e;
+        Slab Xc = r.X[cur], Xn = r.X[nxt];
+        if (tc) {
+          Xc.scale = r.xscale[k];
+          Xn.scale = r.xscale[k + 1];
+        }
+        ex.C = c.plane(Xn);
+        if ((rcode = gemm(c, eng, Xc, r.T[cur], d, d, d, nullptr, nullptr, 4, ex, nb))) return rcode;
+        ++n;
+      }
+      Epi e2 = e;   // T2 = T T
+      e2.C = c.plane(r.T2);
+      if ((rcode = gemm(c, eng, r.T[cur], r.T[cur], d, d, d, nullptr, nullptr, 4, e2, nb))) return rcode;
+      ++n;
+      const Slab* Tp = &r.T2;
+      if (p == 4) {   // T4 = T2 T2
+        Epi e4 = e;
+        e4.C = c.plane(r.T4);
+        if ((rcode = gemm(c, eng, r.T2, r.T2, d, d, d, nullptr, nullptr, 4, e4, nb))) return rcode;
+        ++n;
+        Tp = &r.T4;
+      }
+      Epi em = e;     // M_{k+1} = T^p M_k, T_{k+1}, residual, convergence
+      em.kind = EPI_M;
+      em.C = c.plane(r.M[nxt]);
+      em.C2 = c.plane(r.T[nxt]);
+      if (tc) em.C.rowmax = nullptr;   // row maxima and T come from the symmetrisation pass
+      if ((rcode = gemm(c, eng, *Tp, r.M[cur], d, d, d, nullptr, nullptr, 4, em, nb))) return rcode;
+      ++n;
+      if (tc) {
+        if ((rcode = clear_rowmax(c, r.M[nxt]))) return rcode;
+        SymArgs sa;
+        sa.M = c.plane(r.M[nxt]);
+        sa.T = c.plane(r.T[nxt]);
+        sa.root_of = root_of;
+        sa.stats = c.stats();
+        sa.d = d;
+        sa.p = p;
+        const int tb = (d + 31) / 32;
+        sym_m_kernel<<<dim3(tb, tb, nb), 256, 0, c.st>>>(sa);
+        c.h->launches++;
+        CK(cudaGetLastError());
+        if ((rcode = slice(c, r.M[nxt]))) return rcode;
+      }
+    }
+  }
+  c.h->ns_launches = n;
+  return PRECOND_OK;
+}
+
+int launch_finish(const Ctx& c, float eps) {
+  for (const auto& r : c.P.rc) {
+    const int nb = (int)r.roots.size();
+    RootArgs a = root_args(c, r, eps);
+    dim3 g((r.d + 31) / 32, (r.d + 31) / 32, nb);
+    if (r.eng == ENGINE_F64) root_finish_kernel<ENGINE_F64><<<g, 256, 0, c.st>>>(a);
+    else root_finish_kernel<ENGINE_TC><<<g, 256, 0, c.st>>>(a);
+    c.h->launches++;
+    CK(cudaGetLastError());
+  }
+  return PRECOND_OK;
+}
+
+Plane digits_plane(char* ws, const Slab& s) {
+  Plane p;
+  memset(&p, 0, sizeof(p));
+  p.hi = ws + s.off;
+  p.pstride = s.pstride;
+  p.bstride = (long long)s.rows * s.ld;
+  p.ld = s.ld;
+  p.scale = s.scale;
+  p.S = s.digits;
+  p.rows = s.rows;
+  return p;
+}
+
+int record(precond_ctx* h, int i, cudaStream_t st) {
+  if (h->timing && h->events) CK(cudaEventRecord(h->ev[i], st));
+  return PRECOND_OK;
+}
+
+int run_step(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream_t st) {
+  Ctx c{h, P, (char*)h->ws, st};
+  int rc;
+  CK(cudaMemsetAsync(c.ws + P.stats, 0, sizeof(RootStat) * P.nroots + 64, st));
+  if ((rc = record(h, 0, st))) return rc;
+  // ---- preparation + Gram EMA
+  for (const auto& s : P.sc) {
+    const int nb = (int)s.mats.size();
+    CK(cudaMemsetAsync(c.ws + s.mstat, 0, sizeof(MatStat) * nb, st));
+    PrepArgs a;
+    memset(&a, 0, sizeof(a));
+    a.g = c.at<const void* const>(s.t_g);
+    a.dtype = P.dtype;
+    a.m = s.m;
+    a.n = s.n;
+    a.roots2 = c.at<const int>(s.t_roots2);
+    a.stats = c.stats();
+    a.mstat = c.at<MatStat>(s.mstat);
+    const bool tc = s.eng == ENGINE_TC;
+    if (tc) {
+      a.Gf = c.at<float>(s.Gq.f32);
+      a.ldn = s.Gq.ld;
+      a.GTf = c.at<float>(s.GTq.f32);
+      a.ldm = s.GTq.ld;
+      a.rowmax_G = c.at<float>(s.Gq.rowmax);
+      a.rowmax_GT = c.at<float>(s.GTq.rowmax);
+      if ((rc = clear_rowmax(c, s.GTq))) return rc;
+    } else {
+      a.Gd = c.at<double>(s.Gd.off);
+      a.GTd = c.at<double>(s.GTd.off);
+    }
+    dim3 gs((s.n + 31) / 32, (s.m + 31) / 32, nb);
+    const int rb = std::min((s.m + 7) / 8, 512);
+    prep_reduce_kernel<<<dim3(rb, nb), 256, 0, st>>>(a);
+    if (tc) prep_split_kernel<ENGINE_TC><<<gs, 256, 0, st>>>(a);
+    else prep_split_kernel<ENGINE_F64><<<gs, 256, 0, st>>>(a);
+    h->launches += 2;
+    CK(cudaGetLastError());
+    if (tc) {
+      if ((rc = slice(c, s.Gq))) return rc;
+      if ((rc = slice(c, s.GTq))) return rc;
+    }
+    for (int side = 0; side < 2; ++side) {
+      const int dim = side == 0 ? s.m : s.n, K = side == 0 ? s.n : s.m;
+      Epi e = base_epi(c, EPI_GRAM, dim, dim);
+      e.state = c.at<float* const>(side == 0 ? s.t_L : s.t_R);
+      e.beta = beta;
+      e.nonfinite_of = c.at<const int>(s.t_roots2);
+      const Slab& G = tc ? (side == 0 ? s.Gq : s.GTq) : (side == 0 ? s.Gd : s.GTd);
+      if ((rc = gemm(c, s.eng, G, G, dim, dim, K, nullptr, nullptr, 4, e, nb))) return rc;
+    }
+  }
+  if ((rc = record(h, 1, st))) return rc;
+  if ((rc = launch_roots_start(c, eps))) return rc;
+  if ((rc = record(h, 2, st))) return rc;
+  if ((rc = launch_iterations(c))) return rc;
+  if ((rc = record(h, 3, st))) return rc;
+  if ((rc = launch_finish(c, eps))) return rc;
+  // ---- apply: V = G X_R (stored transposed), U = X_L V
+  for (const auto& s : P.sc) {
+    const int nb = (int)s.mats.size();
+    const RootClass& l = P.rc[s.lrc];
+    const RootClass& r = P.rc[s.rrc];
+    Epi ev = base_epi(c, EPI_VT, s.m, s.n);
+    Epi eu = base_epi(c, EPI_U, s.m, s.n);
+    eu.out = c.at<void* const>(s.t_out);
+    eu.out_dtype = P.out_f32 ? PRECOND_F32 : P.dtype;
+    eu.nonfinite_of = c.at<const int>(s.t_roots2);
+    const int* lsl = c.at<const int>(s.t_lslot);
+    const int* rsl = c.at<const int>(s.t_rslot);
+    if (s.eng == ENGINE_F64) {
+      ev.C = c.plane(s.VTd);
+      if ((rc = gemm(c, ENGINE_F64, s.Gd, r.Xf, s.m, s.n, s.n, nullptr, rsl, 4, ev, nb))) return rc;
+      if ((rc = gemm(c, ENGINE_F64, l.Xf, s.VTd, s.m, s.n, s.m, lsl, nullptr, 4, eu, nb))) return rc;
+    } else {
+      ev.C = c.plane(s.VTq);
+      if ((rc = clear_rowmax(c, s.VTq))) return rc;
+      if ((rc = gemm(c, ENGINE_TC, s.Gq, r.Xf, s.m, s.n, s.n, nullptr, rsl, 4, ev, nb))) return rc;
+      if ((rc = slice(c, s.VTq))) return rc;
+      if ((rc = gemm(c, ENGINE_TC, l.Xf, s.VTq, s.m, s.n, s.m, lsl, nullptr, 4, eu, nb))) return rc;
+    }
+  }
+  if ((rc = record(h, 4, st))) return rc;
+  return PRECOND_OK;
+}
+
+int run_inv_root(precond_ctx* h, const Plan& P, float eps, cudaStream_t st) {
+  Ctx c{h, P, (char*)h->ws, st};
+  int rc;
+  CK(cudaMemsetAsync(c.ws + P.stats, 0, sizeof(RootStat) * P.nroots + 64, st));
+  if ((rc = record(h, 0, st))) return rc;
+  if ((rc = record(h, 1, st))) return rc;
+  if ((rc = launch_roots_start(c, eps))) return rc;
+  if ((rc = record(h, 2, st))) return rc;
+  if ((rc = launch_iterations(c))) return rc;
+  if ((rc = record(h, 3, st))) return rc;
+  if ((rc = launch_finish(c, eps))) return rc;
+  if ((rc = record(h, 4, st))) return rc;
+  return PRECOND_OK;
+}
+
+int prepare_device(precond_ctx* h) {
+  CK(cudaSetDevice(h->device));
+  if (!h->tc_attr_set) {
+    CK(cudaFuncSetAttribute(gemm_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<4>::BYTES));
+    CK(cudaFuncSetAttribute(gemm_tc_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<3>::BYTES));
+    h->tc_attr_set = true;
+  }
+  return PRECOND_OK;
+}
+
+void remember(precond_ctx* h, const Plan& P, cudaStream_t st) {
+  h->last_stream = st;
+  h->last_nroots = P.nroots;
+  h->last_p = P.p;
+  h->have_last = true;
+  h->last_root_d.assign(P.nroots, 0);
+  h->last_root_class.assign(P.nroots, -1);
+  h->last_root_slot.assign(P.nroots, -1);
+  for (size_t ci = 0; ci < P.rc.size(); ++ci)
+    for (size_t j = 0; j < P.rc[ci].roots.size(); ++j) {
+      const int r = P.rc[ci].roots[j];
+      h->last_root_d[r] = P.rc[ci].d;
+      h->last_root_class[r] = (int)ci;
+      h->last_root_slot[r] = (int)j;
+    }
+  h->last_plan = P;
+}
+
+}  // namespace
+
+// =========================================================================== C ABI
+extern "C" {
+
+int precond_create(precond_t* out, int cuda_device) {
+  if (!out || cuda_device < -1) return PRECOND_EINVAL;
+  *out = nullptr;
+  precond_ctx* h = new precond_ctx();
+  h->device = cuda_device;
+  if (cuda_device >= 0) {
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess || cuda_device >= n) {
+      cudaGetLastError();
+      delete h;
+      return PRECOND_ECUDA;
+    }
+    if (cudaSetDevice(cuda_device) != cudaSuccess || cudaEventCreateWithFlags(&h->upload_done, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      delete h;
+      return PRECOND_ECUDA;
+    }
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+      cudaGetLastError();
+      cudaEventDestroy(h->upload_done);
+      delete h;
+      return PRECOND_ECUDA;
+    }
+    h->encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *out = h;
+  return PRECOND_OK;
+}
+
+int precond_destroy(precond_t h) {
+  if (!h) return PRECOND_OK;
+  if (h->device >= 0) {
+    cudaSetDevice(h->device);
+    cudaDeviceSynchronize();
+    if (h->ws) cudaFree(h->ws);
+    if (h->pinned) cudaFreeHost(h->pinned);
+    if (h->upload_done) cudaEventDestroy(h->upload_done);
+    if (h->events)
+      for (auto& e : h->ev) cudaEventDestroy(e);
+  }
+  delete h;
+  return PRECOND_OK;
+}
+
+int precond_set_option(precond_t h, int key, double v) {
+  if (!h) return PRECOND_EINVAL;
+  switch (key) {
+    case PRECOND_OPT_TOL:
+      if (!(v > 0) || !std::isfinite(v)) return PRECOND_EINVAL;
+      h->tol = v;
+      return PRECOND_OK;
+    case PRECOND_OPT_MAX_ITER:
+      if (v < 0 || v > 1000 || v != std::floor(v)) return PRECOND_EINVAL;
+      h->max_iter = (int)v;
+      return PRECOND_OK;
+    case PRECOND_OPT_MIN_ITER:
+      if (v < 1 || v > 1000 || v != std::floor(v)) return PRECOND_EINVAL;
+      h->min_iter = (int)v;
+      return PRECOND_OK;
+    case PRECOND_OPT_ENGINE:
+      if (v != 0 && v != 1 && v != 2) return PRECOND_EINVAL;
+      h->engine = (int)v;
+      return PRECOND_OK;
+    case PRECOND_OPT_SMALL_DIM:
+      if (v < 0 || v > 1e9 || v != std::floor(v)) return PRECOND_EINVAL;
+      h->small_dim = (int)v;
+      return PRECOND_OK;
+    case PRECOND_OPT_WORKSPACE_MAX:
+      if (v < 0 || !std::isfinite(v)) return PRECOND_EINVAL;
+      h->ws_max = v;
+      return PRECOND_OK;
+    case PRECOND_OPT_TIMING:
+      if (v != 0 && v != 1) return PRECOND_EINVAL;
+      if (v == 1 && h->device >= 0 && !h->events) {
+        for (auto& e : h->ev)
+          if (cudaEventCreate(&e) != cudaSuccess) return PRECOND_ECUDA;
+        h->events = true;
+      }
+      h->timing = (int)v;
+      return PRECOND_OK;
+    case PRECOND_OPT_USE_GRAPH:
+      if (v != 0 && v != 1) return PRECOND_EINVAL;
+      h->use_graph = (int)v;
+      return PRECOND_OK;
+  }
+  return PRECOND_EINVAL;
+}
+
+int precond_step(precond_t h, int count, void* const grads[], int grad_dtype, const int64_t shapes[],
+                 float* const L[], float* const R[], float beta, float eps, float power,
+                 float* const out_f32[], void* stream) {
+  if (!h || count < 1 || !grads || !shapes || !L || !R) return PRECOND_EINVAL;
+  if (grad_dtype != PRECOND_F32 && grad_dtype != PRECOND_BF16) return PRECOND_EINVAL;
+  if (!(beta >= 0.f && beta < 1.f)) return PRECOND_EINVAL;
+  if (!(eps > 0.f) || !std::isfinite(eps)) return PRECOND_EINVAL;
+  int p;
+  if (check_power(power, &p)) return PRECOND_EINVAL;
+  std::vector<const void*> state;
+  for (int i = 0; i < count; ++i) {
+    if (shapes[2 * i] < 1 || shapes[2 * i + 1] < 1 || shapes[2 * i] > (1 << 20) || shapes[2 * i + 1] > (1 << 20))
+      return PRECOND_EINVAL;
+    if (!grads[i] || !L[i] || !R[i] || (out_f32 && !out_f32[i])) return PRECOND_EINVAL;
+    state.push_back(L[i]);
+    state.push_back(R[i]);
+  }
+  std::vector<const void*> sorted = state;
+  std::sort(sorted.begin(), sorted.end());
+  if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end()) return PRECOND_EINVAL;
+  Plan P;
+  int rc = build_plan(h, P, true, count, shapes, grad_dtype, eps, p, grads, L, R, out_f32, nullptr, nullptr);
+  if (rc) return rc;
+  if (h->ws_max > 0 && (double)P.total > h->ws_max) return PRECOND_ENOMEM;
+  if (h->device < 0) return PRECOND_ENODEV;
+  if ((rc = prepare_device(h))) return rc;
+  if ((rc = ensure_workspace(h, P.total))) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((rc = upload_meta(h, P, st))) return rc;
+  if ((rc = run_step(h, P, beta, eps, st))) return rc;
+  remember(h, P, st);
+  return PRECOND_OK;
+}
+
+int precond_inv_root(precond_t h, int count, const float* const A[], const int64_t dims[], float eps,
+                     float power, float* const X[], void* stream) {
+  if (!h || count < 1 || !A || !dims || !X) return PRECOND_EINVAL;
+  if (!(eps > 0.f) || !std::isfinite(eps)) return PRECOND_EINVAL;
+  int p;
+  if (check_power(power, &p)) return PRECOND_EINVAL;
+  for (int i = 0; i < count; ++i) {
+    if (dims[i] < 1 || dims[i] > (1 << 20) || !A[i] || !X[i]) return PRECOND_EINVAL;
+    if ((const void*)A[i] == (const void*)X[i]) return PRECOND_EINVAL;
+  }
+  Plan P;
+  int rc = build_plan(h, P, false, count, dims, PRECOND_F32, eps, p, nullptr, nullptr, nullptr, nullptr, A, X);
+  if (rc) return rc;
+  if (h->ws_max > 0 && (double)P.total > h->ws_max) return PRECOND_ENOMEM;
+  if (h->device < 0) return PRECOND_ENODEV;
+  if ((rc = prepare_device(h))) return rc;
+  if ((rc = ensure_workspace(h, P.total))) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((rc = upload_meta(h, P, st))) return rc;
+  if ((rc = run_inv_root(h, P, eps, st))) return rc;
+  remember(h, P, st);
+  return PRECOND_OK;
+}
+
+int precond_get_stats(precond_t h, int nroots, int iters[], float resid[], int status[], float scale[]) {
+  if (!h) return PRECOND_EINVAL;
+  if (h->device < 0) return PRECOND_ENODEV;
+  if (!h->have_last || nroots != h->last_nroots) return PRECOND_EINVAL;
+  CK(cudaSetDevice(h->device));
+  CK(cudaStreamSynchronize(h->last_stream));
+  std::vector<RootStat> st(nroots);
+  unsigned int err = 0;
+  CK(cudaMemcpy(st.data(), (char*)h->ws + h->last_plan.stats, sizeof(RootStat) * nroots, cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(&err, (char*)h->ws + h->last_plan.err, sizeof(err), cudaMemcpyDeviceToHost));
+  for (int r = 0; r < nroots; ++r) {
+    if (iters) iters[r] = st[r].iters;
+    if (resid) resid[r] = (float)st[r].resid;
+    if (status) status[r] = st[r].status;
+    if (scale) scale[r] = (float)st[r].c;
+  }
+  if (err) {
+    fprintf(stderr, "libprecond: a device wait timed out (error word %u)\n", err);
+    return PRECOND_ECUDA;
+  }
+  return PRECOND_OK;
+}
+
+int precond_get_timing(precond_t h, double ms[4], int64_t* ns_gemm_launches, double* ns_flops) {
+  if (!h) return PRECOND_EINVAL;
+  if (h->device < 0) return PRECOND_ENODEV;
+  if (!h->have_last || !h->timing || !h->events) return PRECOND_EINVAL;
+  CK(cudaEventSynchronize(h->ev[4]));
+  if (ms)
+    for (int i = 0; i < 4; ++i) {
+      float t = 0.f;
+      CK(cudaEventElapsedTime(&t, h->ev[i], h->ev[i + 1]));
+      ms[i] = t;
+    }
+  if (ns_gemm_launches) *ns_gemm_launches = h->ns_launches;
+  if (ns_flops) {
+    std::vector<RootStat> st(h->last_nroots);
+    CK(cudaMemcpy(st.data(), (char*)h->ws + h->last_plan.stats, sizeof(RootStat) * h->last_nroots,
+                  cudaMemcpyDeviceToHost));
+    const int g = h->last_p == 4 ? 4 : 3;
+    double f = 0;
+    for (int r = 0; r < h->last_nroots; ++r) {
+      const double d = h->last_root_d[r];
+      if (st[r].iters > 0) f += 2.0 * d * d * d * (double)(st[r].iters * g - 1);
+    }
+    *ns_flops = f;
+  }
+  return PRECOND_OK;
+}
+
+int64_t precond_launch_count(precond_t h) { return h ? h->launches : -1; }
+
+const char* precond_error_string(int code) {
+  switch (code) {
+    case PRECOND_OK: return "ok";
+    case PRECOND_EINVAL: return "invalid argument";
+    case PRECOND_ENOMEM: return "workspace allocation failed or exceeds the limit";
+    case PRECOND_ECUDA: return "CUDA error";
+    case PRECOND_ENODEV: return "host-only handle: no device";
+    case PRECOND_ENOTCONV: return "iteration did not reach the tolerance";
+    case PRECOND_ENONFINITE: return "non-finite input";
+  }
+  return "unknown status";
+}
+
+// Test / debug read-back: the fp32 root of root `r` of the last step call
+// (X_L for root 2i, X_R for root 2i+1) into a d x d device buffer.
+int precond_get_root(precond_t h, int r, float* dst, void* stream) {
+  if (!h || !dst) return PRECOND_EINVAL;
+  if (h->device < 0) return PRECOND_ENODEV;
+  if (!h->have_last || r < 0 || r >= h->last_nroots) return PRECOND_EINVAL;
+  const RootClass& rc = h->last_plan.rc[h->last_root_class[r]];
+  const int slot = h->last_root_slot[r];
+  Plane p = digits_plane((char*)h->ws, rc.Xf);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (rc.eng == ENGINE_F64) plane_to_f32_kernel<ENGINE_F64><<<256, 256, 0, st>>>(p, slot, rc.d, rc.d, dst);
+  else plane_to_f32_kernel<ENGINE_TC><<<256, 256, 0, st>>>(p, slot, rc.d, rc.d, dst);
+  h->launches++;
+  CK(cudaGetLastError());
+  return PRECOND_OK;
+}
+
+// Diagnostic read-back of a work matrix of root `r` of the last call:
+// which = 0/1 X[0]/X[1], 2/3 M[0]/M[1], 4/5 T[0]/T[1], 6 T2, 7 T4, 8 final X.
+int precond_debug_plane(precond_t h, int r, int which, float* dst, void* stream) {
+  if (!h || !dst || which < 0 || which > 8) return PRECOND_EINVAL;
+  if (h->device < 0) return PRECOND_ENODEV;
+  if (!h->have_last || r < 0 || r >= h->last_nroots) return PRECOND_EINVAL;
+  const RootClass& rc = h->last_plan.rc[h->last_root_class[r]];
+  const Slab* sl[9] = {&rc.X[0], &rc.X[1], &rc.M[0], &rc.M[1], &rc.T[0], &rc.T[1], &rc.T2, &rc.T4, &rc.Xf};
+  const Slab& S = *sl[which];
+  if (S.batch == 0) return PRECOND_EINVAL;
+  Plane p = digits_plane((char*)h->ws, S);
+  if (S.f32) p.f32 = reinterpret_cast<float*>((char*)h->ws + S.f32);   // per-row matrices: read the fp32 form
+  cudaStream_t st = (cudaStream_t)stream;
+  const int slot = h->last_root_slot[r];
+  if (rc.eng == ENGINE_F64) plane_to_f32_kernel<ENGINE_F64><<<256, 256, 0, st>>>(p, slot, rc.d, rc.d, dst);
+  else plane_to_f32_kernel<ENGINE_TC><<<256, 256, 0, st>>>(p, slot, rc.d, rc.d, dst);
+  CK(cudaGetLastError());
+  return PRECOND_OK;
+}
+
+// Self-test of the GEMM core: C = A . B^T (A: M x K, B: N x K, C: M x N, fp32
+// device buffers) through one engine's batched GEMM with a plain store.
+int precond_gemm_selftest(precond_t h, int engine, int M, int N, int K, const float* A, const float* B, float* C,
+                          int passes, void* stream) {
+  if (!h || !A || !B || !C || M < 1 || N < 1 || K < 1 || (engine != 1 && engine != 2)) return PRECOND_EINVAL;
+  if (passes != 3 && passes != 4) return PRECOND_EINVAL;
+  if (h->device < 0) return PRECOND_ENODEV;
+  int rc;
+  if ((rc = prepare_device(h))) return rc;
+  const int eng = engine == 1 ? ENGINE_F64 : ENGINE_TC;
+  Layout L;
+  Plan P;
+  P.stats = L.take(sizeof(RootStat));
+  P.err = L.take(64);
+  Slab sa = make_slab(L, eng, 1, M, K, 4, true), sb = make_slab(L, eng, 1, N, K, 4, true);
+  Slab sc = make_slab(L, eng, 1, M, N, 4, true);
+  if ((rc = ensure_workspace(h, L.top))) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  Ctx c{h, P, (char*)h->ws, st};
+  CK(cudaMemsetAsync(c.ws + P.stats, 0, sizeof(RootStat) + 64, st));
+  if (eng == ENGINE_F64) {
+    f32_to_plane_kernel<ENGINE_F64><<<256, 256, 0, st>>>(A, c.plane(sa), M, K);
+    f32_to_plane_kernel<ENGINE_F64><<<256, 256, 0, st>>>(B, c.plane(sb), N, K);
+  } else {
+    if ((rc = clear_rowmax(c, sa)) || (rc = clear_rowmax(c, sb))) return rc;
+    f32_to_plane_kernel<ENGINE_TC><<<256, 256, 0, st>>>(A, c.plane(sa), M, K);
+    f32_to_plane_kernel<ENGINE_TC><<<256, 256, 0, st>>>(B, c.plane(sb), N, K);
+    if ((rc = slice(c, sa)) || (rc = slice(c, sb))) return rc;
+  }
+  Epi e = base_epi(c, EPI_STORE, M, N);
+  e.C = c.plane(sc);
+  if ((rc = gemm(c, eng, sa, sb, M, N, K, nullptr, nullptr, passes, e, 1))) return rc;
+  if (eng == ENGINE_F64) plane_to_f32_kernel<ENGINE_F64><<<256, 256, 0, st>>>(c.plane(sc), 0, M, N, C);
+  else plane_to_f32_kernel<ENGINE_TC><<<256, 256, 0, st>>>(c.plane(sc), 0, M, N, C);
+  CK(cudaGetLastError());
+  CK(cudaStreamSynchronize(st));
+  unsigned int err = 0;
+  CK(cudaMemcpy(&err, c.ws + P.err, sizeof(err), cudaMemcpyDeviceToHost));
+  return err ? PRECOND_ECUDA : PRECOND_OK;
+}
+
+}  // extern "C"

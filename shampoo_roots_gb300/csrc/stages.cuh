@@ -1,0 +1,390 @@
+// Element-wise and reduction stages of the preconditioner step:
+// gradient preparation, Gram statistics, the largest-eigenvalue bound, the
+// start of the iteration and its finish.  All O(d^2), HBM-bound.
+#pragma once
+
+#include "engine.cuh"
+
+namespace precond {
+
+// ---------------------------------------------------------------------------
+// Gradient preparation
+// ---------------------------------------------------------------------------
+struct PrepArgs {
+  const void* const* g;   // per batch entry: caller's gradient (m x n)
+  int dtype;
+  int m, n;
+  const int* roots2;      // per batch entry: the two root ids (left, right)
+  RootStat* stats;
+  MatStat* mstat;
+  // fp64 engine outputs
+  double* Gd; double* GTd;            // [b][m][n], [b][n][m]
+  // tcgen05 engine outputs: fp32 copies (rows padded to ld) and row maxima
+  float* Gf; int ldn;                 // [b][m][ldn]
+  float* GTf; int ldm;                // [b][n][ldm]
+  float* rowmax_G;                    // [b][m]   max_j |G_ij|
+  float* rowmax_GT;                   // [b][n]   max_i |G_ij|
+};
+
+__device__ __forceinline__ float pow2_scale(float target, float maxabs) {
+  // largest power of two s with maxabs * s <= target (1 when maxabs is 0)
+  if (!(maxabs > 0.0f) || !isfinite(maxabs)) return 1.0f;
+  int e;
+  frexpf(target / maxabs, &e);     // target/maxabs = f * 2^e, f in [0.5, 1)
+  return ldexpf(1.0f, e - 1);
+}
+
+// Per batch entry: max |G|, max row sum of squares, non-finite check.
+__global__ void __launch_bounds__(256) prep_reduce_kernel(PrepArgs a) {
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const void* g = a.g[b];
+  float gmax = 0.f, rmax = 0.f;
+  int bad = 0;
+  for (int r = blockIdx.x * 8 + warp; r < a.m; r += gridDim.x * 8) {
+    float s2 = 0.f, mx = 0.f;
+    for (int c = lane; c < a.n; c += 32) {
+      const float v = load_grad(g, a.dtype, (long long)r * a.n + c);
+      if (!isfinite(v)) bad = 1;
+      s2 = fmaf(v, v, s2);
+      mx = fmaxf(mx, fabsf(v));
+    }
+    s2 = warp_sum(s2);
+    mx = warp_max(mx);
+    rmax = fmaxf(rmax, s2);
+    gmax = fmaxf(gmax, mx);
+    if (a.rowmax_G && lane == 0) a.rowmax_G[(long long)b * a.m + r] = isfinite(mx) ? mx : 0.f;
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    if (isfinite(gmax)) atomic_max_nonneg(&a.mstat[b].gmax, gmax);
+    if (isfinite(rmax)) atomic_max_nonneg(&a.mstat[b].rownorm2_max, rmax);
+    if (bad) {
+      a.stats[a.roots2[2 * b]].nonfinite = 1;
+      a.stats[a.roots2[2 * b + 1]].nonfinite = 1;
+    }
+  }
+}
+
+// 32 x 32 tiles: writes the engine copies of G and G^T.
+template <int E>
+__global__ void __launch_bounds__(256) prep_split_kernel(PrepArgs a) {
+  __shared__ float tile[32][33];
+  __shared__ float cmax[8][32];
+  const int b = blockIdx.z;
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  const void* g = a.g[b];
+  float cm = 0.f;
+  for (int q = ty; q < 32; q += 8) {
+    const int r = r0 + q, c = c0 + tx;
+    float v = 0.f;
+    if (r < a.m && c < a.n) {
+      v = load_grad(g, a.dtype, (long long)r * a.n + c);
+      if constexpr (E == ENGINE_F64) a.Gd[((long long)b * a.m + r) * a.n + c] = (double)v;
+      else a.Gf[((long long)b * a.m + r) * a.ldn + c] = v;
+    }
+    tile[q][tx] = v;
+    if (isfinite(v)) cm = fmaxf(cm, fabsf(v));
+  }
+  if constexpr (E == ENGINE_TC) {
+    cmax[ty][tx] = cm;
+    __syncthreads();
+    if (ty == 0 && c0 + tx < a.n) {
+      float m = cmax[0][tx];
+      for (int q = 1; q < 8; ++q) m = fmaxf(m, cmax[q][tx]);
+      atomic_max_nonneg(&a.rowmax_GT[(long long)b * a.n + c0 + tx], m);
+    }
+  }
+  __syncthreads();
+  for (int q = ty; q < 32; q += 8) {
+    const int c = c0 + q, r = r0 + tx;   // output row c of G^T, column r
+    if (c < a.n && r < a.m) {
+      const float v = tile[tx][q];
+      if constexpr (E == ENGINE_F64) a.GTd[((long long)b * a.n + c) * a.m + r] = (double)v;
+      else a.GTf[((long long)b * a.n + c) * a.ldm + r] = v;
+    }
+  }
+}
+
+// fp32 rows -> per-row-scaled digits: sigma_i = smallest power of two >= max_j |x_ij|.
+struct SliceArgs {
+  const float* src; long long src_bstride; int src_ld;
+  const float* rowmax;      // [b][rows]
+  float* rowscale;          // [b][rows] out
+  Plane dst;                // digit form (scale unused)
+  int rows, cols;
+};
+
+__device__ __forceinline__ float pow2_ceil(float x) {
+  if (!(x > 0.f) || !isfinite(x)) return 1.f;
+  int e;
+  const float f = frexpf(x, &e);          // x = f 2^e, f in [0.5, 1)
+  return f == 0.5f ? x : ldexpf(1.f, e);
+}
+
+__global__ void __launch_bounds__(256) slice_rows_kernel(SliceArgs a) {
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = blockIdx.x * 8 + warp; r < a.rows; r += gridDim.x * 8) {
+    const double sigma = (double)pow2_ceil(a.rowmax[(long long)b * a.rows + r]);
+    if (lane == 0) a.rowscale[(long long)b * a.rows + r] = (float)sigma;
+    const float* src = a.src + (long long)b * a.src_bstride + (long long)r * a.src_ld;
+    const long long o = (long long)b * a.dst.bstride + (long long)r * a.dst.ld;
+    for (int c = lane; c < a.cols; c += 32) digits_store(a.dst, o + c, (double)src[c], sigma);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Statistics of each root's source matrix (the Gram after the EMA, or a given
+// SPD matrix): trace, squared Frobenius norm, absolute row sums.
+// ---------------------------------------------------------------------------
+struct RootArgs {
+  const float* const* src;   // per batch entry: fp32 d x d source (caller's L / R / A)
+  const int* root_of;        // batch entry -> root id
+  RootStat* stats;
+  double* rowabs;            // [b][d]  sum_j |src_ij|
+  double* diag;              // [b][d]  src_ii
+  double* rowsq;             // [b][d]  sum_j src_ij^2
+  int d;
+  float eps;
+  IterCtl ctl;
+  // engine planes
+  Plane M0, T0, X1;          // init outputs
+  Plane X[2];                // finalize input (X buffer kfinal & 1)
+  const float* xscale;       // tcgen05 engine: digit scale of X_k by k (device table), or null
+  Plane Xf;                  // finalize output in engine format (step), or unused
+  float* const* dst;         // finalize output to caller fp32 (inv_root), or null
+};
+
+__global__ void __launch_bounds__(256) root_stats_kernel(RootArgs a) {
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* A = a.src[b];
+  RootStat* st = &a.stats[a.root_of[b]];
+  int bad = 0;
+  for (int r = blockIdx.x * 8 + warp; r < a.d; r += gridDim.x * 8) {
+    double s1 = 0.0, s2 = 0.0;
+    for (int c = lane; c < a.d; c += 32) {
+      const double v = A[(long long)r * a.d + c];
+      if (!isfinite(v)) bad = 1;
+      s1 += fabs(v);
+      s2 += v * v;
+    }
+    s1 = warp_sum(s1);
+    s2 = warp_sum(s2);
+    if (lane == 0) {
+      const long long o = (long long)b * a.d + r;
+      a.rowabs[o] = s1;
+      a.rowsq[o] = s2;
+      a.diag[o] = A[(long long)r * a.d + r];
+    }
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0 && bad) st->nonfinite = 1;
+}
+
+// Fixed-order (deterministic) sum of a per-row vector by one block.
+__device__ double block_vec_sum(const double* v, int n) {
+  double s = 0.0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) s += v[i];
+  s = block_sum(s);
+  __shared__ double out;
+  if (threadIdx.x == 0) out = s;
+  __syncthreads();
+  return out;
+}
+
+// Minc's bound on A_hat = src / tr + eps I:  max_i (|A_hat| r)_i / r_i, r = |A_hat| 1.
+__global__ void __launch_bounds__(256) root_bound_kernel(RootArgs a) {
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* A = a.src[b];
+  RootStat* st = &a.stats[a.root_of[b]];
+  const double t = block_vec_sum(a.diag + (long long)b * a.d, a.d);
+  if (blockIdx.x == 0) {
+    const double f2 = block_vec_sum(a.rowsq + (long long)b * a.d, a.d);
+    if (threadIdx.x == 0) {
+      st->trace = t;
+      st->frob2 = f2;
+    }
+  }
+  if (!(t > 0.0) || !isfinite(t)) return;
+  const double it = 1.0 / t, eps = (double)a.eps;
+  const double* ra = a.rowabs + (long long)b * a.d;
+  const double* dg = a.diag + (long long)b * a.d;
+  double best = 0.0;
+  for (int r = blockIdx.x * 8 + warp; r < a.d; r += gridDim.x * 8) {
+    double y = 0.0;
+    for (int c = lane; c < a.d; c += 32) {
+      const double v = A[(long long)r * a.d + c];
+      const double dc = dg[c];
+      const double rc = (ra[c] - fabs(dc)) * it + fabs(dc * it + eps);   // row sum of |A_hat|, row c
+      const double ahat = (c == r) ? fabs(v * it + eps) : fabs(v) * it;
+      y += ahat * fmax(rc, 1e-12);
+    }
+    y = warp_sum(y);
+    const double dr = dg[r];
+    const double rr = fmax((ra[r] - fabs(dr)) * it + fabs(dr * it + eps), 1e-12);
+    best = fmax(best, y / rr);
+  }
+  if (lane == 0 && isfinite(best)) atomic_max_nonneg(&st->minc, best);
+}
+
+__device__ __forceinline__ double root_scale(const RootStat& st, int d, double eps) {
+  // Wolkowicz-Styan on A_hat: mu = tr/d, s^2 = ||A_hat||_F^2/d - mu^2, mu + s sqrt(d-1)
+  const double t = st.trace;
+  const double fro2 = st.frob2 / (t * t) + 2.0 * eps + (double)d * eps * eps;
+  const double mu = (1.0 + (double)d * eps) / (double)d;
+  const double s2 = fmax(fro2 / (double)d - mu * mu, 0.0);
+  const double ws = mu + sqrt(s2) * sqrt((double)(d - 1));
+  return 1.01 * fmin(ws, st.minc);
+}
+
+// M_0 = A_hat / c, T_0 = ((p+1) I - M_0) / p, X_1 = X_0 T_0 = T_0.
+template <int E>
+__global__ void __launch_bounds__(256) root_init_kernel(RootArgs a) {
+  const int b = blockIdx.z;
+  RootStat* st = &a.stats[a.root_of[b]];
+  const double t = st->trace, eps = (double)a.eps;
+  const double c = root_scale(*st, a.d, eps);
+  const bool bad = st->nonfinite || !(t > 0.0) || !isfinite(t) || !isfinite(c) || !(c > 0.0);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    st->c = c;
+    st->resid = 1e300;
+    st->iters = 0;
+    st->kfinal = 0;
+    st->done = bad ? 1 : 0;
+    st->status = bad ? PRECOND_ENONFINITE : PRECOND_OK;
+  }
+  if (bad) return;
+  const float* A = a.src[b];
+  const double p = (double)a.ctl.p;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int q = ty; q < 32; q += 8) {
+    const int r = r0 + q, col = c0 + tx;
+    float mx = 0.f;
+    if (r < a.d && col < a.d) {
+      const double id = (r == col) ? 1.0 : 0.0;
+      const double m0 = ((double)A[(long long)r * a.d + col] / t + eps * id) / c;
+      const double t0 = ((p + 1.0) * id - m0) / p;
+      plane_store<E>(a.M0, b, r, col, m0);
+      plane_store<E>(a.T0, b, r, col, t0);
+      plane_store<E>(a.X1, b, r, col, t0);
+      mx = (float)fabs(m0);
+    }
+    if (E == ENGINE_TC && a.M0.rowmax) {
+      mx = warp_max(mx);
+      if (tx == 0 && r < a.d) atomic_max_nonneg(&a.M0.rowmax[(long long)b * a.d + r], mx);
+    }
+  }
+}
+
+// Result = sym(X_kfinal) * c^(-1/p): to the engine plane Xf (step) or caller fp32 (inv_root).
+template <int E>
+__global__ void __launch_bounds__(256) root_finish_kernel(RootArgs a) {
+  __shared__ double tile[32][33];
+  const int b = blockIdx.z;
+  const RootStat* st = &a.stats[a.root_of[b]];
+  if (st->status == PRECOND_ENONFINITE || st->kfinal < 1) return;
+  Plane X = a.X[st->kfinal & 1];
+  if (E == ENGINE_TC && a.xscale) X.scale = a.xscale[st->kfinal];
+  const double f = pow(st->c, -1.0 / (double)a.ctl.p);
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  // load the transposed tile (rows c0.., cols r0..)
+  for (int q = ty; q < 32; q += 8) {
+    const int r = c0 + q, col = r0 + tx;
+    tile[q][tx] = (r < a.d && col < a.d) ? plane_load<E>(X, b, r, col) : 0.0;
+  }
+  __syncthreads();
+  for (int q = ty; q < 32; q += 8) {
+    const int r = r0 + q, col = c0 + tx;
+    if (r >= a.d || col >= a.d) continue;
+    const double v = 0.5 * (plane_load<E>(X, b, r, col) + tile[tx][q]) * f;
+    if (a.dst) a.dst[b][(long long)r * a.d + col] = (float)v;
+    else plane_store<E>(a.Xf, b, r, col, v);
+  }
+}
+
+// Caller fp32 -> engine plane (GEMM self-test inputs).
+template <int E>
+__global__ void f32_to_plane_kernel(const float* src, Plane p, int rows, int cols) {
+  const long long n = (long long)rows * cols;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    plane_store<E>(p, 0, i / cols, i % cols, (double)src[i]);
+    if (E == ENGINE_TC && p.rowmax) atomic_max_nonneg(&p.rowmax[i / cols], fabsf(src[i]));
+  }
+}
+
+// After M_{k+1} = T^p M_k (tcgen05 engine): M <- (M + M^T) / 2 in place (M is
+// symmetric in exact arithmetic, and the iteration amplifies any antisymmetric
+// rounding by up to ((p+1)/p)^p per step), T_{k+1} = ((p+1) I - M) / p as
+// fixed-scale digits, and the row maxima for slicing M.  Each block handles a
+// pair of mirrored 32 x 32 tiles (bx <= by).
+struct SymArgs {
+  Plane M;          // fp32 form (f32, rowmax)
+  Plane T;          // digit form
+  const int* root_of;
+  const RootStat* stats;
+  int d, p;
+};
+
+__global__ void __launch_bounds__(256) sym_m_kernel(SymArgs a) {
+  const int bx = blockIdx.x, by = blockIdx.y, b = blockIdx.z;
+  if (bx > by) return;
+  if (a.stats[a.root_of[b]].done) return;
+  __shared__ float ta[32][33], tb[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  float* M = a.M.f32 + (long long)b * a.M.bstride;
+  const int ld = a.M.ld;
+  const int ra = by * 32, ca = bx * 32;      // tile A rows ra.., cols ca..; tile B = mirrored
+  for (int q = ty; q < 32; q += 8) {
+    const int r = ra + q, c = ca + tx;
+    ta[q][tx] = (r < a.d && c < a.d) ? M[(long long)r * ld + c] : 0.f;
+    const int r2 = ca + q, c2 = ra + tx;
+    tb[q][tx] = (r2 < a.d && c2 < a.d) ? M[(long long)r2 * ld + c2] : 0.f;
+  }
+  __syncthreads();
+  const double pp = (double)a.p;
+  // tile A: element (q, tx) = (ta[q][tx] + tb[tx][q]) / 2
+  for (int q = ty; q < 32; q += 8) {
+    const int r = ra + q, c = ca + tx;
+    float mx = 0.f;
+    if (r < a.d && c < a.d) {
+      const double m = 0.5 * ((double)ta[q][tx] + (double)tb[tx][q]);
+      M[(long long)r * ld + c] = (float)m;
+      plane_store<ENGINE_TC>(a.T, b, r, c, ((pp + 1.0) * (r == c ? 1.0 : 0.0) - m) / pp);
+      mx = (float)fabs(m);
+    }
+    mx = warp_max(mx);
+    if (tx == 0 && r < a.d) atomic_max_nonneg(&a.M.rowmax[(long long)b * a.d + r], mx);
+  }
+  if (bx == by) return;
+  // tile B (rows ca.., cols ra..): element (q, tx) = (tb[q][tx] + ta[tx][q]) / 2
+  for (int q = ty; q < 32; q += 8) {
+    const int r = ca + q, c = ra + tx;
+    float mx = 0.f;
+    if (r < a.d && c < a.d) {
+      const double m = 0.5 * ((double)tb[q][tx] + (double)ta[tx][q]);
+      M[(long long)r * ld + c] = (float)m;
+      plane_store<ENGINE_TC>(a.T, b, r, c, ((pp + 1.0) * (r == c ? 1.0 : 0.0) - m) / pp);
+      mx = (float)fabs(m);
+    }
+    mx = warp_max(mx);
+    if (tx == 0 && r < a.d) atomic_max_nonneg(&a.M.rowmax[(long long)b * a.d + r], mx);
+  }
+}
+
+// Engine plane -> caller fp32 (debug / test read-back of a root).
+template <int E>
+__global__ void plane_to_f32_kernel(Plane p, int b, int rows, int cols, float* dst) {
+  const long long n = (long long)rows * cols;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / cols, c = i % cols;
+    dst[i] = (float)plane_load<E>(p, b, r, c);
+  }
+}
+
+}  // namespace precond

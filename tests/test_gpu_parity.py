@@ -1,0 +1,157 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle,
+element by element (relative Frobenius error <= 1e-3 on the fp32 path)."""
+import numpy as np
+import pytest
+
+from gpu_common import TOL, run_steps, to_dev
+from oracle import roots as oracle
+from workloads import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def test_single_256x128_full_size():
+    w = synth.workload(0)
+    G = synth.gradients_for_step(w, 0)
+    worst, (it, res, status, scale) = run_steps(list(w.shapes), [G], w.dtype, w.beta, w.eps, -0.25)
+    assert all(s == 0 for s in status), status
+    assert max(worst.values()) <= TOL, worst
+    # start scale c = 1.01 x the bound of the oracle's rescaled, regularised Gram
+    st = oracle.OracleState(list(w.shapes))
+    Lo, Ro = oracle.gram_ema(st.L[0], st.R[0], G[0].astype(np.float64), w.beta)
+    for k, A in enumerate((Lo, Ro)):
+        Ah = oracle.trace_normalise(A) + w.eps * np.eye(A.shape[0])
+        assert abs(scale[k] / (1.01 * oracle.lambda_max_bound(Ah)) - 1) < 1e-5
+
+
+@pytest.mark.parametrize("engine", [1, 2])
+@pytest.mark.parametrize("power", [-0.25, -0.5])
+def test_ragged_shapes_both_engines(engine, power):
+    """Sizes that leave ragged tiles in both engines (tile 64 / 128 x 256)."""
+    shapes = [(300, 130), (130, 300), (257, 257)]
+    rng = [synth.rng_for(9, 0, i) for i in range(3)]
+    G = [synth.gradient(m, n, -0.7, rng[i], synth.F32) for i, (m, n) in enumerate(shapes)]
+    worst, (it, res, status, _) = run_steps(shapes, [G], synth.F32, 0.95, 1e-6, power, engine=engine)
+    assert all(s == 0 for s in status), status
+    assert max(worst.values()) <= TOL, worst
+
+
+def test_stack_bf16_scaled_quarter():
+    """The 24-layer d=1024 stack recipe at 1/4 size (2 layers), 3 EMA steps:
+    256^2 Grams on the fp64 engine, 1024^2 on the tcgen05 engine."""
+    w = synth.scaled(synth.workload(1), 4)
+    shapes = list(w.shapes[:12])
+    steps = [[synth.gradient(m, n, w.alpha, synth.rng_for(1, s, i), w.dtype) for i, (m, n) in enumerate(shapes)]
+             for s in range(3)]
+    worst, (it, res, status, _) = run_steps(shapes, steps, w.dtype, w.beta, w.eps, -0.25)
+    assert all(s == 0 for s in status), status
+    assert max(worst.values()) <= TOL, worst
+
+
+@pytest.mark.parametrize("power", [-0.25, -0.5])
+def test_spd_inv_root_tcgen05(power):
+    """Conditioning-stress recipe (log-uniform spectrum on [1e-8, 1]) at d=1024."""
+    import torch
+    import shampoo_roots_gb300 as sr
+    A = [synth.spd(1024, synth.rng_for(3, 0, i)) for i in range(3)]
+    pc = sr.Preconditioner(0)
+    X = [torch.empty_like(to_dev(a)) for a in A]
+    sr.precond_inv_root(pc.h, [to_dev(a) for a in A], X, 1e-6, power)
+    it, res, status, _ = sr.precond_get_stats(pc.h, len(A))
+    pc.close()
+    assert all(s == 0 for s in status), status
+    for a, x in zip(A, X):
+        err = oracle.rel_fro(x.cpu().numpy(), oracle.inv_root(a.astype(np.float64), 1e-6, power))
+        assert err <= TOL, err
+
+
+def test_nonfinite_gradient_flags_and_keeps_state():
+    import torch
+    import shampoo_roots_gb300 as sr
+    pc = sr.Preconditioner(0)
+    g = torch.randn(64, 32, device="cuda")
+    g[3, 5] = float("nan")
+    L = torch.full((64, 64), 0.5, device="cuda")
+    R = torch.full((32, 32), 0.25, device="cuda")
+    out = torch.full((64, 32), 7.0, device="cuda")
+    sr.precond_step(pc.h, [g], [L], [R], 0.9, 1e-6, -0.25, out=[out])
+    it, res, status, _ = sr.precond_get_stats(pc.h, 2)
+    pc.close()
+    assert status == [sr.ENONFINITE, sr.ENONFINITE]
+    assert torch.all(L == 0.5) and torch.all(R == 0.25)
+    assert torch.all(out == 7.0)
+
+
+def test_iteration_cap_reports_notconv_and_writes():
+    import torch
+    import shampoo_roots_gb300 as sr
+    pc = sr.Preconditioner(0, max_iter=1)
+    g = to_dev(synth.gradients_for_step(synth.workload(0), 0)[0])
+    L = torch.zeros(256, 256, device="cuda")
+    R = torch.zeros(128, 128, device="cuda")
+    out = torch.full((256, 128), float("nan"), device="cuda")
+    sr.precond_step(pc.h, [g], [L], [R], 0.95, 1e-6, -0.25, out=[out])
+    it, res, status, _ = sr.precond_get_stats(pc.h, 2)
+    pc.close()
+    assert status == [sr.ENOTCONV, sr.ENOTCONV] and it == [1, 1]
+    assert torch.isfinite(out).all()
+
+
+def test_resume_matches_straight_run():
+    """Run 3 steps, copy the state out and back, run 3 more: identical bits to 6 straight steps."""
+    import torch
+    import shampoo_roots_gb300 as sr
+    shapes = [(96, 160), (600, 520)]
+    grads = [[to_dev(synth.gradient(m, n, -0.7, synth.rng_for(7, s, i), synth.F32)) for i, (m, n) in
+              enumerate(shapes)] for s in range(6)]
+
+    def run(steps, L, R, pc):
+        outs = []
+        for G in steps:
+            o = [torch.empty_like(x) for x in G]
+            sr.precond_step(pc.h, [x.clone() for x in G], L, R, 0.95, 1e-6, -0.25, out=o)
+            outs.append(o)
+        torch.cuda.synchronize()
+        return outs
+
+    pc = sr.Preconditioner(0)
+    L = [torch.zeros(m, m, device="cuda") for m, _ in shapes]
+    R = [torch.zeros(n, n, device="cuda") for _, n in shapes]
+    straight = run(grads, L, R, pc)
+    L2 = [torch.zeros(m, m, device="cuda") for m, _ in shapes]
+    R2 = [torch.zeros(n, n, device="cuda") for _, n in shapes]
+    run(grads[:3], L2, R2, pc)
+    saved = [x.cpu() for x in L2 + R2]
+    pc.close()
+    pc = sr.Preconditioner(0)
+    L3 = [s.cuda() for s in saved[:2]]
+    R3 = [s.cuda() for s in saved[2:]]
+    resumed = run(grads[3:], L3, R3, pc)
+    pc.close()
+    for a, b in zip(straight[3:], resumed):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+    for x, y in zip(L + R, L3 + R3):
+        assert torch.equal(x, y)
+
+
+def test_bf16_in_place_output():
+    import torch
+    import shampoo_roots_gb300 as sr
+    shapes = [(128, 96)]
+    G = [synth.gradient(128, 96, -0.7, synth.rng_for(5, 0, 0), synth.BF16)]
+    g = to_dev(G[0]).to(torch.bfloat16)
+    pc = sr.Preconditioner(0)
+    L = torch.zeros(128, 128, device="cuda")
+    R = torch.zeros(96, 96, device="cuda")
+    sr.precond_step(pc.h, [g], [L], [R], 0.95, 1e-6, -0.5)
+    pc.close()
+    st = oracle.OracleState(shapes)
+    Uo, _, _ = oracle.precond_step(st, [G[0].astype(np.float64)], 0.95, 1e-6, -0.5)
+    want = synth.round_to_bf16(Uo[0])
+    got = g.float().cpu().numpy()
+    # in-place bf16 output: the fp32 U (relative error ~1e-5 of max |U|) rounded
+    # once; near a rounding boundary that is one bf16 step from the rounded oracle
+    ulp = np.abs(want) * 2.0 ** -7
+    assert np.all(np.abs(got - want) <= ulp + 1e-4 * np.abs(Uo[0]).max())
+    assert oracle.rel_fro(got, Uo[0]) <= 2.0 ** -8
