@@ -162,8 +162,8 @@ int precond_gemm_selftest(precond_t h, int engine, int M, int N, int K, const fl
 /*
  * Diagnostic read-back (no counterpart in the method) of a work matrix of
  * root `r` of the last call into a d x d fp32 device buffer:
- * which = 0/1 X buffers, 2/3 M buffers, 4/5 T buffers, 6 T^2, 7 T^4, 8 the
- * final root (step calls).  Iteration k reads buffers k & 1 and writes
+ * which = 0/1 X buffers, 2/3 M buffers, 4 D (the T^2 - tau^2 I term), 5 F
+ * (the T^4 - tau^4 I term, p = 4), 8 the final root (step calls).  Iteration k reads buffers k & 1 and writes
  * (k + 1) & 1.  Enqueued on `stream`.
  */
 int precond_debug_plane(precond_t h, int r, int which, float* dst, void* stream);

@@ -79,19 +79,21 @@ __device__ __forceinline__ double plane_load(const Plane& p, int b, long long i,
 // by the operands' scales, and hands each element to one of these.
 // ---------------------------------------------------------------------------
 enum EpiKind {
-  EPI_STORE = 0,  // C_b = acc                           (X T, T T, T2 T2)
-  EPI_M     = 1,  // M'_b = acc, T'_b = ((p+1) I - M')/p, residual, convergence
+  EPI_STORE = 0,  // C_b = acc
+  EPI_M     = 1,  // M'_b = acc + beta In_b, residual ||M' - I||, convergence
   EPI_GRAM  = 2,  // state_b = beta state_b + (1-beta) acc   (caller's fp32 L or R)
   EPI_VT    = 3,  // C_b^T = acc   (V = G X_R stored transposed for the second product)
   EPI_U     = 4,  // out_b = acc   (caller's fp32 out or the gradient in place)
+  EPI_AFF   = 5,  // C_b = alpha acc + beta In_b + gamma I
 };
 
 struct Epi {
   int kind;
   int rows, cols;            // output extent (M x N of the GEMM)
-  Plane C;                   // EPI_STORE / EPI_M (M') / EPI_VT
-  Plane C2;                  // EPI_M: T'
-  // root bookkeeping (EPI_STORE / EPI_M): batch entry -> root id; skip done roots
+  Plane C;                   // EPI_STORE / EPI_M / EPI_VT / EPI_AFF output
+  Plane In;                  // EPI_M / EPI_AFF element-wise input (same shape as C)
+  double alpha, beta_in, gamma;
+  // root bookkeeping (EPI_STORE / EPI_M / EPI_AFF): batch entry -> root id; skip done roots
   const int* root_of;        // may be null (no skipping)
   RootStat* stats;
   IterCtl ctl;
@@ -106,10 +108,9 @@ struct Epi {
   void* const* out;          // per batch entry: destination (rows x cols)
   int out_dtype;             // PRECOND_F32 or PRECOND_BF16
   const int* nonfinite_of;   // per batch entry: two root ids whose status gates the write
-  // scaling of acc (tcgen05 engine): acc / (scaleA * scaleB); per-matrix scale tables
-  float inv_scale;           // constant part
-  const MatStat* mstat;      // per batch entry scales (EPI_GRAM / EPI_VT / EPI_U; may be null)
-  int scale_mode;            // unused (scales are carried by the digit operands)
+  float inv_scale;           // constant factor on acc
+  const MatStat* mstat;
+  int scale_mode;
 };
 
 __device__ __forceinline__ double epi_matrix_scale(const Epi& e, int b) { return 1.0; }
@@ -121,11 +122,15 @@ __device__ __forceinline__ double epi_apply(const Epi& e, int b, long long i, lo
     case EPI_STORE:
       plane_store<E>(e.C, b, i, j, acc);
       return 0.0;
+    case EPI_AFF: {
+      const double v = e.alpha * acc + e.beta_in * plane_load<E>(e.In, b, i, j) + (i == j ? e.gamma : 0.0);
+      plane_store<E>(e.C, b, i, j, v);
+      return fabs(v);        // row-max tracking (tcgen05 engine)
+    }
     case EPI_M: {
-      const double id = (i == j) ? 1.0 : 0.0;
-      plane_store<E>(e.C, b, i, j, acc);
-      if (E == ENGINE_F64) plane_store<E>(e.C2, b, i, j, ((double)(e.ctl.p + 1) * id - acc) / (double)e.ctl.p);
-      const double r = acc - id;
+      const double v = acc + e.beta_in * plane_load<E>(e.In, b, i, j);
+      plane_store<E>(e.C, b, i, j, v);
+      const double r = v - ((i == j) ? 1.0 : 0.0);
       return r * r;
     }
     case EPI_GRAM: {

@@ -75,7 +75,8 @@ gemm_f64_kernel(GemmF64Args g, Epi e) {
     for (int j = 0; j < 4; ++j) {
       const int c = tile_n + tx + 16 * j;
       if (c >= g.N) continue;
-      part += epi_apply<ENGINE_F64>(e, b, r, c, acc[i][j] * sc);
+      const double v = epi_apply<ENGINE_F64>(e, b, r, c, acc[i][j] * sc);
+      if (e.kind == EPI_M) part += v;
     }
   }
   if (e.kind == EPI_M) {

@@ -263,7 +263,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
     if (gr < g.M) sa = g.a_rowscale ? (double)g.a_rowscale[(long long)za * g.a_rs_stride + gr] : (double)g.a_scale;
     double part = 0.0;
     float rmax = 0.f;
-    const bool track = (e.kind == EPI_M) && e.C.rowmax != nullptr;
+    const bool track = (e.kind == EPI_AFF) && e.C.rowmax != nullptr;
     if (ok) {
 #pragma unroll 1
       for (int ch = 0; ch < TC_BN / 32; ++ch) {
@@ -280,8 +280,9 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
               const double sb = g.b_rowscale ? (double)g.b_rowscale[(long long)zb * g.b_rs_stride + gc]
                                              : (double)g.b_scale;
               const double acc = (((double)v0[j] + (double)v1[j]) + (double)v2[j]) * (c0 * sa * sb);
-              part += epi_apply<ENGINE_TC>(e, b, gr, gc, acc);
-              rmax = fmaxf(rmax, (float)fabs(acc));
+              const double v = epi_apply<ENGINE_TC>(e, b, gr, gc, acc);
+              if (e.kind == EPI_M) part += v;
+              else rmax = fmaxf(rmax, (float)v);
             }
           }
         }

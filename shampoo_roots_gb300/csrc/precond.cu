@@ -54,12 +54,11 @@ struct RootClass {
   std::vector<int> roots;              // global root ids
   std::vector<const float*> src;       // per entry: source matrix (caller)
   std::vector<float*> dst;             // per entry: caller output (inv_root)
-  Slab X[2], M[2], T[2], T2, T4, Xf;
+  Slab X[2], M[2], D, F, Xf;   // per-row-scaled (tcgen05) or double planes
   size_t rowabs = 0, diag = 0, rowsq = 0, partials = 0;
   long long tiles = 0;
-  size_t t_root = 0, t_src = 0, t_dst = 0, t_xscale = 0;   // device tables (offsets)
+  size_t t_root = 0, t_src = 0, t_dst = 0;   // device tables (offsets)
   int kmax = 0;
-  std::vector<float> xscale;           // tcgen05 engine: digit scale of X_k, k = 0..kmax
 };
 
 struct ShapeClass {
@@ -200,35 +199,21 @@ int pick_engine(const precond_ctx* h, int64_t maxdim) {
   return maxdim <= h->small_dim ? ENGINE_F64 : ENGINE_TC;
 }
 
-// Root-class planes and scales.
-void layout_root_class(Layout& L, RootClass& r, int p, double eps) {
+// Root-class planes.  The iteration is written without identity offsets in
+// any product operand (see launch_iterations), so every tcgen05 operand is a
+// per-row-scaled digit split of an fp32 matrix.
+void layout_root_class(Layout& L, RootClass& r, int p) {
   const int nb = (int)r.roots.size(), d = r.d, e = r.eng;
   for (int i = 0; i < 2; ++i) {
-    r.X[i] = make_slab(L, e, nb, d, d);
+    r.X[i] = make_slab(L, e, nb, d, d, 4, true);
     r.M[i] = make_slab(L, e, nb, d, d, 4, true);
-    r.T[i] = make_slab(L, e, nb, d, d);
   }
-  r.T2 = make_slab(L, e, nb, d, d);
-  if (p == 4) r.T4 = make_slab(L, e, nb, d, d);
-  r.Xf = make_slab(L, e, nb, d, d);
+  r.D = make_slab(L, e, nb, d, d, 4, true);
+  if (p == 4) r.F = make_slab(L, e, nb, d, d, 4, true);
+  r.Xf = make_slab(L, e, nb, d, d, 4, true);
   r.rowabs = L.take((size_t)nb * d * sizeof(double));
   r.diag = L.take((size_t)nb * d * sizeof(double));
   r.rowsq = L.take((size_t)nb * d * sizeof(double));
-  if (e == ENGINE_TC) {
-    // entry bounds from the spectra (|a_ij| <= ||A||_2 for symmetric A):
-    // T in [1, (p+1)/p], T^2, T^4 accordingly, X_k <= m0^(-1/p), final X <= eps^(-1/p).
-    const double tmax = (p + 1.0) / p;
-    const double m0 = eps / (1.01 * (1.0 + d * eps));
-    const double xmax = std::pow(m0, -1.0 / p);
-    const double xf = std::pow(eps, -1.0 / p);
-    for (int i = 0; i < 2; ++i) {
-      r.T[i].scale = pow2_ceil_host(tmax * 1.001);
-      r.X[i].scale = pow2_ceil_host(xmax * 1.001);
-    }
-    r.T2.scale = pow2_ceil_host(tmax * tmax * 1.001);
-    r.T4.scale = pow2_ceil_host(std::pow(tmax, 4) * 1.001);
-    r.Xf.scale = pow2_ceil_host(xf * 1.001);
-  }
 }
 
 int build_plan(precond_ctx* h, Plan& P, bool step, int count, const int64_t* dims2, int dtype, float eps,
@@ -304,18 +289,8 @@ int build_plan(precond_ctx* h, Plan& P, bool step, int count, const int64_t* dim
   P.stats = L.take(sizeof(RootStat) * P.nroots);
   P.err = L.take(64);
   for (auto& r : P.rc) {
-    layout_root_class(L, r, p, eps);
+    layout_root_class(L, r, p);
     r.kmax = iter_cap(eps, r.d, p, h->tol, h->max_iter);
-    // X_k = prod_j T_j; its largest eigenvalue follows the scalar model on the
-    // smallest scaled eigenvalue m0 = eps / (1.01 (1 + d eps)) <= lambda_min(M_0):
-    // x_k = (m_k / m0)^(1/p) with m_{k+1} = m_k ((p+1-m_k)/p)^p.
-    r.xscale.assign(r.kmax + 2, 1.f);
-    double m = eps / (1.01 * (1.0 + r.d * eps));
-    const double m0 = m;
-    for (int k = 0; k <= r.kmax + 1; ++k) {
-      r.xscale[k] = pow2_ceil_host(std::pow(m / m0, 1.0 / p) * 1.01);
-      m = m * std::pow((p + 1 - m) / p, p);
-    }
     const long long t = r.eng == ENGINE_F64
         ? (long long)((r.d + F64_BM - 1) / F64_BM) * ((r.d + F64_BN - 1) / F64_BN)
         : (long long)((r.d + TC_BM - 1) / TC_BM) * ((r.d + TC_BN - 1) / TC_BN);
@@ -343,7 +318,6 @@ int build_plan(precond_ctx* h, Plan& P, bool step, int count, const int64_t* dim
     r.t_root = W.put(ro);
     r.t_src = W.put(r.src);
     r.t_dst = W.put(r.dst);
-    r.t_xscale = W.put(r.xscale);
   }
   for (auto& c : P.sc) {
     std::vector<const void*> g;
@@ -563,14 +537,11 @@ RootArgs root_args(const Ctx& c, const RootClass& r, float eps) {
   a.ctl.kmax = r.kmax;
   a.ctl.tol = (float)c.h->tol;
   a.M0 = c.plane(r.M[0]);     // fp32 form (tcgen05 engine), sliced after the start
-  a.T0 = c.plane(r.T[0]);
   a.X1 = c.plane(r.X[1]);
-  if (r.eng == ENGINE_TC) a.X1.scale = r.xscale[1];
-  a.X[0] = c.digits(r.X[0]);
-  a.X[1] = c.digits(r.X[1]);
+  a.X[0] = c.plane(r.X[0]);   // read in fp32 form by the finish
+  a.X[1] = c.plane(r.X[1]);
   a.Xf = c.plane(r.Xf);
   a.dst = c.P.step ? nullptr : c.at<float* const>(r.t_dst);
-  a.xscale = r.eng == ENGINE_TC ? c.at<const float>(r.t_xscale) : nullptr;
   return a;
 }
 
@@ -586,12 +557,12 @@ int launch_roots_start(const Ctx& c, float eps) {
     if (r.eng == ENGINE_F64) {
       root_init_kernel<ENGINE_F64><<<g, 256, 0, c.st>>>(a);
     } else {
-      if ((rc = clear_rowmax(c, r.M[0]))) return rc;
+      if ((rc = clear_rowmax(c, r.M[0])) || (rc = clear_rowmax(c, r.X[1]))) return rc;
       root_init_kernel<ENGINE_TC><<<g, 256, 0, c.st>>>(a);
     }
     c.h->launches += 3;
     CK(cudaGetLastError());
-    if (r.eng == ENGINE_TC && (rc = slice(c, r.M[0]))) return rc;
+    if (r.eng == ENGINE_TC && ((rc = slice(c, r.M[0])) || (rc = slice(c, r.X[1])))) return rc;
   }
   return PRECOND_OK;
 }
@@ -618,45 +589,49 @@ int launch_iterations(const Ctx& c) {
       e.ctl.tol = (float)c.h->tol;
       e.k = k;
       const bool tc = eng == ENGINE_TC;
-      if (k >= 1) {   // X_{k+1} = X_k T_k   (X_1 = T_0 was written by the start)
-        Epi ex = e;
-        Slab Xc = r.X[cur], Xn = r.X[nxt];
-        if (tc) {
-          Xc.scale = r.xscale[k];
-          Xn.scale = r.xscale[k + 1];
-        }
-        ex.C = c.plane(Xn);
-        if ((rcode = gemm(c, eng, Xc, r.T[cur], d, d, d, nullptr, nullptr, 4, ex, nb))) return rcode;
+      // Identity-free form of  T = tau I - M/p,  tau = (p+1)/p:
+      //   p = 2:  T^2 = tau^2 I + D,   D = M M / p^2 - (2 tau / p) M,   M' = tau^2 M + D M
+      //   p = 4:  T^2 = tau^2 I + D,   T^4 = tau^4 I + F,   F = D D + 2 tau^2 D,   M' = tau^4 M + F M
+      //   X' = X T = tau X - X M / p
+      // so every product operand (M, D, F, X) keeps its information in its own
+      // digits instead of next to a dominant identity.
+      const double tau = (p + 1.0) / p;
+      auto aff = [&](const Slab& A, const Slab& B, const Slab& In, const Slab& C, double alpha, double beta_in) -> int {
+        Epi ea = e;
+        ea.kind = EPI_AFF;
+        ea.C = c.plane(C);
+        ea.In = c.plane(In);
+        ea.alpha = alpha;
+        ea.beta_in = beta_in;
+        ea.gamma = 0.0;
+        int rc2;
+        if (tc && (rc2 = clear_rowmax(c, C))) return rc2;
+        if ((rc2 = gemm(c, eng, A, B, d, d, d, nullptr, nullptr, 4, ea, nb))) return rc2;
         ++n;
+        if (tc && (rc2 = slice(c, C))) return rc2;
+        return PRECOND_OK;
+      };
+      if (k >= 1 && (rcode = aff(r.X[cur], r.M[cur], r.X[cur], r.X[nxt], -1.0 / p, tau))) return rcode;
+      if ((rcode = aff(r.M[cur], r.M[cur], r.M[cur], r.D, 1.0 / (p * p), -2.0 * tau / p))) return rcode;
+      const Slab* Pk = &r.D;
+      if (p == 4) {
+        if ((rcode = aff(r.D, r.D, r.D, r.F, 1.0, 2.0 * tau * tau))) return rcode;
+        Pk = &r.F;
       }
-      Epi e2 = e;   // T2 = T T
-      e2.C = c.plane(r.T2);
-      if ((rcode = gemm(c, eng, r.T[cur], r.T[cur], d, d, d, nullptr, nullptr, 4, e2, nb))) return rcode;
-      ++n;
-      const Slab* Tp = &r.T2;
-      if (p == 4) {   // T4 = T2 T2
-        Epi e4 = e;
-        e4.C = c.plane(r.T4);
-        if ((rcode = gemm(c, eng, r.T2, r.T2, d, d, d, nullptr, nullptr, 4, e4, nb))) return rcode;
-        ++n;
-        Tp = &r.T4;
-      }
-      Epi em = e;     // M_{k+1} = T^p M_k, T_{k+1}, residual, convergence
+      Epi em = e;     // M_{k+1} = tau^p M_k + P M_k, residual, convergence
       em.kind = EPI_M;
       em.C = c.plane(r.M[nxt]);
-      em.C2 = c.plane(r.T[nxt]);
-      if (tc) em.C.rowmax = nullptr;   // row maxima and T come from the symmetrisation pass
-      if ((rcode = gemm(c, eng, *Tp, r.M[cur], d, d, d, nullptr, nullptr, 4, em, nb))) return rcode;
+      em.In = c.plane(r.M[cur]);
+      em.beta_in = std::pow(tau, p);
+      if ((rcode = gemm(c, eng, *Pk, r.M[cur], d, d, d, nullptr, nullptr, 4, em, nb))) return rcode;
       ++n;
       if (tc) {
         if ((rcode = clear_rowmax(c, r.M[nxt]))) return rcode;
         SymArgs sa;
         sa.M = c.plane(r.M[nxt]);
-        sa.T = c.plane(r.T[nxt]);
         sa.root_of = root_of;
         sa.stats = c.stats();
         sa.d = d;
-        sa.p = p;
         const int tb = (d + 31) / 32;
         sym_m_kernel<<<dim3(tb, tb, nb), 256, 0, c.st>>>(sa);
         c.h->launches++;
@@ -674,10 +649,13 @@ int launch_finish(const Ctx& c, float eps) {
     const int nb = (int)r.roots.size();
     RootArgs a = root_args(c, r, eps);
     dim3 g((r.d + 31) / 32, (r.d + 31) / 32, nb);
+    int rc;
+    if (r.eng == ENGINE_TC && c.P.step && (rc = clear_rowmax(c, r.Xf))) return rc;
     if (r.eng == ENGINE_F64) root_finish_kernel<ENGINE_F64><<<g, 256, 0, c.st>>>(a);
     else root_finish_kernel<ENGINE_TC><<<g, 256, 0, c.st>>>(a);
     c.h->launches++;
     CK(cudaGetLastError());
+    if (r.eng == ENGINE_TC && c.P.step && (rc = slice(c, r.Xf))) return rc;
   }
   return PRECOND_OK;
 }
@@ -1057,6 +1035,7 @@ int precond_get_root(precond_t h, int r, float* dst, void* stream) {
   const RootClass& rc = h->last_plan.rc[h->last_root_class[r]];
   const int slot = h->last_root_slot[r];
   Plane p = digits_plane((char*)h->ws, rc.Xf);
+  if (rc.Xf.f32) p.f32 = reinterpret_cast<float*>((char*)h->ws + rc.Xf.f32);   // fp32 form of the root
   cudaStream_t st = (cudaStream_t)stream;
   if (rc.eng == ENGINE_F64) plane_to_f32_kernel<ENGINE_F64><<<256, 256, 0, st>>>(p, slot, rc.d, rc.d, dst);
   else plane_to_f32_kernel<ENGINE_TC><<<256, 256, 0, st>>>(p, slot, rc.d, rc.d, dst);
@@ -1066,13 +1045,13 @@ int precond_get_root(precond_t h, int r, float* dst, void* stream) {
 }
 
 // Diagnostic read-back of a work matrix of root `r` of the last call:
-// which = 0/1 X[0]/X[1], 2/3 M[0]/M[1], 4/5 T[0]/T[1], 6 T2, 7 T4, 8 final X.
+// which = 0/1 X[0]/X[1], 2/3 M[0]/M[1], 4 D, 5 F, 8 final X.
 int precond_debug_plane(precond_t h, int r, int which, float* dst, void* stream) {
-  if (!h || !dst || which < 0 || which > 8) return PRECOND_EINVAL;
+  if (!h || !dst || which < 0 || which > 8 || which == 6 || which == 7) return PRECOND_EINVAL;
   if (h->device < 0) return PRECOND_ENODEV;
   if (!h->have_last || r < 0 || r >= h->last_nroots) return PRECOND_EINVAL;
   const RootClass& rc = h->last_plan.rc[h->last_root_class[r]];
-  const Slab* sl[9] = {&rc.X[0], &rc.X[1], &rc.M[0], &rc.M[1], &rc.T[0], &rc.T[1], &rc.T2, &rc.T4, &rc.Xf};
+  const Slab* sl[9] = {&rc.X[0], &rc.X[1], &rc.M[0], &rc.M[1], &rc.D, &rc.F, nullptr, nullptr, &rc.Xf};
   const Slab& S = *sl[which];
   if (S.batch == 0) return PRECOND_EINVAL;
   Plane p = digits_plane((char*)h->ws, S);

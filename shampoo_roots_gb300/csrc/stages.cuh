@@ -150,9 +150,8 @@ struct RootArgs {
   float eps;
   IterCtl ctl;
   // engine planes
-  Plane M0, T0, X1;          // init outputs
+  Plane M0, X1;              // start outputs (fp32 form in the tcgen05 engine)
   Plane X[2];                // finalize input (X buffer kfinal & 1)
-  const float* xscale;       // tcgen05 engine: digit scale of X_k by k (device table), or null
   Plane Xf;                  // finalize output in engine format (step), or unused
   float* const* dst;         // finalize output to caller fp32 (inv_root), or null
 };
@@ -241,7 +240,7 @@ __device__ __forceinline__ double root_scale(const RootStat& st, int d, double e
   return 1.01 * fmin(ws, st.minc);
 }
 
-// M_0 = A_hat / c, T_0 = ((p+1) I - M_0) / p, X_1 = X_0 T_0 = T_0.
+// M_0 = A_hat / c and X_1 = X_0 T_0 = T_0 = ((p+1) I - M_0) / p.
 template <int E>
 __global__ void __launch_bounds__(256) root_init_kernel(RootArgs a) {
   const int b = blockIdx.z;
@@ -264,19 +263,23 @@ __global__ void __launch_bounds__(256) root_init_kernel(RootArgs a) {
   const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
   for (int q = ty; q < 32; q += 8) {
     const int r = r0 + q, col = c0 + tx;
-    float mx = 0.f;
+    float mx = 0.f, xx = 0.f;
     if (r < a.d && col < a.d) {
       const double id = (r == col) ? 1.0 : 0.0;
       const double m0 = ((double)A[(long long)r * a.d + col] / t + eps * id) / c;
-      const double t0 = ((p + 1.0) * id - m0) / p;
+      const double x1 = ((p + 1.0) * id - m0) / p;
       plane_store<E>(a.M0, b, r, col, m0);
-      plane_store<E>(a.T0, b, r, col, t0);
-      plane_store<E>(a.X1, b, r, col, t0);
+      plane_store<E>(a.X1, b, r, col, x1);
       mx = (float)fabs(m0);
+      xx = (float)fabs(x1);
     }
-    if (E == ENGINE_TC && a.M0.rowmax) {
+    if (E == ENGINE_TC) {
       mx = warp_max(mx);
-      if (tx == 0 && r < a.d) atomic_max_nonneg(&a.M0.rowmax[(long long)b * a.d + r], mx);
+      xx = warp_max(xx);
+      if (tx == 0 && r < a.d) {
+        atomic_max_nonneg(&a.M0.rowmax[(long long)b * a.d + r], mx);
+        atomic_max_nonneg(&a.X1.rowmax[(long long)b * a.d + r], xx);
+      }
     }
   }
 }
@@ -288,8 +291,7 @@ __global__ void __launch_bounds__(256) root_finish_kernel(RootArgs a) {
   const int b = blockIdx.z;
   const RootStat* st = &a.stats[a.root_of[b]];
   if (st->status == PRECOND_ENONFINITE || st->kfinal < 1) return;
-  Plane X = a.X[st->kfinal & 1];
-  if (E == ENGINE_TC && a.xscale) X.scale = a.xscale[st->kfinal];
+  const Plane& X = a.X[st->kfinal & 1];
   const double f = pow(st->c, -1.0 / (double)a.ctl.p);
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
@@ -301,10 +303,17 @@ __global__ void __launch_bounds__(256) root_finish_kernel(RootArgs a) {
   __syncthreads();
   for (int q = ty; q < 32; q += 8) {
     const int r = r0 + q, col = c0 + tx;
-    if (r >= a.d || col >= a.d) continue;
-    const double v = 0.5 * (plane_load<E>(X, b, r, col) + tile[tx][q]) * f;
-    if (a.dst) a.dst[b][(long long)r * a.d + col] = (float)v;
-    else plane_store<E>(a.Xf, b, r, col, v);
+    float mx = 0.f;
+    if (r < a.d && col < a.d) {
+      const double v = 0.5 * (plane_load<E>(X, b, r, col) + tile[tx][q]) * f;
+      if (a.dst) a.dst[b][(long long)r * a.d + col] = (float)v;
+      else plane_store<E>(a.Xf, b, r, col, v);
+      mx = (float)fabs(v);
+    }
+    if (E == ENGINE_TC && !a.dst) {
+      mx = warp_max(mx);
+      if (tx == 0 && r < a.d) atomic_max_nonneg(&a.Xf.rowmax[(long long)b * a.d + r], mx);
+    }
   }
 }
 
@@ -318,17 +327,16 @@ __global__ void f32_to_plane_kernel(const float* src, Plane p, int rows, int col
   }
 }
 
-// After M_{k+1} = T^p M_k (tcgen05 engine): M <- (M + M^T) / 2 in place (M is
-// symmetric in exact arithmetic, and the iteration amplifies any antisymmetric
-// rounding by up to ((p+1)/p)^p per step), T_{k+1} = ((p+1) I - M) / p as
-// fixed-scale digits, and the row maxima for slicing M.  Each block handles a
-// pair of mirrored 32 x 32 tiles (bx <= by).
+// After the product M_{k+1} (tcgen05 engine): M <- (M + M^T) / 2 in place.  M
+// is symmetric in exact arithmetic, and the iteration amplifies any
+// antisymmetric rounding by up to ((p+1)/p)^p per step while M is far from I,
+// so it is projected back every step; also writes the row maxima for slicing.
+// Each block handles a pair of mirrored 32 x 32 tiles (bx <= by).
 struct SymArgs {
   Plane M;          // fp32 form (f32, rowmax)
-  Plane T;          // digit form
   const int* root_of;
   const RootStat* stats;
-  int d, p;
+  int d;
 };
 
 __global__ void __launch_bounds__(256) sym_m_kernel(SymArgs a) {
@@ -347,33 +355,20 @@ __global__ void __launch_bounds__(256) sym_m_kernel(SymArgs a) {
     tb[q][tx] = (r2 < a.d && c2 < a.d) ? M[(long long)r2 * ld + c2] : 0.f;
   }
   __syncthreads();
-  const double pp = (double)a.p;
-  // tile A: element (q, tx) = (ta[q][tx] + tb[tx][q]) / 2
-  for (int q = ty; q < 32; q += 8) {
-    const int r = ra + q, c = ca + tx;
-    float mx = 0.f;
-    if (r < a.d && c < a.d) {
-      const double m = 0.5 * ((double)ta[q][tx] + (double)tb[tx][q]);
-      M[(long long)r * ld + c] = (float)m;
-      plane_store<ENGINE_TC>(a.T, b, r, c, ((pp + 1.0) * (r == c ? 1.0 : 0.0) - m) / pp);
-      mx = (float)fabs(m);
+  for (int half = 0; half < 2; ++half) {
+    if (half == 1 && bx == by) break;
+    const int rbase = half == 0 ? ra : ca, cbase = half == 0 ? ca : ra;
+    for (int q = ty; q < 32; q += 8) {
+      const int r = rbase + q, c = cbase + tx;
+      float mx = 0.f;
+      if (r < a.d && c < a.d) {
+        const float m = half == 0 ? 0.5f * (ta[q][tx] + tb[tx][q]) : 0.5f * (tb[q][tx] + ta[tx][q]);
+        M[(long long)r * ld + c] = m;
+        mx = fabsf(m);
+      }
+      mx = warp_max(mx);
+      if (tx == 0 && r < a.d) atomic_max_nonneg(&a.M.rowmax[(long long)b * a.d + r], mx);
     }
-    mx = warp_max(mx);
-    if (tx == 0 && r < a.d) atomic_max_nonneg(&a.M.rowmax[(long long)b * a.d + r], mx);
-  }
-  if (bx == by) return;
-  // tile B (rows ca.., cols ra..): element (q, tx) = (tb[q][tx] + ta[tx][q]) / 2
-  for (int q = ty; q < 32; q += 8) {
-    const int r = ca + q, c = ra + tx;
-    float mx = 0.f;
-    if (r < a.d && c < a.d) {
-      const double m = 0.5 * ((double)tb[q][tx] + (double)ta[tx][q]);
-      M[(long long)r * ld + c] = (float)m;
-      plane_store<ENGINE_TC>(a.T, b, r, c, ((pp + 1.0) * (r == c ? 1.0 : 0.0) - m) / pp);
-      mx = (float)fabs(m);
-    }
-    mx = warp_max(mx);
-    if (tx == 0 && r < a.d) atomic_max_nonneg(&a.M.rowmax[(long long)b * a.d + r], mx);
   }
 }
 
