@@ -1,0 +1,331 @@
+"""Benchmark of the matrix-preconditioner step on GB300.
+
+A step = one call of the whole hot path (Gram EMAs, statistics and bound,
+coupled Newton-Schulz roots, two-sided apply) over one batch of synthetic
+gradients of the 24-layer d = 1024 transformer stack (bf16 gradients, fp32
+Grams, power -1/4): 144 weight matrices, 288 roots.
+
+Prints ONE JSON line (rank 0).  `value` is whole-job algorithmic TFLOP/s of
+the step (2mnk per logical GEMM, iterations actually executed); `e2e` is the
+same metric with the gradients copied from pinned host memory and the
+update copied back inside the timed region.  `--impl reference` times the
+float64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "preconditioner step ms and TFLOP/s (% GB300 tensor peak) vs CPU oracle"
+WORKLOAD_INDEX = 1          # the 24-layer d=1024 stack, power -1/4
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def step_flops_outside_roots(shapes):
+    """Algorithmic FLOPs of the Gram EMAs and the apply (2mnk per product)."""
+    f = 0.0
+    for m, n in shapes:
+        f += 2.0 * m * m * n + 2.0 * n * n * m      # L = G G^T, R = G^T G
+        f += 2.0 * m * n * n + 2.0 * m * m * n      # V = G X_R, U = X_L V
+    return f
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if not self.path or not os.path.exists(self.path):
+            return out
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return out
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        out.update(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(mx) if mx else None,
+                   reasons=reasons, samples=len(rows))
+        return out
+
+
+def oracle_sample(w, seconds_budget=20.0):
+    """Time the float64 oracle on one matrix of each shape class of the stack
+    (one EMA step from zero Grams) and extrapolate to the whole stack.
+    Returns (oracle seconds per full step, sample description, cores)."""
+    import numpy as np
+    from oracle import roots as oracle
+    from workloads import synth
+    classes = {}
+    for i, s in enumerate(w.shapes):
+        classes.setdefault(s, []).append(i)
+    per_class = {}
+    t_used = 0.0
+    for shape, idx in classes.items():
+        G = synth.gradients_for_step(w, 0, [idx[0]])[0].astype(np.float64)
+        st = oracle.OracleState([shape])
+        t0 = time.perf_counter()
+        oracle.precond_step(st, [G], w.beta, w.eps, w.powers[0])
+        dt = time.perf_counter() - t0
+        per_class[shape] = (dt, len(idx))
+        t_used += dt
+        if t_used > seconds_budget:
+            break
+    total = sum(dt * cnt for dt, cnt in per_class.values())
+    # classes not sampled within the budget are extrapolated by d^3
+    for shape, idx in classes.items():
+        if shape not in per_class:
+            ref_shape, (dt, _) = next(iter(per_class.items()))
+            scale = (max(shape) / max(ref_shape)) ** 3
+            total += dt * scale * len(idx)
+    desc = ("one matrix of each shape class " + ", ".join(f"{m}x{n}" for (m, n) in per_class) +
+            f" (one EMA step, {t_used:.1f} s), extrapolated to all {len(w.shapes)} matrices")
+    return total, desc, os.cpu_count()
+
+
+def run_reference(args):
+    """Reference arm: the float64 CPU oracle on a bounded sample per step."""
+    from workloads import synth
+    w = synth.workload(WORKLOAD_INDEX)
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    secs = []
+    desc = ""
+    cores = os.cpu_count()
+    for _ in range(args.warmup + args.steps):
+        t, desc, cores = oracle_sample(w, seconds_budget=8.0)
+        secs.append(t)
+    timed = secs[args.warmup:]
+    per_step = statistics.median(timed)
+    # the step's algorithmic FLOPs at the iteration counts the GPU path runs (about 20 per root)
+    flops = step_flops_outside_roots(w.shapes) + sum(2.0 * d ** 3 * (20 * 4 - 1) for m, n in w.shapes for d in (m, n))
+    value = flops / per_step / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "matrices": len(w.shapes), "grad_dtype": w.dtype, "power": w.powers[0]},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def profile_small(args):
+    """A small case for ncu captures: inverse quarter roots of 4 SPD 2048^2
+    matrices of the conditioning-stress recipe (a few GB on the device)."""
+    import torch
+    import shampoo_roots_gb300 as sr
+    from workloads import synth
+    w = synth.workload(3)
+    dev = torch.device("cuda")
+    A = synth.torch_spd_inputs(w, dev, matrices=range(4))
+    X = [torch.empty_like(a) for a in A]
+    pc = sr.Preconditioner(0)
+    for _ in range(args.warmup + args.steps):
+        sr.precond_inv_root(pc.h, A, X, w.eps, -0.25)
+    torch.cuda.synchronize()
+    it, _, status, _ = sr.precond_get_stats(pc.h, len(A))
+    pc.close()
+    print(json.dumps({"profile_small": True, "iterations": it, "status": status}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--profile-small", action="store_true",
+                    help="profiling case: roots of 4 SPD 2048^2 matrices, no JSON line")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.profile_small:
+        return profile_small(args)
+
+    import torch
+    import shampoo_roots_gb300 as sr
+    from workloads import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    w = synth.workload(WORKLOAD_INDEX)
+    shapes = list(w.shapes)
+    power = w.powers[0]
+    # two distinct gradient batches (ranks draw from their own seeds: weak scaling)
+    pools = [synth.torch_gradients_for_step(w, 1000 * rank + s, dev) for s in range(2)]
+    L = [torch.zeros((m, m), device=dev) for m, _ in shapes]
+    R = [torch.zeros((n, n), device=dev) for _, n in shapes]
+    out = [torch.empty((m, n), device=dev) for m, n in shapes]
+    pc = sr.Preconditioner(local, timing=1)
+
+    def step(i):
+        sr.precond_step(pc.h, pools[i % 2], L, R, w.beta, w.eps, power, out=out, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---------------- timed region (device-resident inputs)
+    launches0 = sr.precond_launch_count(pc.h)
+    ns_ms, ns_flops, gemm_ms, gemm_n, root_flops = 0.0, 0.0, 0.0, 0, 0.0
+    iters_seen = []
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        barrier()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+            ms, nl, fl = sr.precond_get_timing(pc.h)     # synchronises the step
+            gms, gn = sr.precond_get_gemm_timing(pc.h)
+            ns_ms += ms[2]
+            root_flops += fl
+            gemm_ms += gms
+            gemm_n += gn
+            it, _, _, _ = sr.precond_get_stats(pc.h, 2 * len(shapes))
+            iters_seen.append(statistics.mean(it))
+        ev1.record(stream)
+        barrier()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    gpu_launches = sr.precond_launch_count(pc.h) - launches0
+    if dist is not None:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    step_flops = step_flops_outside_roots(shapes) + root_flops / args.steps
+    value = world * step_flops * args.steps / elapsed / 1e12
+    ms_per_step = elapsed / args.steps * 1e3
+
+    # ---------------- end to end: pinned host gradients in, update out, inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        host_g = [[g.cpu().pin_memory() for g in pool] for pool in pools]
+        host_u = [torch.empty((m, n), dtype=torch.float32).pin_memory() for m, n in shapes]
+        dev_g = [torch.empty_like(g) for g in pools[0]]
+        h2d = sum(g.numel() * g.element_size() for g in host_g[0])
+        d2h = sum(u.numel() * u.element_size() for u in host_u)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            for dg, hg in zip(dev_g, host_g[i % 2]):
+                dg.copy_(hg, non_blocking=True)
+            sr.precond_step(pc.h, dev_g, L, R, w.beta, w.eps, power, out=out, stream=stream)
+            for hu, o in zip(host_u, out):
+                hu.copy_(o, non_blocking=True)
+        e1.record(stream)
+        barrier()
+        t_e2e = e0.elapsed_time(e1) / 1e3
+        if dist is not None:
+            t = torch.tensor([t_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            t_e2e = float(t.item())
+        e2e = {"value": world * step_flops * args.steps / t_e2e / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": t_e2e / args.steps * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    peaks = load_peaks()
+    # dominant kernel: the tcgen05 GEMM of the iteration stage (timed inside a long step -> sustained peak)
+    achieved = (root_flops / (gemm_ms / 1e3) / 1e12) if gemm_ms > 0 else None
+    peak = peaks["bf16_tflops_sustained"]
+    issued = achieved * 10 if achieved else None     # 10 bf16 digit products per logical product
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": (achieved / peak) if achieved else None, "traffic": None,
+                "kernel": "gemm_tc_kernel<4> (iteration-stage products)",
+                "peak_kind": f"bf16 dense, sustained ({peaks['source']})",
+                "issued_tflops": issued, "issued_frac": (issued / peak) if issued else None,
+                "avg_launch_ms": gemm_ms / gemm_n if gemm_n else None}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        t_oracle, desc, cores = oracle_sample(w)
+        cpu = {"value": step_flops / t_oracle / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": desc, "ms_per_step_extrapolated": t_oracle * 1e3}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": w.name, "matrices": len(shapes), "roots": 2 * len(shapes),
+                           "grad_dtype": w.dtype, "power": power, "beta": w.beta, "eps": w.eps,
+                           "mean_iterations": statistics.mean(iters_seen) if iters_seen else None,
+                           "l2": "inputs larger than L2 (fp32 Gram state 4.6 GB, gradients 0.6 GB per batch)",
+                           "numerics": "bf16 tensor-core digit products, exact fp32 accumulation of leading levels"},
+                "pct_tensor_peak": value / peaks["bf16_tflops"],
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
+                "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+    pc.close()
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

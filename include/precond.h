@@ -137,6 +137,13 @@ int precond_set_option(precond_t h, int key, double value);
  */
 int precond_get_timing(precond_t h, double ms[4], int64_t* ns_gemm_launches, double* ns_flops);
 
+/*
+ * With PRECOND_OPT_TIMING on: total milliseconds of the tcgen05 GEMM launches
+ * of the last call's iteration stage (CUDA events around each launch on the
+ * call's stream; synchronises) and their number.
+ */
+int precond_get_gemm_timing(precond_t h, double* ms_total, int64_t* launches);
+
 /* Kernel launches this handle has issued since creation (every library kernel). */
 int64_t precond_launch_count(precond_t h);
 

@@ -48,6 +48,7 @@ def load():
     L.precond_set_option.argtypes = [vp, i32, f64]
     L.precond_get_timing.argtypes = [vp, ctypes.POINTER(f64), ctypes.POINTER(i64), ctypes.POINTER(f64)]
     L.precond_launch_count.argtypes = [vp]
+    L.precond_get_gemm_timing.argtypes = [vp, ctypes.POINTER(f64), ctypes.POINTER(i64)]
     L.precond_launch_count.restype = i64
     L.precond_get_root.argtypes = [vp, i32, vp, vp]
     L.precond_debug_plane.argtypes = [vp, i32, i32, vp, vp]
@@ -56,7 +57,7 @@ def load():
     L.precond_error_string.restype = ctypes.c_char_p
     for name in ("precond_create", "precond_destroy", "precond_step", "precond_inv_root", "precond_get_stats",
                  "precond_set_option", "precond_get_timing", "precond_get_root", "precond_gemm_selftest",
-                 "precond_debug_plane"):
+                 "precond_debug_plane", "precond_get_gemm_timing"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -174,6 +175,13 @@ def precond_get_timing(h):
     fl = ctypes.c_double()
     _check(load().precond_get_timing(h, ms, ctypes.byref(nl), ctypes.byref(fl)), "precond_get_timing")
     return list(ms), nl.value, fl.value
+
+
+def precond_get_gemm_timing(h):
+    ms = ctypes.c_double()
+    n = ctypes.c_int64()
+    _check(load().precond_get_gemm_timing(h, ctypes.byref(ms), ctypes.byref(n)), "precond_get_gemm_timing")
+    return ms.value, n.value
 
 
 def precond_launch_count(h) -> int:

@@ -107,6 +107,9 @@ struct precond_ctx {
   Plan last_plan;
   int64_t launches = 0;
   int64_t ns_launches = 0;
+  bool in_ns = false;                  // timing: inside the iteration stage
+  std::vector<cudaEvent_t> gemm_ev;    // timing: start/stop pairs around iteration-stage GEMMs
+  size_t gemm_ev_used = 0;
   EncodeTiledFn encode = nullptr;
   bool tc_attr_set = false;
 };
@@ -488,10 +491,23 @@ int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int 
     g.err = c.err();
     dim3 grid((N + TC_BN - 1) / TC_BN, (M + TC_BM - 1) / TC_BM, batch);
     e.tiles_per_entry = grid.x * grid.y;
+    const bool timed = c.h->timing && c.h->events && c.h->in_ns;
+    if (timed) {
+      while (c.h->gemm_ev.size() < c.h->gemm_ev_used + 2) {
+        cudaEvent_t ev;
+        CK(cudaEventCreate(&ev));
+        c.h->gemm_ev.push_back(ev);
+      }
+      CK(cudaEventRecord(c.h->gemm_ev[c.h->gemm_ev_used], c.st));
+    }
     if (S == 4)
       gemm_tc_kernel<4><<<grid, TC_THREADS, TcSmem<4>::BYTES, c.st>>>(maps, g, e);
     else
       gemm_tc_kernel<3><<<grid, TC_THREADS, TcSmem<3>::BYTES, c.st>>>(maps, g, e);
+    if (timed) {
+      CK(cudaEventRecord(c.h->gemm_ev[c.h->gemm_ev_used + 1], c.st));
+      c.h->gemm_ev_used += 2;
+    }
   }
   c.h->launches++;
   CK(cudaGetLastError());
@@ -568,6 +584,9 @@ int launch_roots_start(const Ctx& c, float eps) {
 }
 
 int launch_iterations(const Ctx& c) {
+  c.h->in_ns = true;
+  c.h->gemm_ev_used = 0;
+  struct Guard { precond_ctx* h; ~Guard() { h->in_ns = false; } } guard{c.h};
   const int p = c.P.p;
   int kall = 0;
   for (const auto& r : c.P.rc) kall = std::max(kall, r.kmax);
@@ -854,6 +873,7 @@ int precond_destroy(precond_t h) {
     if (h->upload_done) cudaEventDestroy(h->upload_done);
     if (h->events)
       for (auto& e : h->ev) cudaEventDestroy(e);
+    for (auto& e : h->gemm_ev) cudaEventDestroy(e);
   }
   delete h;
   return PRECOND_OK;
@@ -1012,6 +1032,22 @@ int precond_get_timing(precond_t h, double ms[4], int64_t* ns_gemm_launches, dou
 }
 
 int64_t precond_launch_count(precond_t h) { return h ? h->launches : -1; }
+
+int precond_get_gemm_timing(precond_t h, double* ms_total, int64_t* launches) {
+  if (!h) return PRECOND_EINVAL;
+  if (h->device < 0) return PRECOND_ENODEV;
+  if (!h->have_last || !h->timing || !h->events) return PRECOND_EINVAL;
+  CK(cudaEventSynchronize(h->ev[4]));
+  double t = 0.0;
+  for (size_t i = 0; i + 1 < h->gemm_ev_used; i += 2) {
+    float x = 0.f;
+    CK(cudaEventElapsedTime(&x, h->gemm_ev[i], h->gemm_ev[i + 1]));
+    t += x;
+  }
+  if (ms_total) *ms_total = t;
+  if (launches) *launches = (int64_t)(h->gemm_ev_used / 2);
+  return PRECOND_OK;
+}
 
 const char* precond_error_string(int code) {
   switch (code) {
