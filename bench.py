@@ -170,7 +170,7 @@ def profile_small(args):
     from workloads import synth
     w = synth.workload(3)
     dev = torch.device("cuda")
-    A = synth.torch_spd_inputs(w, dev, matrices=range(4))
+    A = [torch.from_numpy(a).to(dev) for a in synth.spd_inputs(w, matrices=range(4))]
     X = [torch.empty_like(a) for a in A]
     pc = sr.Preconditioner(0)
     for _ in range(args.warmup + args.steps):
