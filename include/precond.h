@@ -175,6 +175,32 @@ int precond_gemm_selftest(precond_t h, int engine, int M, int N, int K, const fl
  */
 int precond_debug_plane(precond_t h, int r, int which, float* dst, void* stream);
 
+/*
+ * Allocation-free inverse root of ONE matrix (no counterpart in the pages: a
+ * deployment variant of precond_inv_root).  For callers that cannot allocate
+ * device memory when they need the root -- code inside a pool-allocator
+ * hook, a host callback, or a runtime that forbids cudaMalloc after start-up
+ * because it would synchronise the device or break a fixed memory budget.
+ *
+ *   X = (A / tr(A) + eps I)^power,  A and X fp32 d x d device buffers owned by
+ *   the caller (X may not alias A), power -0.25f or -0.5f, fp64 SIMT engine.
+ *
+ * All scratch lives in one fixed file-scope device array of 4 MiB that every
+ * GPU which loads this library holds until the process exits; no cudaMalloc,
+ * cudaFree or other allocating routine is called.  d above
+ * PRECOND_NOALLOC_MAX_D is rejected with PRECOND_EINVAL (and a message on
+ * stderr).  The first call on each device looks up the array's device address
+ * (with that device current); make that first call before any stream capture.
+ * Every call shares the array and overwrites it, so calls whose GPU work
+ * overlaps (other streams, other host threads, unsynchronised loops on
+ * different streams) race: order them on one stream.  `status` (host, may be
+ * NULL): when given, the call synchronises `stream` and stores the root's
+ * PRECOND_OK / ENOTCONV / ENONFINITE.
+ */
+#define PRECOND_NOALLOC_MAX_D 256
+int precond_inv_root_noalloc(const float* A, int64_t d, float eps, float power, float* X, void* stream,
+                             int* status);
+
 /* Static text for a status code. */
 const char* precond_error_string(int code);
 

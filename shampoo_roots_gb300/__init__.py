@@ -52,12 +52,14 @@ def load():
     L.precond_launch_count.restype = i64
     L.precond_get_root.argtypes = [vp, i32, vp, vp]
     L.precond_debug_plane.argtypes = [vp, i32, i32, vp, vp]
+    L.precond_inv_root_noalloc.argtypes = [vp, i64, f32, f32, vp, vp, ctypes.POINTER(i32)]
     L.precond_gemm_selftest.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, i32, vp]
     L.precond_error_string.argtypes = [i32]
     L.precond_error_string.restype = ctypes.c_char_p
     for name in ("precond_create", "precond_destroy", "precond_step", "precond_inv_root", "precond_get_stats",
                  "precond_set_option", "precond_get_timing", "precond_get_root", "precond_gemm_selftest",
-                 "precond_debug_plane", "precond_get_gemm_timing"):
+                 "precond_debug_plane", "precond_get_gemm_timing",
+                 "precond_inv_root_noalloc"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -194,6 +196,22 @@ def precond_get_root(h, r: int, dst, stream=None) -> None:
 
 def precond_debug_plane(h, r: int, which: int, dst, stream=None) -> None:
     _check(load().precond_debug_plane(h, int(r), int(which), _ptr(dst), _stream(stream)), "precond_debug_plane")
+
+
+NOALLOC_MAX_D = 256
+
+
+def precond_inv_root_noalloc(A, X, eps: float, power: float, stream=None, raw: bool = False):
+    """Allocation-free inverse root of one d x d matrix (d <= NOALLOC_MAX_D);
+    returns (return code, per-root status)."""
+    if A.dim() != 2 or A.shape[0] != A.shape[1] or not A.is_contiguous() or not X.is_contiguous():
+        raise ValueError("A must be a contiguous square matrix and X contiguous")
+    st = ctypes.c_int(0)
+    code = load().precond_inv_root_noalloc(_ptr(A), int(A.shape[0]), float(eps), float(power), _ptr(X),
+                                           _stream(stream), ctypes.byref(st))
+    if not raw:
+        _check(code, "precond_inv_root_noalloc")
+    return code, st.value
 
 
 def precond_gemm_selftest(h, engine: int, A, B, C, passes: int = 3, stream=None) -> None:

@@ -19,6 +19,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -1142,3 +1143,106 @@ int precond_gemm_selftest(precond_t h, int engine, int M, int N, int K, const fl
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// Allocation-free inverse root.
+//
+// Some callers cannot allocate device memory at the point where they need a
+// root: code running inside a pool-allocator hook, a host callback, or an
+// embedding runtime that forbids cudaMalloc after start-up (it would
+// synchronise the device or break a memory budget fixed in advance).  For
+// them, precond_inv_root_noalloc runs the fp64-engine inverse root of ONE
+// matrix (side d <= PRECOND_NOALLOC_MAX_D) with all scratch in a fixed
+// file-scope device array, so the call itself allocates nothing.
+// ===========================================================================
+namespace {
+constexpr size_t NOALLOC_BYTES = (size_t)4 << 20;   // 4 MiB, held by every GPU that loads the library
+constexpr int NOALLOC_MAX_DEVICES = 64;
+}  // namespace
+
+// The scratch itself.  In host code this name is only a host-side stand-in:
+// its device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
+
+namespace {
+struct NoAllocSlots {
+  std::mutex mu;
+  void* addr[NOALLOC_MAX_DEVICES] = {};
+};
+NoAllocSlots& noalloc_slots() {
+  static NoAllocSlots s;
+  return s;
+}
+
+struct MetaBlob {   // the call's pointer / index tables, passed by value (no staging buffer)
+  unsigned char bytes[512];
+  int n;
+};
+__global__ void noalloc_meta_kernel(MetaBlob blob, unsigned char* dst) {
+  for (int i = threadIdx.x; i < blob.n; i += blockDim.x) dst[i] = blob.bytes[i];
+}
+}  // namespace
+
+extern "C" int precond_inv_root_noalloc(const float* A, int64_t d, float eps, float power, float* X,
+                                        void* stream, int* status) {
+  if (!A || !X || (const void*)A == (const void*)X || d < 1) return PRECOND_EINVAL;
+  if (d > PRECOND_NOALLOC_MAX_D) {
+    fprintf(stderr, "libprecond: precond_inv_root_noalloc: d = %lld exceeds the fixed scratch limit %d\n",
+            (long long)d, PRECOND_NOALLOC_MAX_D);
+    return PRECOND_EINVAL;
+  }
+  if (!(eps > 0.f) || !std::isfinite(eps)) return PRECOND_EINVAL;
+  int p;
+  if (check_power(power, &p)) return PRECOND_EINVAL;
+  int dev = -1;
+  CK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return PRECOND_ECUDA;
+  // One-time set-up per device (with that device current): the device address
+  // of the scratch array.  This first call must not be made during a stream capture.
+  void* scratch = nullptr;
+  {
+    NoAllocSlots& s = noalloc_slots();
+    std::lock_guard<std::mutex> lock(s.mu);
+    if (!s.addr[dev]) {
+      void* ptr = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+      if (e != cudaSuccess || !ptr) {
+        fprintf(stderr, "libprecond: cudaGetSymbolAddress of the scratch failed: %s\n", cudaGetErrorString(e));
+        return PRECOND_ECUDA;
+      }
+      s.addr[dev] = ptr;
+    }
+    scratch = s.addr[dev];
+  }
+  precond_ctx h;          // options only; its workspace points at the scratch
+  h.device = dev;
+  h.engine = 1;           // fp64 SIMT engine
+  Plan P;
+  const int64_t dims[1] = {d};
+  const float* As[1] = {A};
+  float* Xs[1] = {X};
+  int rc = build_plan(&h, P, false, 1, dims, PRECOND_F32, eps, p, nullptr, nullptr, nullptr, nullptr, As, Xs);
+  if (rc) return rc;
+  if (P.total > NOALLOC_BYTES || P.meta_bytes > sizeof(MetaBlob::bytes)) return PRECOND_ENOMEM;
+  h.ws = scratch;
+  h.ws_cap = NOALLOC_BYTES;
+  cudaStream_t st = (cudaStream_t)stream;
+  MetaBlob blob;
+  memcpy(blob.bytes, P.meta_host.data(), P.meta_bytes);
+  blob.n = (int)P.meta_bytes;
+  noalloc_meta_kernel<<<1, 128, 0, st>>>(blob, (unsigned char*)scratch + P.meta);
+  CK(cudaGetLastError());
+  rc = run_inv_root(&h, P, eps, st);   // clears the per-root state it accumulates into
+  h.ws = nullptr;
+  if (rc) return rc;
+  if (status) {
+    CK(cudaStreamSynchronize(st));
+    RootStat rs;
+    unsigned int err = 0;
+    CK(cudaMemcpy(&rs, (char*)scratch + P.stats, sizeof(rs), cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(&err, (char*)scratch + P.err, sizeof(err), cudaMemcpyDeviceToHost));
+    *status = rs.status;
+    if (err) return PRECOND_ECUDA;
+  }
+  return PRECOND_OK;
+}
