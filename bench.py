@@ -237,6 +237,7 @@ def main():
     # ---------------- timed region (device-resident inputs)
     launches0 = sr.precond_launch_count(pc.h)
     ns_ms, ns_flops, gemm_ms, gemm_n, root_flops = 0.0, 0.0, 0.0, 0, 0.0
+    stage_ms = [0.0, 0.0, 0.0, 0.0]
     iters_seen = []
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
@@ -247,6 +248,7 @@ def main():
             ms, nl, fl = sr.precond_get_timing(pc.h)     # synchronises the step
             gms, gn = sr.precond_get_gemm_timing(pc.h)
             ns_ms += ms[2]
+            stage_ms = [a + b for a, b in zip(stage_ms, ms)]
             root_flops += fl
             gemm_ms += gms
             gemm_n += gn
@@ -319,6 +321,9 @@ def main():
                            "l2": "inputs larger than L2 (fp32 Gram state 4.6 GB, gradients 0.6 GB per batch)",
                            "numerics": "bf16 tensor-core digit products, exact fp32 accumulation of leading levels"},
                 "pct_tensor_peak": value / peaks["bf16_tflops"],
+                "stages_ms_per_step": {k: v / args.steps for k, v in zip(
+                    ("prep_gram", "bound_start", "iterations", "finish_apply"), stage_ms)},
+                "iteration_gemm_ms_per_step": gemm_ms / args.steps,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
                 "clocks": clk.summary()}
         print(json.dumps(line), flush=True)

@@ -36,6 +36,7 @@ constexpr unsigned long long TC_WAIT_CYCLES = 4000000000ull;   // ~2 s at 2 GHz
 
 struct TcGemmArgs {
   int M, N, K;
+  int batch;             // batch entries (z extent of the tile space)
   const int* a_index;    // batch entry -> z coordinate of A (null: b)
   const int* b_index;    // batch entry -> z coordinate of B (null: b)
   // operand scales: per-row arrays [z][rows] (A rows = output rows, B rows = output cols) or constants
@@ -49,9 +50,11 @@ struct TcSmem {
   static constexpr int A_BYTES = TC_BM * TC_BK * 2;            // 8 KB per digit plane
   static constexpr int B_BYTES = TC_BN * TC_BK * 2;            // 8 KB
   static constexpr int STAGE_BYTES = S * (A_BYTES + B_BYTES);
-  static constexpr int STAGES = (S == 4) ? 3 : 4;
+  static constexpr int STAGES = (S == 4) ? 2 : 3;
+  static constexpr int STG_LD = TC_BN + 1;                      // staging row stride (floats), bank-conflict free
+  static constexpr int STAGING_BYTES = TC_BM * STG_LD * 4;
   static constexpr int TMEM_COLS = 512;                        // 3 x 128 used
-  static constexpr int BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 1024 /*barriers, scales*/;
 };
 
 // ----------------------------------------------------------------- PTX helpers
@@ -164,22 +167,34 @@ struct TcMaps {
   CUtensorMap b[4];
 };
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Persistent: CTA c takes tiles c, c + gridDim.x, ...; tile t = (entry, row block,
+// column block) with the column block fastest.  The producer and the MMA
+// issuer run ahead through the shared-memory ring; the epilogue drains the
+// tensor-memory accumulators of a tile into a shared staging tile, releases
+// tensor memory (the next tile's MMAs start), then runs the element-wise
+// epilogue from shared memory with coalesced global accesses.
 template <int S>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
   using SM = TcSmem<S>;
-  const int b = blockIdx.z;
-  if (epi_skip(e, b)) return;
-
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t bars = base + SM::STAGES * SM::STAGE_BYTES;
+  float* staging = reinterpret_cast<float*>(gbase + SM::STAGES * SM::STAGE_BYTES);
+  uint8_t* tail = gbase + SM::STAGES * SM::STAGE_BYTES + SM::STAGING_BYTES;
+  const uint32_t bars = smem_u32(tail);
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (SM::STAGES + s); };
   const uint32_t accum_bar = bars + 8u * (2 * SM::STAGES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + SM::STAGES * SM::STAGE_BYTES + 8 * (2 * SM::STAGES + 1));
+  const uint32_t tmem_empty_bar = accum_bar + 8u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + 8 * (2 * SM::STAGES + 2));
+  float* colscale = reinterpret_cast<float*>(tail + 512);      // 128 floats
   __shared__ double red[4];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -189,6 +204,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       mbar_init(empty_bar(s), 1);
     }
     mbar_init(accum_bar, 1);
+    mbar_init(tmem_empty_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -202,25 +218,34 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int tile_m = blockIdx.y * TC_BM, tile_n = blockIdx.x * TC_BN;
-  const int za = g.a_index ? g.a_index[b] : b;
-  const int zb = g.b_index ? g.b_index[b] : b;
+  const int tiles_m = (g.M + TC_BM - 1) / TC_BM, tiles_n = (g.N + TC_BN - 1) / TC_BN;
+  const int tiles_per_entry = tiles_m * tiles_n;
+  const int total = tiles_per_entry * g.batch;
   const int nk = (g.K + TC_BK - 1) / TC_BK;
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % SM::STAGES;
-        const uint32_t round = kb / SM::STAGES;
-        if (kb >= SM::STAGES && !mbar_wait(empty_bar(s), (round - 1) & 1, g.err)) break;
-        const uint32_t st = base + s * SM::STAGE_BYTES;
-        mbar_expect_tx(full_bar(s), SM::STAGE_BYTES);
-        const int kx = kb * TC_BK;
+      uint32_t q = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const int b = t / tiles_per_entry, tl = t % tiles_per_entry;
+        if (epi_skip(e, b)) continue;
+        const int tile_m = (tl / tiles_n) * TC_BM, tile_n = (tl % tiles_n) * TC_BN;
+        const int za = g.a_index ? g.a_index[b] : b;
+        const int zb = g.b_index ? g.b_index[b] : b;
+        for (int kb = 0; kb < nk; ++kb, ++q) {
+          const int s = q % SM::STAGES;
+          const uint32_t round = q / SM::STAGES;
+          if (q >= (uint32_t)SM::STAGES && !mbar_wait(empty_bar(s), (round - 1) & 1, g.err)) { ok = false; break; }
+          const uint32_t st = base + s * SM::STAGE_BYTES;
+          mbar_expect_tx(full_bar(s), SM::STAGE_BYTES);
+          const int kx = kb * TC_BK;
 #pragma unroll
-        for (int q = 0; q < S; ++q) {
-          tma_load_3d(st + q * SM::A_BYTES, &maps.a[q], full_bar(s), kx, tile_m, za);
-          tma_load_3d(st + S * SM::A_BYTES + q * SM::B_BYTES, &maps.b[q], full_bar(s), kx, tile_n, zb);
+          for (int p = 0; p < S; ++p) {
+            tma_load_3d(st + p * SM::A_BYTES, &maps.a[p], full_bar(s), kx, tile_m, za);
+            tma_load_3d(st + S * SM::A_BYTES + p * SM::B_BYTES, &maps.b[p], full_bar(s), kx, tile_n, zb);
+          }
         }
       }
     }
@@ -228,43 +253,65 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = tc_idesc();
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % SM::STAGES;
-        const uint32_t round = kb / SM::STAGES;
-        if (!mbar_wait(full_bar(s), round & 1, g.err)) break;
+      uint32_t q = 0, it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const int b = t / tiles_per_entry;
+        if (epi_skip(e, b)) continue;
+        if (it > 0 && !mbar_wait(tmem_empty_bar, (it - 1) & 1, g.err)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t st = base + s * SM::STAGE_BYTES;
+        for (int kb = 0; kb < nk; ++kb, ++q) {
+          const int s = q % SM::STAGES;
+          const uint32_t round = q / SM::STAGES;
+          if (!mbar_wait(full_bar(s), round & 1, g.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = base + s * SM::STAGE_BYTES;
 #pragma unroll
-        for (int k = 0; k < TC_BK / 16; ++k) {
-          const uint32_t koff = k * 32;   // 16 bf16 = 32 bytes inside the 64 B swizzle row
+          for (int k = 0; k < TC_BK / 16; ++k) {
+            const uint32_t koff = k * 32;   // 16 bf16 = 32 bytes inside the 64 B swizzle row
 #pragma unroll
-          for (int i = 0; i < Pairs<S>::N; ++i) {
-            const int pa = pair_a(i), pb = pair_b(i);
-            const int acc_id = pair_acc(pa, pb);
-            // first contribution of each accumulator in this tile starts it fresh
-            const bool first = (kb == 0 && k == 0) && (i == 0 || i == 1 || i == 3);
-            tc_mma(tmem + 128u * acc_id, sw64_desc(st + pa * SM::A_BYTES + koff),
-                   sw64_desc(st + S * SM::A_BYTES + pb * SM::B_BYTES + koff), idesc, first ? 0u : 1u);
+            for (int i = 0; i < Pairs<S>::N; ++i) {
+              const int pa = pair_a(i), pb = pair_b(i);
+              const int acc_id = pair_acc(pa, pb);
+              const bool first = (kb == 0 && k == 0) && (i == 0 || i == 1 || i == 3);
+              tc_mma(tmem + 128u * acc_id, sw64_desc(st + pa * SM::A_BYTES + koff),
+                     sw64_desc(st + S * SM::A_BYTES + pb * SM::B_BYTES + koff), idesc, first ? 0u : 1u);
+            }
           }
+          tc_commit(empty_bar(s));
         }
-        tc_commit(empty_bar(s));
+        tc_commit(accum_bar);
+        ++it;
       }
-      tc_commit(accum_bar);
     }
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
-    const int q = warp & 3;
-    const int row = q * 32 + lane;
-    const bool ok = mbar_wait(accum_bar, 0, g.err);
-    tc_fence_after();
-    const long long gr = tile_m + row;
-    const double c0 = (double)e.inv_scale * epi_matrix_scale(e, b) * ldexp(1.0, -2 * DIGIT_BITS);
-    double sa = 0.0;
-    if (gr < g.M) sa = g.a_rowscale ? (double)g.a_rowscale[(long long)za * g.a_rs_stride + gr] : (double)g.a_scale;
-    double part = 0.0;
-    float rmax = 0.f;
-    const bool track = (e.kind == EPI_AFF) && e.C.rowmax != nullptr;
-    if (ok) {
+    const int q = warp & 3;                 // TMEM lane quadrant of this warp (rows q*32 ..)
+    const int ew = warp - 2;                // epilogue warp index 0..3
+    const int et = threadIdx.x - 64;        // epilogue thread index 0..127
+    const double c0 = (double)e.inv_scale * ldexp(1.0, -2 * DIGIT_BITS);
+    uint32_t it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const int b = t / tiles_per_entry, tl = t % tiles_per_entry;
+      if (epi_skip(e, b)) continue;
+      const int tile_m = (tl / tiles_n) * TC_BM, tile_n = (tl % tiles_n) * TC_BN;
+      const int za = g.a_index ? g.a_index[b] : b;
+      const int zb = g.b_index ? g.b_index[b] : b;
+      // column scales of this tile
+      {
+        const long long gc = tile_n + et;
+        colscale[et] = (gc < g.N) ? (g.b_rowscale ? g.b_rowscale[(long long)zb * g.b_rs_stride + gc] : g.b_scale) : 0.f;
+      }
+      const bool ok = mbar_wait(accum_bar, it & 1, g.err);
+      tc_fence_after();
+      epi_bar();
+      // ---- drain: tensor memory -> staging (scaled fp32)
+      const int row = q * 32 + lane;
+      const long long gr = tile_m + row;
+      const double sa = (gr < g.M) ? (g.a_rowscale ? (double)g.a_rowscale[(long long)za * g.a_rs_stride + gr]
+                                                    : (double)g.a_scale) : 0.0;
+      const float rs = (float)(c0 * sa);
+      float* srow = staging + row * SM::STG_LD;
 #pragma unroll 1
       for (int ch = 0; ch < TC_BN / 32; ++ch) {
         float v0[32], v1[32], v2[32];
@@ -272,28 +319,67 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
         tmem_ld32(taddr, v0);
         tmem_ld32(taddr + 128, v1);
         tmem_ld32(taddr + 256, v2);
-        if (gr < g.M) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const long long gc = tile_n + ch * 32 + j;
+        for (int j = 0; j < 32; ++j) srow[ch * 32 + j] = ((v0[j] + v1[j]) + v2[j]) * rs * colscale[ch * 32 + j];
+      }
+      tc_fence_before();
+      epi_bar();
+      if (et == 0) mbar_arrive(tmem_empty_bar);    // tensor memory may take the next tile
+      // ---- element-wise epilogue from staging
+      double part = 0.0;
+      if (ok) {
+        if (e.kind == EPI_VT) {
+          // transposed output: warp ew takes tile columns ew*32.., lanes run over rows
+          for (int cc = 0; cc < 32; ++cc) {
+            const int c = ew * 32 + cc;
+            const long long gc = tile_n + c;
+            float mx = 0.f;
             if (gc < g.N) {
-              const double sb = g.b_rowscale ? (double)g.b_rowscale[(long long)zb * g.b_rs_stride + gc]
-                                             : (double)g.b_scale;
-              const double acc = (((double)v0[j] + (double)v1[j]) + (double)v2[j]) * (c0 * sa * sb);
-              const double v = epi_apply<ENGINE_TC>(e, b, gr, gc, acc);
-              if (e.kind == EPI_M) part += v;
-              else rmax = fmaxf(rmax, (float)v);
+#pragma unroll
+              for (int r4 = 0; r4 < 4; ++r4) {
+                const int r = r4 * 32 + lane;
+                const long long grr = tile_m + r;
+                if (grr < g.M) {
+                  const float v = staging[r * SM::STG_LD + c];
+                  plane_store<ENGINE_TC>(e.C, b, gc, grr, (double)v);
+                  mx = fmaxf(mx, fabsf(v));
+                }
+              }
+            }
+            mx = warp_max(mx);
+            if (lane == 0 && gc < g.N && e.C.rowmax) atomic_max_nonneg(&e.C.rowmax[(long long)b * e.C.rows + gc], mx);
+          }
+        } else {
+          for (int rr = 0; rr < 32; ++rr) {
+            const int r = ew * 32 + rr;
+            const long long grr = tile_m + r;
+            float mx = 0.f;
+            if (grr < g.M) {
+#pragma unroll
+              for (int c4 = 0; c4 < 4; ++c4) {
+                const int c = c4 * 32 + lane;
+                const long long gc = tile_n + c;
+                if (gc < g.N) {
+                  const double v = epi_apply<ENGINE_TC>(e, b, grr, gc, (double)staging[r * SM::STG_LD + c]);
+                  if (e.kind == EPI_M) part += v;
+                  else mx = fmaxf(mx, (float)v);
+                }
+              }
+            }
+            if (e.kind == EPI_AFF && e.C.rowmax) {
+              mx = warp_max(mx);
+              if (lane == 0 && grr < g.M) atomic_max_nonneg(&e.C.rowmax[(long long)b * e.C.rows + grr], mx);
             }
           }
         }
       }
-      if (track && gr < g.M) atomic_max_nonneg(&e.C.rowmax[(long long)b * e.C.rows + gr], rmax);
-    }
-    if (e.kind == EPI_M) {
-      part = warp_sum(part);
-      if (lane == 0) red[q] = part;
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (warp == 2) epi_m_finish(e, b, red[0] + red[1] + red[2] + red[3], g.M, blockIdx.y * gridDim.x + blockIdx.x);
+      if (e.kind == EPI_M) {
+        part = warp_sum(part);
+        if (lane == 0) red[ew] = part;
+      }
+      epi_bar();                          // staging free; residual parts visible
+      if (e.kind == EPI_M && ew == 0) epi_m_finish(e, b, red[0] + red[1] + red[2] + red[3], g.M, tl);
+      ++it;
     }
   }
 

@@ -113,6 +113,7 @@ struct precond_ctx {
   size_t gemm_ev_used = 0;
   EncodeTiledFn encode = nullptr;
   bool tc_attr_set = false;
+  int num_sms = 148;
 };
 
 namespace {
@@ -171,12 +172,6 @@ Slab make_slab(Layout& L, int eng, int batch, int rows, int cols, int digits = 4
   return s;
 }
 
-float pow2_ceil_host(double x) {
-  if (!(x > 0)) return 1.f;
-  int e;
-  const double f = std::frexp(x, &e);
-  return f == 0.5 ? (float)x : std::ldexp(1.0f, e);
-}
 
 struct MetaWriter {
   std::vector<uint8_t>& buf;
@@ -490,8 +485,10 @@ int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int 
     g.b_rs_stride = B.rows;
     g.b_scale = B.scale;
     g.err = c.err();
-    dim3 grid((N + TC_BN - 1) / TC_BN, (M + TC_BM - 1) / TC_BM, batch);
-    e.tiles_per_entry = grid.x * grid.y;
+    g.batch = batch;
+    const long long tiles = (long long)((N + TC_BN - 1) / TC_BN) * ((M + TC_BM - 1) / TC_BM);
+    e.tiles_per_entry = (unsigned int)tiles;
+    dim3 grid((unsigned int)std::min<long long>(tiles * batch, (long long)c.h->num_sms), 1, 1);
     const bool timed = c.h->timing && c.h->events && c.h->in_ns;
     if (timed) {
       while (c.h->gemm_ev.size() < c.h->gemm_ev_used + 2) {
@@ -804,6 +801,7 @@ int prepare_device(precond_ctx* h) {
   if (!h->tc_attr_set) {
     CK(cudaFuncSetAttribute(gemm_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<4>::BYTES));
     CK(cudaFuncSetAttribute(gemm_tc_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<3>::BYTES));
+    CK(cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device));
     h->tc_attr_set = true;
   }
   return PRECOND_OK;
