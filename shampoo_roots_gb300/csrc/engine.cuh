@@ -32,18 +32,21 @@ struct Plane {
   int rows;             // rows per batch entry (rowmax stride)
 };
 
-__device__ __forceinline__ void digits_store(const Plane& p, long long o, double v, double sigma) {
-  // v = sigma * 2^-7 * (d_1 + d_2 2^-7 + ...), integer digits, round to nearest
-  double r = v / sigma * 128.0;
+// Digits of an fp32 value: y = v / sigma * 2^7 (exact: sigma is a power of
+// two), d_1 = rint(y), y <- (y - d_1) * 2^7 (exact: y - rint(y) needs no more
+// bits than y), ...  All steps are exact in fp32, so S = 4 digits (28 bits)
+// hold every fp32 value of the row whose magnitude is within 2^-4 of sigma.
+__device__ __forceinline__ void digits_store(const Plane& p, long long o, float v, float inv_sigma) {
+  float r = v * inv_sigma * 128.0f;
   __nv_bfloat16* base = reinterpret_cast<__nv_bfloat16*>(p.hi) + o;
-  double w = 1.0;
+  float w = 1.0f;
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     if (s < p.S) {
-      const double d = rint(r);
-      base[s * p.pstride] = __float2bfloat16_rn((float)(d * w));   // exact: |d| <= 129, power-of-two weight
-      r = (r - d) * 128.0;
-      w *= 0.0078125;
+      const float d = rintf(r);
+      base[s * p.pstride] = __float2bfloat16_rn(d * w);   // exact: |d| <= 129, power-of-two weight
+      r = (r - d) * 128.0f;
+      w *= 0.0078125f;
     }
   }
 }
@@ -55,7 +58,7 @@ __device__ __forceinline__ void plane_store(const Plane& p, int b, long long i, 
     reinterpret_cast<double*>(p.hi)[o] = v;
   } else {
     if (p.f32) p.f32[o] = (float)v;
-    else digits_store(p, o, v, (double)p.scale);
+    else digits_store(p, o, (float)v, 1.0f / p.scale);
   }
 }
 
@@ -153,6 +156,50 @@ __device__ __forceinline__ double epi_apply(const Epi& e, int b, long long i, lo
     }
   }
   return 0.0;
+}
+
+// The same epilogues in fp32 for the tcgen05 engine (its outputs are fp32, and
+// fp64 arithmetic is slow on this GPU).  Returns the residual part (EPI_M) or
+// |value| (for row maxima).
+__device__ __forceinline__ float epi_apply_tc(const Epi& e, int b, long long i, long long j, float acc) {
+  switch (e.kind) {
+    case EPI_STORE: {
+      const long long o = (long long)b * e.C.bstride + i * e.C.ld + j;
+      e.C.f32[o] = acc;
+      return fabsf(acc);
+    }
+    case EPI_AFF: {
+      const long long o = (long long)b * e.C.bstride + i * e.C.ld + j;
+      const float in = e.In.f32[(long long)b * e.In.bstride + i * e.In.ld + j];
+      float v = fmaf((float)e.alpha, acc, (float)e.beta_in * in);
+      if (i == j) v += (float)e.gamma;
+      e.C.f32[o] = v;
+      return fabsf(v);
+    }
+    case EPI_M: {
+      const long long o = (long long)b * e.C.bstride + i * e.C.ld + j;
+      const float in = e.In.f32[(long long)b * e.In.bstride + i * e.In.ld + j];
+      const float v = fmaf((float)e.beta_in, in, acc);
+      e.C.f32[o] = v;
+      const float r = v - ((i == j) ? 1.0f : 0.0f);
+      return r * r;
+    }
+    case EPI_GRAM: {
+      float* s = e.state[b];
+      const long long o = i * e.cols + j;
+      s[o] = fmaf(e.beta, s[o], (1.0f - e.beta) * acc);
+      return 0.f;
+    }
+    case EPI_U: {
+      const long long o = i * e.cols + j;
+      if (e.out_dtype == PRECOND_BF16)
+        reinterpret_cast<__nv_bfloat16*>(e.out[b])[o] = __float2bfloat16_rn(acc);
+      else
+        reinterpret_cast<float*>(e.out[b])[o] = acc;
+      return 0.f;
+    }
+  }
+  return 0.f;
 }
 
 // Should this batch entry be skipped?  (root converged, or input non-finite)

@@ -37,6 +37,8 @@ constexpr unsigned long long TC_WAIT_CYCLES = 4000000000ull;   // ~2 s at 2 GHz
 struct TcGemmArgs {
   int M, N, K;
   int batch;             // batch entries (z extent of the tile space)
+  int sym;               // 1: the product is symmetric (M == N): compute tiles with row block <=
+                         //    column block only and write each off-diagonal tile mirrored too
   const int* a_index;    // batch entry -> z coordinate of A (null: b)
   const int* b_index;    // batch entry -> z coordinate of B (null: b)
   // operand scales: per-row arrays [z][rows] (A rows = output rows, B rows = output cols) or constants
@@ -167,6 +169,23 @@ struct TcMaps {
   CUtensorMap b[4];
 };
 
+// Tile `tl` of a batch entry -> (row block, column block); symmetric products
+// enumerate the upper triangle row by row.
+__device__ __forceinline__ void tile_coords(int tl, int tiles_n, int sym, int& ti, int& tj) {
+  if (!sym) {
+    ti = tl / tiles_n;
+    tj = tl % tiles_n;
+    return;
+  }
+  int r = 0;
+  while (tl >= tiles_n - r) {
+    tl -= tiles_n - r;
+    ++r;
+  }
+  ti = r;
+  tj = r + tl;
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -219,7 +238,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
   const uint32_t tmem = *tmem_slot;
 
   const int tiles_m = (g.M + TC_BM - 1) / TC_BM, tiles_n = (g.N + TC_BN - 1) / TC_BN;
-  const int tiles_per_entry = tiles_m * tiles_n;
+  const int tiles_per_entry = g.sym ? tiles_n * (tiles_n + 1) / 2 : tiles_m * tiles_n;
   const int total = tiles_per_entry * g.batch;
   const int nk = (g.K + TC_BK - 1) / TC_BK;
 
@@ -231,7 +250,9 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const int b = t / tiles_per_entry, tl = t % tiles_per_entry;
         if (epi_skip(e, b)) continue;
-        const int tile_m = (tl / tiles_n) * TC_BM, tile_n = (tl % tiles_n) * TC_BN;
+        int ti, tj;
+        tile_coords(tl, tiles_n, g.sym, ti, tj);
+        const int tile_m = ti * TC_BM, tile_n = tj * TC_BN;
         const int za = g.a_index ? g.a_index[b] : b;
         const int zb = g.b_index ? g.b_index[b] : b;
         for (int kb = 0; kb < nk; ++kb, ++q) {
@@ -294,7 +315,10 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const int b = t / tiles_per_entry, tl = t % tiles_per_entry;
       if (epi_skip(e, b)) continue;
-      const int tile_m = (tl / tiles_n) * TC_BM, tile_n = (tl % tiles_n) * TC_BN;
+      int ti, tj;
+      tile_coords(tl, tiles_n, g.sym, ti, tj);
+      const int tile_m = ti * TC_BM, tile_n = tj * TC_BN;
+      const bool mirror = g.sym && ti != tj;
       const int za = g.a_index ? g.a_index[b] : b;
       const int zb = g.b_index ? g.b_index[b] : b;
       // column scales of this tile
@@ -326,7 +350,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       epi_bar();
       if (et == 0) mbar_arrive(tmem_empty_bar);    // tensor memory may take the next tile
       // ---- element-wise epilogue from staging
-      double part = 0.0;
+      float part = 0.f;
       if (ok) {
         if (e.kind == EPI_VT) {
           // transposed output: warp ew takes tile columns ew*32.., lanes run over rows
@@ -341,7 +365,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
                 const long long grr = tile_m + r;
                 if (grr < g.M) {
                   const float v = staging[r * SM::STG_LD + c];
-                  plane_store<ENGINE_TC>(e.C, b, gc, grr, (double)v);
+                  e.C.f32[(long long)b * e.C.bstride + gc * e.C.ld + grr] = v;
                   mx = fmaxf(mx, fabsf(v));
                 }
               }
@@ -350,6 +374,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
             if (lane == 0 && gc < g.N && e.C.rowmax) atomic_max_nonneg(&e.C.rowmax[(long long)b * e.C.rows + gc], mx);
           }
         } else {
+          const bool track = (e.kind == EPI_AFF || e.kind == EPI_M) && e.C.rowmax;
           for (int rr = 0; rr < 32; ++rr) {
             const int r = ew * 32 + rr;
             const long long grr = tile_m + r;
@@ -360,22 +385,81 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
                 const int c = c4 * 32 + lane;
                 const long long gc = tile_n + c;
                 if (gc < g.N) {
-                  const double v = epi_apply<ENGINE_TC>(e, b, grr, gc, (double)staging[r * SM::STG_LD + c]);
-                  if (e.kind == EPI_M) part += v;
-                  else mx = fmaxf(mx, (float)v);
+                  float* sp = &staging[r * SM::STG_LD + c];
+                  const float acc = *sp;
+                  const float v = epi_apply_tc(e, b, grr, gc, acc);
+                  if (e.kind == EPI_M) {
+                    part += mirror ? 2.f * v : v;
+                    const long long o = (long long)b * e.C.bstride + grr * e.C.ld + gc;
+                    mx = fmaxf(mx, fabsf(e.C.f32[o]));
+                    if (g.sym) *sp = e.C.f32[o];
+                  } else {
+                    mx = fmaxf(mx, v);
+                    if (g.sym && e.kind != EPI_GRAM) *sp = e.C.f32[(long long)b * e.C.bstride + grr * e.C.ld + gc];
+                  }
                 }
               }
             }
-            if (e.kind == EPI_AFF && e.C.rowmax) {
+            if (track) {
               mx = warp_max(mx);
               if (lane == 0 && grr < g.M) atomic_max_nonneg(&e.C.rowmax[(long long)b * e.C.rows + grr], mx);
+            }
+          }
+          if (g.sym && !mirror && (e.kind == EPI_AFF || e.kind == EPI_M)) {
+            // diagonal tile: its lower triangle takes the upper triangle's values, so
+            // the result is exactly symmetric (the iteration amplifies any
+            // antisymmetric part while M is far from I)
+            epi_bar();
+            for (int rr = 0; rr < 32; ++rr) {
+              const int r = ew * 32 + rr;
+              const long long grr = tile_m + r;
+              if (grr >= g.M) continue;
+#pragma unroll
+              for (int c4 = 0; c4 < 4; ++c4) {
+                const int c = c4 * 32 + lane;
+                const long long gc = tile_n + c;
+                if (c < r && gc < g.N)
+                  e.C.f32[(long long)b * e.C.bstride + grr * e.C.ld + gc] = staging[c * SM::STG_LD + r];
+              }
+            }
+          }
+          if (mirror) {
+            // the mirrored tile (rows tile_n.., columns tile_m..) = transpose of this one
+            __syncwarp();
+            epi_bar();
+            for (int cc = 0; cc < 32; ++cc) {
+              const int c = ew * 32 + cc;                 // tile column = mirrored row
+              const long long gc = tile_n + c;
+              float mx = 0.f;
+              if (gc < g.N) {
+#pragma unroll
+                for (int r4 = 0; r4 < 4; ++r4) {
+                  const int r = r4 * 32 + lane;            // tile row = mirrored column
+                  const long long grr = tile_m + r;
+                  if (grr < g.M) {
+                    const float v = staging[r * SM::STG_LD + c];
+                    if (e.kind == EPI_GRAM) {
+                      float* st = e.state[b];
+                      const long long o = gc * e.cols + grr;
+                      st[o] = fmaf(e.beta, st[o], (1.0f - e.beta) * v);
+                    } else {
+                      e.C.f32[(long long)b * e.C.bstride + gc * e.C.ld + grr] = v;
+                      mx = fmaxf(mx, fabsf(v));
+                    }
+                  }
+                }
+              }
+              if (track) {
+                mx = warp_max(mx);
+                if (lane == 0 && gc < g.N) atomic_max_nonneg(&e.C.rowmax[(long long)b * e.C.rows + gc], mx);
+              }
             }
           }
         }
       }
       if (e.kind == EPI_M) {
-        part = warp_sum(part);
-        if (lane == 0) red[ew] = part;
+        const double pd = warp_sum((double)part);
+        if (lane == 0) red[ew] = pd;
       }
       epi_bar();                          // staging free; residual parts visible
       if (e.kind == EPI_M && ew == 0) epi_m_finish(e, b, red[0] + red[1] + red[2] + red[3], g.M, tl);

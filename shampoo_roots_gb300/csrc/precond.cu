@@ -444,7 +444,7 @@ int encode_map(precond_ctx* h, CUtensorMap* map, void* base, const Slab& s, int 
 // Batched product C_b = A_b B_b^T in the engine of the operands; the tcgen05
 // engine uses the first `S` digit planes of each operand (S = 3 or 4).
 int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int K, const int* aidx,
-         const int* bidx, int S, const Epi& e0, int batch) {
+         const int* bidx, int S, const Epi& e0, int batch, bool sym = false) {
   Epi e = e0;
   if (eng == ENGINE_F64) {
     GemmF64Args g;
@@ -486,7 +486,9 @@ int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int 
     g.b_scale = B.scale;
     g.err = c.err();
     g.batch = batch;
-    const long long tiles = (long long)((N + TC_BN - 1) / TC_BN) * ((M + TC_BM - 1) / TC_BM);
+    g.sym = (sym && M == N) ? 1 : 0;
+    const long long tn = (N + TC_BN - 1) / TC_BN;
+    const long long tiles = g.sym ? tn * (tn + 1) / 2 : tn * ((M + TC_BM - 1) / TC_BM);
     e.tiles_per_entry = (unsigned int)tiles;
     dim3 grid((unsigned int)std::min<long long>(tiles * batch, (long long)c.h->num_sms), 1, 1);
     const bool timed = c.h->timing && c.h->events && c.h->in_ns;
@@ -623,7 +625,7 @@ int launch_iterations(const Ctx& c) {
         ea.gamma = 0.0;
         int rc2;
         if (tc && (rc2 = clear_rowmax(c, C))) return rc2;
-        if ((rc2 = gemm(c, eng, A, B, d, d, d, nullptr, nullptr, 4, ea, nb))) return rc2;
+        if ((rc2 = gemm(c, eng, A, B, d, d, d, nullptr, nullptr, 4, ea, nb, true))) return rc2;
         ++n;
         if (tc && (rc2 = slice(c, C))) return rc2;
         return PRECOND_OK;
@@ -640,21 +642,12 @@ int launch_iterations(const Ctx& c) {
       em.C = c.plane(r.M[nxt]);
       em.In = c.plane(r.M[cur]);
       em.beta_in = std::pow(tau, p);
-      if ((rcode = gemm(c, eng, *Pk, r.M[cur], d, d, d, nullptr, nullptr, 4, em, nb))) return rcode;
+      // symmetric product (upper-triangle tiles mirrored): M' is exactly symmetric,
+      // which also removes the antisymmetric mode the iteration would amplify
+      if (tc && (rcode = clear_rowmax(c, r.M[nxt]))) return rcode;
+      if ((rcode = gemm(c, eng, *Pk, r.M[cur], d, d, d, nullptr, nullptr, 4, em, nb, true))) return rcode;
       ++n;
-      if (tc) {
-        if ((rcode = clear_rowmax(c, r.M[nxt]))) return rcode;
-        SymArgs sa;
-        sa.M = c.plane(r.M[nxt]);
-        sa.root_of = root_of;
-        sa.stats = c.stats();
-        sa.d = d;
-        const int tb = (d + 31) / 32;
-        sym_m_kernel<<<dim3(tb, tb, nb), 256, 0, c.st>>>(sa);
-        c.h->launches++;
-        CK(cudaGetLastError());
-        if ((rcode = slice(c, r.M[nxt]))) return rcode;
-      }
+      if (tc && (rcode = slice(c, r.M[nxt]))) return rcode;
     }
   }
   c.h->ns_launches = n;
@@ -744,7 +737,7 @@ int run_step(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream_t 
       e.beta = beta;
       e.nonfinite_of = c.at<const int>(s.t_roots2);
       const Slab& G = tc ? (side == 0 ? s.Gq : s.GTq) : (side == 0 ? s.Gd : s.GTd);
-      if ((rc = gemm(c, s.eng, G, G, dim, dim, K, nullptr, nullptr, 4, e, nb))) return rc;
+      if ((rc = gemm(c, s.eng, G, G, dim, dim, K, nullptr, nullptr, 4, e, nb, true))) return rc;
     }
   }
   if ((rc = record(h, 1, st))) return rc;

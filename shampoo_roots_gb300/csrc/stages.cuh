@@ -127,11 +127,12 @@ __global__ void __launch_bounds__(256) slice_rows_kernel(SliceArgs a) {
   const int b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int r = blockIdx.x * 8 + warp; r < a.rows; r += gridDim.x * 8) {
-    const double sigma = (double)pow2_ceil(a.rowmax[(long long)b * a.rows + r]);
-    if (lane == 0) a.rowscale[(long long)b * a.rows + r] = (float)sigma;
+    const float sigma = pow2_ceil(a.rowmax[(long long)b * a.rows + r]);
+    if (lane == 0) a.rowscale[(long long)b * a.rows + r] = sigma;
+    const float inv = 1.0f / sigma;          // exact: sigma is a power of two
     const float* src = a.src + (long long)b * a.src_bstride + (long long)r * a.src_ld;
     const long long o = (long long)b * a.dst.bstride + (long long)r * a.dst.ld;
-    for (int c = lane; c < a.cols; c += 32) digits_store(a.dst, o + c, (double)src[c], sigma);
+    for (int c = lane; c < a.cols; c += 32) digits_store(a.dst, o + c, src[c], inv);
   }
 }
 
@@ -266,7 +267,8 @@ __global__ void __launch_bounds__(256) root_init_kernel(RootArgs a) {
     float mx = 0.f, xx = 0.f;
     if (r < a.d && col < a.d) {
       const double id = (r == col) ? 1.0 : 0.0;
-      const double m0 = ((double)A[(long long)r * a.d + col] / t + eps * id) / c;
+      const double a_sym = 0.5 * ((double)A[(long long)r * a.d + col] + (double)A[(long long)col * a.d + r]);
+      const double m0 = (a_sym / t + eps * id) / c;
       const double x1 = ((p + 1.0) * id - m0) / p;
       plane_store<E>(a.M0, b, r, col, m0);
       plane_store<E>(a.X1, b, r, col, x1);
