@@ -236,7 +236,7 @@ def main():
 
     # ---------------- timed region (device-resident inputs)
     launches0 = sr.precond_launch_count(pc.h)
-    ns_ms, ns_flops, gemm_ms, gemm_n, root_flops = 0.0, 0.0, 0.0, 0, 0.0
+    ns_ms, ns_flops, gemm_ms, gemm_n, root_flops, issued_flops = 0.0, 0.0, 0.0, 0, 0.0, 0.0
     stage_ms = [0.0, 0.0, 0.0, 0.0]
     iters_seen = []
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -246,7 +246,8 @@ def main():
         for i in range(args.steps):
             step(i)
             ms, nl, fl = sr.precond_get_timing(pc.h)     # synchronises the step
-            gms, gn = sr.precond_get_gemm_timing(pc.h)
+            gms, gn, gis = sr.precond_get_gemm_timing(pc.h)
+            issued_flops += gis
             ns_ms += ms[2]
             stage_ms = [a + b for a, b in zip(stage_ms, ms)]
             root_flops += fl
@@ -297,7 +298,8 @@ def main():
     # dominant kernel: the tcgen05 GEMM of the iteration stage (timed inside a long step -> sustained peak)
     achieved = (root_flops / (gemm_ms / 1e3) / 1e12) if gemm_ms > 0 else None
     peak = peaks["bf16_tflops_sustained"]
-    issued = achieved * 10 if achieved else None     # 10 bf16 digit products per logical product
+    # issued: tiles actually run (upper triangles of symmetric products) x 10 bf16 digit products
+    issued = (issued_flops / (gemm_ms / 1e3) / 1e12) if gemm_ms > 0 else None
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": (achieved / peak) if achieved else None, "traffic": None,
                 "kernel": "gemm_tc_kernel<4> (iteration-stage products)",

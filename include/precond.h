@@ -140,9 +140,11 @@ int precond_get_timing(precond_t h, double ms[4], int64_t* ns_gemm_launches, dou
 /*
  * With PRECOND_OPT_TIMING on: total milliseconds of the tcgen05 GEMM launches
  * of the last call's iteration stage (CUDA events around each launch on the
- * call's stream; synchronises) and their number.
+ * call's stream; synchronises), their number, and the bf16 MMA FLOPs they
+ * issued (tiles launched x 2 x 128 x 128 x K x digit products per tile step).
+ * Any output pointer may be NULL.
  */
-int precond_get_gemm_timing(precond_t h, double* ms_total, int64_t* launches);
+int precond_get_gemm_timing(precond_t h, double* ms_total, int64_t* launches, double* issued_flops);
 
 /* Kernel launches this handle has issued since creation (every library kernel). */
 int64_t precond_launch_count(precond_t h);

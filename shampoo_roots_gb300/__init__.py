@@ -48,7 +48,7 @@ def load():
     L.precond_set_option.argtypes = [vp, i32, f64]
     L.precond_get_timing.argtypes = [vp, ctypes.POINTER(f64), ctypes.POINTER(i64), ctypes.POINTER(f64)]
     L.precond_launch_count.argtypes = [vp]
-    L.precond_get_gemm_timing.argtypes = [vp, ctypes.POINTER(f64), ctypes.POINTER(i64)]
+    L.precond_get_gemm_timing.argtypes = [vp, ctypes.POINTER(f64), ctypes.POINTER(i64), ctypes.POINTER(f64)]
     L.precond_launch_count.restype = i64
     L.precond_get_root.argtypes = [vp, i32, vp, vp]
     L.precond_debug_plane.argtypes = [vp, i32, i32, vp, vp]
@@ -180,10 +180,13 @@ def precond_get_timing(h):
 
 
 def precond_get_gemm_timing(h):
+    """(milliseconds, launches, issued bf16 MMA FLOPs) of the last call's iteration-stage GEMMs."""
     ms = ctypes.c_double()
     n = ctypes.c_int64()
-    _check(load().precond_get_gemm_timing(h, ctypes.byref(ms), ctypes.byref(n)), "precond_get_gemm_timing")
-    return ms.value, n.value
+    fl = ctypes.c_double()
+    _check(load().precond_get_gemm_timing(h, ctypes.byref(ms), ctypes.byref(n), ctypes.byref(fl)),
+           "precond_get_gemm_timing")
+    return ms.value, n.value, fl.value
 
 
 def precond_launch_count(h) -> int:

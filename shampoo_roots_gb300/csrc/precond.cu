@@ -109,6 +109,7 @@ struct precond_ctx {
   int64_t launches = 0;
   int64_t ns_launches = 0;
   bool in_ns = false;                  // timing: inside the iteration stage
+  double ns_issued = 0.0;              // issued bf16 MMA FLOPs of the iteration stage (tile work x digit pairs)
   std::vector<cudaEvent_t> gemm_ev;    // timing: start/stop pairs around iteration-stage GEMMs
   size_t gemm_ev_used = 0;
   EncodeTiledFn encode = nullptr;
@@ -209,7 +210,7 @@ void layout_root_class(Layout& L, RootClass& r, int p) {
   }
   r.D = make_slab(L, e, nb, d, d, 4, true);
   if (p == 4) r.F = make_slab(L, e, nb, d, d, 4, true);
-  r.Xf = make_slab(L, e, nb, d, d, 4, true);
+  r.Xf = r.D;   // D is free once the iteration ends; the finished root takes its place
   r.rowabs = L.take((size_t)nb * d * sizeof(double));
   r.diag = L.take((size_t)nb * d * sizeof(double));
   r.rowsq = L.take((size_t)nb * d * sizeof(double));
@@ -492,6 +493,10 @@ int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int 
     e.tiles_per_entry = (unsigned int)tiles;
     dim3 grid((unsigned int)std::min<long long>(tiles * batch, (long long)c.h->num_sms), 1, 1);
     const bool timed = c.h->timing && c.h->events && c.h->in_ns;
+    if (c.h->in_ns) {
+      const long long kpad = (long long)((K + TC_BK - 1) / TC_BK) * TC_BK;
+      c.h->ns_issued += (double)tiles * batch * 2.0 * TC_BM * TC_BN * kpad * (S == 4 ? 10 : 6);
+    }
     if (timed) {
       while (c.h->gemm_ev.size() < c.h->gemm_ev_used + 2) {
         cudaEvent_t ev;
@@ -586,6 +591,7 @@ int launch_roots_start(const Ctx& c, float eps) {
 int launch_iterations(const Ctx& c) {
   c.h->in_ns = true;
   c.h->gemm_ev_used = 0;
+  c.h->ns_issued = 0.0;
   struct Guard { precond_ctx* h; ~Guard() { h->in_ns = false; } } guard{c.h};
   const int p = c.P.p;
   int kall = 0;
@@ -1025,7 +1031,7 @@ int precond_get_timing(precond_t h, double ms[4], int64_t* ns_gemm_launches, dou
 
 int64_t precond_launch_count(precond_t h) { return h ? h->launches : -1; }
 
-int precond_get_gemm_timing(precond_t h, double* ms_total, int64_t* launches) {
+int precond_get_gemm_timing(precond_t h, double* ms_total, int64_t* launches, double* issued_flops) {
   if (!h) return PRECOND_EINVAL;
   if (h->device < 0) return PRECOND_ENODEV;
   if (!h->have_last || !h->timing || !h->events) return PRECOND_EINVAL;
@@ -1038,6 +1044,7 @@ int precond_get_gemm_timing(precond_t h, double* ms_total, int64_t* launches) {
   }
   if (ms_total) *ms_total = t;
   if (launches) *launches = (int64_t)(h->gemm_ev_used / 2);
+  if (issued_flops) *issued_flops = h->ns_issued;
   return PRECOND_OK;
 }
 

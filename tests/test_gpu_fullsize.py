@@ -12,12 +12,13 @@ from workloads import synth
 pytestmark = pytest.mark.gpu
 
 
-def _stack_parity(index, steps, power):
+def _stack_parity(index, steps, power, sample=None):
     import torch
     import shampoo_roots_gb300 as sr
     w = synth.workload(index)
     shapes = list(w.shapes)
-    sample = sorted({shapes.index(s) for s in set(shapes)})     # first matrix of each shape class
+    if sample is None:
+        sample = sorted({shapes.index(s) for s in set(shapes)})     # first matrix of each shape class
     dev = torch.device("cuda")
     L = [torch.zeros((m, m), device=dev) for m, _ in shapes]
     R = [torch.zeros((n, n), device=dev) for _, n in shapes]
@@ -54,6 +55,13 @@ def test_stack_quarter_power_full_size():
 def test_stack_inverse_sqrt_full_size():
     """Same stack, power -1/2, 10 EMA steps."""
     _stack_parity(2, 10, -0.5)
+
+
+def test_wide_6144_full_size():
+    """16 fp32 gradients of 6144^2 and 16 of 6144x3072 (alpha -0.5), power -1/4,
+    4 EMA steps; the oracle recomputes one 6144x3072 matrix (its 6144^2 left
+    and 3072^2 right Grams) at every step."""
+    _stack_parity(4, 4, -0.25, sample=[16])
 
 
 @pytest.mark.parametrize("power", [-0.25, -0.5])
