@@ -5,11 +5,13 @@ coupled Newton-Schulz roots, two-sided apply) over one batch of synthetic
 gradients of the 24-layer d = 1024 transformer stack (bf16 gradients, fp32
 Grams, power -1/4): 144 weight matrices, 288 roots.
 
-Prints ONE JSON line (rank 0).  `value` is whole-job algorithmic TFLOP/s of
-the step (2mnk per logical GEMM, iterations actually executed); `e2e` is the
-same metric with the gradients copied from pinned host memory and the
-update copied back inside the timed region.  `--impl reference` times the
-float64 CPU oracle on a bounded sample of the same workload.
+Prints ONE JSON line (rank 0).  `value` is whole-job throughput in
+preconditioner steps per second (1000 / ms_per_step per GPU, summed over
+ranks); `tflops_algorithmic` is the step's algorithmic FLOPs (2mnk per logical
+GEMM, iterations actually executed) over its time; `e2e` is the throughput
+with the gradients copied from pinned host memory and the update copied back
+inside the timed region.  `--impl reference` times the float64 CPU oracle on
+a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -150,15 +152,14 @@ def run_reference(args):
         secs.append(t)
     timed = secs[args.warmup:]
     per_step = statistics.median(timed)
-    # the step's algorithmic FLOPs at the iteration counts the GPU path runs (about 20 per root)
-    flops = step_flops_outside_roots(w.shapes) + sum(2.0 * d ** 3 * (20 * 4 - 1) for m, n in w.shapes for d in (m, n))
-    value = flops / per_step / 1e12
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+    value = 1.0 / per_step
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "preconditioner steps/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "matrices": len(w.shapes), "grad_dtype": w.dtype, "power": w.powers[0]},
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
-            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": {"value": value, "unit": "preconditioner steps/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "preconditioner steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
@@ -264,7 +265,8 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed = float(t.item())
     step_flops = step_flops_outside_roots(shapes) + root_flops / args.steps
-    value = world * step_flops * args.steps / elapsed / 1e12
+    value = world * args.steps / elapsed                       # preconditioner steps per second, whole job
+    tflops = world * step_flops * args.steps / elapsed / 1e12
     ms_per_step = elapsed / args.steps * 1e3
 
     # ---------------- end to end: pinned host gradients in, update out, inside the timed region
@@ -291,7 +293,7 @@ def main():
             t = torch.tensor([t_e2e], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             t_e2e = float(t.item())
-        e2e = {"value": world * step_flops * args.steps / t_e2e / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": world * args.steps / t_e2e, "unit": "preconditioner steps/s",
                "ms_per_step": t_e2e / args.steps * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     peaks = load_peaks()
@@ -310,11 +312,11 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         t_oracle, desc, cores = oracle_sample(w)
-        cpu = {"value": step_flops / t_oracle / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+        cpu = {"value": 1.0 / t_oracle, "unit": "preconditioner steps/s", "cores": cores, "kind": "oracle",
                "sample": desc, "ms_per_step_extrapolated": t_oracle * 1e3}
 
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        line = {"metric": METRIC, "value": value, "unit": "preconditioner steps/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": w.name, "matrices": len(shapes), "roots": 2 * len(shapes),
@@ -322,7 +324,8 @@ def main():
                            "mean_iterations": statistics.mean(iters_seen) if iters_seen else None,
                            "l2": "inputs larger than L2 (fp32 Gram state 4.6 GB, gradients 0.6 GB per batch)",
                            "numerics": "bf16 tensor-core digit products, exact fp32 accumulation of leading levels"},
-                "pct_tensor_peak": value / peaks["bf16_tflops"],
+                "tflops_algorithmic": tflops,
+                "pct_tensor_peak": tflops / peaks["bf16_tflops"],
                 "stages_ms_per_step": {k: v / args.steps for k, v in zip(
                     ("prep_gram", "bound_start", "iterations", "finish_apply"), stage_ms)},
                 "iteration_gemm_ms_per_step": gemm_ms / args.steps,

@@ -15,8 +15,10 @@
  * computed here without any eigensolver, by the coupled Newton-Schulz
  * iteration of "Online KL Shampoo" (Tilde Research), section 2.2 and the
  * Appendix D algorithm box, generalised to the inverse p-th root
- * (T = ((p+1) I - M) / p, X <- X T, M <- T^p M, X_0 = I, M_0 = A_hat / c,
- * c = 1.01 x the Appendix D upper bound on the largest eigenvalue), and it
+ * (T = alpha_k I - beta_k M, X <- X T, M <- T^p M, X_0 = I, M_0 = A_hat / c,
+ * c = 1.01 x the Appendix D upper bound on the largest eigenvalue; the
+ * classical step is alpha = (p+1)/p, beta = 1/p, the default is a per-step
+ * minimax choice in the spirit of the section 2.3 CANS coefficients), and it
  * stops when ||M - I||_F <= tol * sqrt(d) (M equals X^p A_hat / c in exact
  * arithmetic, so this is the residual of the inverse-root equation that
  * Appendix E calls explicit and measurable).
@@ -69,6 +71,10 @@ typedef struct precond_ctx* precond_t;
 #define PRECOND_OPT_WORKSPACE_MAX  6  /* workspace limit in bytes; 0 = unlimited (default) */
 #define PRECOND_OPT_TIMING         7  /* 1 = record per-stage CUDA events (read by precond_get_timing) */
 #define PRECOND_OPT_USE_GRAPH      8  /* 1 = capture the step as a CUDA graph and replay it (default 0) */
+#define PRECOND_OPT_CLASSICAL      9  /* 1 = classical Newton step (p+1)/p I - M/p at every iteration;
+                                         0 = per-step minimax step polynomial (default) */
+#define PRECOND_OPT_FOLD          10  /* minimax step: the interval's top may not fall below this
+                                         fraction of its bottom's factor, T(1) >= fold T(l); [0, 1), default 0.3 */
 
 /*
  * Create a handle bound to `cuda_device` (>= 0).  cuda_device = -1 creates a

@@ -50,6 +50,10 @@ struct Slab {   // an engine-format matrix batch inside the workspace
   size_t f32 = 0, rowmax = 0, rowscale = 0;   // fp32 form + per-row max / scale (0: absent)
 };
 
+struct StepPoly {       // per-iteration step polynomial coefficients T_k = alpha_k I - beta_k M
+  std::vector<double> alpha, beta;
+};
+
 struct RootClass {
   int d = 0, eng = 0;
   std::vector<int> roots;              // global root ids
@@ -60,6 +64,7 @@ struct RootClass {
   long long tiles = 0;
   size_t t_root = 0, t_src = 0, t_dst = 0;   // device tables (offsets)
   int kmax = 0;
+  StepPoly steps;                      // per-iteration step polynomial coefficients
 };
 
 struct ShapeClass {
@@ -90,6 +95,8 @@ struct precond_ctx {
   int device = -1;
   double tol = 1e-5;
   int max_iter = 0, min_iter = 4, engine = 0, small_dim = 512, timing = 0, use_graph = 0;
+  int classical = 0;                   // 1: classical Newton step polynomial at every iteration
+  double fold = 0.3;                   // minimax step: T(1) >= fold * T(l)
   double ws_max = 0;
   void* ws = nullptr;
   size_t ws_cap = 0;
@@ -140,6 +147,58 @@ int iter_cap(double eps, int d, int p, double tol, int user_max) {
   return std::min(k + 3, 60);
 }
 
+
+// Step polynomials of the iteration.  Every step uses T_k = alpha_k I - beta_k M_k
+// (X <- X T, M <- T^p M keep M = X^p M_0 for ANY such polynomial).  The
+// classical choice is alpha = (p+1)/p, beta = 1/p.  Here each step is the
+// minimax choice for the interval [l_k, 1] that holds M_k's spectrum: among
+// g(m) = m (a - m)^p, a in (1, p+1], take the one maximising
+// min(g(l), g(1)) / max_[l,1] g, then scale so the image's top is 1; the image
+// [l_{k+1}, 1] is the next interval (the idea of the Chebyshev-optimised
+// coefficients of "Online KL Shampoo" section 2.3, computed here for
+// any p from the interval alone).  From l_0 = 1e-6 it needs 10 steps at p = 4
+// where the classical step needs 20.
+static double step_ratio(double l, double a, int p, double* gmax_out) {
+  auto g = [&](double m) { return m * std::pow(a - m, p); };
+  const double ms = a / (p + 1);
+  double gmax = std::max(g(l), g(1.0));
+  if (ms > l && ms < 1.0) gmax = std::max(gmax, g(ms));
+  if (gmax_out) *gmax_out = gmax;
+  return std::min(g(l), g(1.0)) / gmax;
+}
+
+// `fold` caps how far a step may push the top of the interval below its
+// bottom: T(1) >= fold * T(l), i.e. a - 1 >= fold (a - l).  A deep fold
+// stores directions at tiny magnitudes for a step and costs accuracy; with
+// fold = 0.3 the step count at p = 4 is unchanged (10 from l = 1e-6).
+static StepPoly step_schedule(double l0, int p, int max_steps, double fold) {
+  StepPoly sp;
+  double l = l0;
+  for (int k = 0; k < max_steps; ++k) {
+    const double amin = std::max(1.0 + 1e-12, (1.0 - fold * l) / (1.0 - fold));
+    double best_a = p + 1.0, best_r = step_ratio(l, best_a, p, nullptr);
+    for (int i = 0; i <= 600; ++i) {      // coarse search on log(a - amin)
+      const double a = amin + std::pow(10.0, -10.0 + 10.0 * i / 600.0) * (p + 1.0 - amin);
+      if (a > p + 1.0) break;
+      const double r = step_ratio(l, a, p, nullptr);
+      if (r > best_r) { best_r = r; best_a = a; }
+    }
+    double lo = std::max(amin, amin + (best_a - amin) * 0.9), hi = std::min(p + 1.0, amin + (best_a - amin) * 1.1 + 1e-12);
+    for (int it = 0; it < 200; ++it) {    // golden refinement
+      const double m1 = lo + (hi - lo) * 0.381966, m2 = hi - (hi - lo) * 0.381966;
+      if (step_ratio(l, m1, p, nullptr) < step_ratio(l, m2, p, nullptr)) lo = m1; else hi = m2;
+    }
+    const double a = 0.5 * (lo + hi);
+    double gmax;
+    const double r = step_ratio(l, a, p, &gmax);
+    const double sc = std::pow(gmax, -1.0 / p);
+    sp.alpha.push_back(a * sc);
+    sp.beta.push_back(sc);
+    l = r;
+    if (1.0 - l < 1e-9) break;
+  }
+  return sp;
+}
 
 struct Layout {
   size_t top = 0;
@@ -290,7 +349,18 @@ int build_plan(precond_ctx* h, Plan& P, bool step, int count, const int64_t* dim
   P.err = L.take(64);
   for (auto& r : P.rc) {
     layout_root_class(L, r, p);
-    r.kmax = iter_cap(eps, r.d, p, h->tol, h->max_iter);
+    // interval of M_0's spectrum: [eps / c_max, 1], c_max = 1.01 tr(A_hat) >= c
+    r.steps = step_schedule(eps / (1.01 * (1.0 + r.d * eps)), p, 60, h->fold);
+    if (h->classical) {
+      r.steps.alpha.assign(r.steps.alpha.size(), (p + 1.0) / p);
+      r.steps.beta.assign(r.steps.beta.size(), 1.0 / p);
+    }
+    const int planned = h->classical ? iter_cap(eps, r.d, p, h->tol, 0) : (int)r.steps.alpha.size() + 3;
+    r.kmax = h->max_iter > 0 ? h->max_iter : std::min(planned, 60);
+    while ((int)r.steps.alpha.size() < std::max(r.kmax, 1)) {   // then Newton steps
+      r.steps.alpha.push_back((p + 1.0) / p);
+      r.steps.beta.push_back(1.0 / p);
+    }
     const long long t = r.eng == ENGINE_F64
         ? (long long)((r.d + F64_BM - 1) / F64_BM) * ((r.d + F64_BN - 1) / F64_BN)
         : (long long)((r.d + TC_BM - 1) / TC_BM) * ((r.d + TC_BN - 1) / TC_BN);
@@ -559,6 +629,8 @@ RootArgs root_args(const Ctx& c, const RootClass& r, float eps) {
   a.ctl.tol = (float)c.h->tol;
   a.M0 = c.plane(r.M[0]);     // fp32 form (tcgen05 engine), sliced after the start
   a.X1 = c.plane(r.X[1]);
+  a.alpha0 = r.steps.alpha[0];
+  a.beta0 = r.steps.beta[0];
   a.X[0] = c.plane(r.X[0]);   // read in fp32 form by the finish
   a.X[1] = c.plane(r.X[1]);
   a.Xf = c.plane(r.Xf);
@@ -620,8 +692,9 @@ int launch_iterations(const Ctx& c) {
       //   X' = X T = tau X - X M / p
       // so every product operand (M, D, F, X) keeps its information in its own
       // digits instead of next to a dominant identity.
-      const double tau = (p + 1.0) / p;
-      auto aff = [&](const Slab& A, const Slab& B, const Slab& In, const Slab& C, double alpha, double beta_in) -> int {
+      const double al = r.steps.alpha[k], be = r.steps.beta[k];
+      auto aff = [&](const Slab& A, const Slab& B, const Slab& In, const Slab& C, double alpha, double beta_in,
+                     int digits) -> int {
         Epi ea = e;
         ea.kind = EPI_AFF;
         ea.C = c.plane(C);
@@ -631,23 +704,25 @@ int launch_iterations(const Ctx& c) {
         ea.gamma = 0.0;
         int rc2;
         if (tc && (rc2 = clear_rowmax(c, C))) return rc2;
-        if ((rc2 = gemm(c, eng, A, B, d, d, d, nullptr, nullptr, 4, ea, nb, true))) return rc2;
+        if ((rc2 = gemm(c, eng, A, B, d, d, d, nullptr, nullptr, digits, ea, nb, true))) return rc2;
         ++n;
         if (tc && (rc2 = slice(c, C))) return rc2;
         return PRECOND_OK;
       };
-      if (k >= 1 && (rcode = aff(r.X[cur], r.M[cur], r.X[cur], r.X[nxt], -1.0 / p, tau))) return rcode;
-      if ((rcode = aff(r.M[cur], r.M[cur], r.M[cur], r.D, 1.0 / (p * p), -2.0 * tau / p))) return rcode;
+      // T = al I - be M:  T^2 = al^2 I + D, D = be^2 M M - 2 al be M;  T^4 = al^4 I + F,
+      // F = D D + 2 al^2 D;  M' = al^p M + (D or F) M;  X' = X T = al X - be X M
+      if (k >= 1 && (rcode = aff(r.X[cur], r.M[cur], r.X[cur], r.X[nxt], -be, al, 4))) return rcode;
+      if ((rcode = aff(r.M[cur], r.M[cur], r.M[cur], r.D, be * be, -2.0 * al * be, 4))) return rcode;
       const Slab* Pk = &r.D;
       if (p == 4) {
-        if ((rcode = aff(r.D, r.D, r.D, r.F, 1.0, 2.0 * tau * tau))) return rcode;
+        if ((rcode = aff(r.D, r.D, r.D, r.F, 1.0, 2.0 * al * al, 4))) return rcode;
         Pk = &r.F;
       }
       Epi em = e;     // M_{k+1} = tau^p M_k + P M_k, residual, convergence
       em.kind = EPI_M;
       em.C = c.plane(r.M[nxt]);
       em.In = c.plane(r.M[cur]);
-      em.beta_in = std::pow(tau, p);
+      em.beta_in = std::pow(al, p);
       // symmetric product (upper-triangle tiles mirrored): M' is exactly symmetric,
       // which also removes the antisymmetric mode the iteration would amplify
       if (tc && (rcode = clear_rowmax(c, r.M[nxt]))) return rcode;
@@ -912,6 +987,14 @@ int precond_set_option(precond_t h, int key, double v) {
         h->events = true;
       }
       h->timing = (int)v;
+      return PRECOND_OK;
+    case PRECOND_OPT_FOLD:
+      if (!(v >= 0.0 && v < 1.0)) return PRECOND_EINVAL;
+      h->fold = v;
+      return PRECOND_OK;
+    case PRECOND_OPT_CLASSICAL:
+      if (v != 0 && v != 1) return PRECOND_EINVAL;
+      h->classical = (int)v;
       return PRECOND_OK;
     case PRECOND_OPT_USE_GRAPH:
       if (v != 0 && v != 1) return PRECOND_EINVAL;

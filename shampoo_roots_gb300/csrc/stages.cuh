@@ -150,6 +150,7 @@ struct RootArgs {
   int d;
   float eps;
   IterCtl ctl;
+  double alpha0, beta0;      // first step polynomial T_0 = alpha0 I - beta0 M_0
   // engine planes
   Plane M0, X1;              // start outputs (fp32 form in the tcgen05 engine)
   Plane X[2];                // finalize input (X buffer kfinal & 1)
@@ -241,7 +242,7 @@ __device__ __forceinline__ double root_scale(const RootStat& st, int d, double e
   return 1.01 * fmin(ws, st.minc);
 }
 
-// M_0 = A_hat / c and X_1 = X_0 T_0 = T_0 = ((p+1) I - M_0) / p.
+// M_0 = A_hat / c and X_1 = X_0 T_0 = T_0 = alpha0 I - beta0 M_0.
 template <int E>
 __global__ void __launch_bounds__(256) root_init_kernel(RootArgs a) {
   const int b = blockIdx.z;
@@ -259,7 +260,6 @@ __global__ void __launch_bounds__(256) root_init_kernel(RootArgs a) {
   }
   if (bad) return;
   const float* A = a.src[b];
-  const double p = (double)a.ctl.p;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
   for (int q = ty; q < 32; q += 8) {
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(256) root_init_kernel(RootArgs a) {
       const double id = (r == col) ? 1.0 : 0.0;
       const double a_sym = 0.5 * ((double)A[(long long)r * a.d + col] + (double)A[(long long)col * a.d + r]);
       const double m0 = (a_sym / t + eps * id) / c;
-      const double x1 = ((p + 1.0) * id - m0) / p;
+      const double x1 = a.alpha0 * id - a.beta0 * m0;
       plane_store<E>(a.M0, b, r, col, m0);
       plane_store<E>(a.X1, b, r, col, x1);
       mx = (float)fabs(m0);
