@@ -28,7 +28,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "preconditioner step ms and TFLOP/s (% GB300 tensor peak) vs CPU oracle"
-WORKLOAD_INDEX = 1          # the 24-layer d=1024 stack, power -1/4
+WORKLOAD_INDEX = 1          # default: the 24-layer d=1024 stack, power -1/4
 
 
 def load_peaks():
@@ -137,18 +137,35 @@ def oracle_sample(w, seconds_budget=20.0):
     return total, desc, os.cpu_count()
 
 
+def oracle_sample_spd(w, power, n=2):
+    """Time the oracle on `n` of the SPD matrices; extrapolate to all of them."""
+    import numpy as np
+    from oracle import roots as oracle
+    from workloads import synth
+    A = synth.spd_inputs(w, matrices=range(n))
+    t0 = time.perf_counter()
+    for a in A:
+        oracle.inv_root(a.astype(np.float64), w.eps, power)
+    dt = time.perf_counter() - t0
+    return dt / n * w.count, f"{n} of the {w.count} SPD {w.dims[0]}^2 matrices ({dt:.1f} s), extrapolated", os.cpu_count()
+
+
 def run_reference(args):
     """Reference arm: the float64 CPU oracle on a bounded sample per step."""
     from workloads import synth
-    w = synth.workload(WORKLOAD_INDEX)
+    w = synth.workload(args.workload)
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     secs = []
     desc = ""
     cores = os.cpu_count()
+    power = args.power if args.power is not None else w.powers[0]
     for _ in range(args.warmup + args.steps):
-        t, desc, cores = oracle_sample(w, seconds_budget=8.0)
+        if w.kind == "step":
+            t, desc, cores = oracle_sample(w, seconds_budget=8.0)
+        else:
+            t, desc, cores = oracle_sample_spd(w, power, n=1)
         secs.append(t)
     timed = secs[args.warmup:]
     per_step = statistics.median(timed)
@@ -156,7 +173,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "preconditioner steps/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "matrices": len(w.shapes), "grad_dtype": w.dtype, "power": w.powers[0]},
+            "config": {"workload": w.name, "matrices": w.count, "grad_dtype": w.dtype, "power": power},
             "cpu_baseline": {"value": value, "unit": "preconditioner steps/s", "cores": cores, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": "preconditioner steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -190,6 +207,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,
+                    help="0 single 256x128, 1 stack p=-1/4 (default), 2 stack p=-1/2, 3 SPD 64x2048^2, 4 wide 6144")
+    ap.add_argument("--power", type=float, default=None, help="override the workload's power")
     ap.add_argument("--profile-small", action="store_true",
                     help="profiling case: roots of 4 SPD 2048^2 matrices, no JSON line")
     args = ap.parse_args()
@@ -213,18 +233,28 @@ def main():
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
 
-    w = synth.workload(WORKLOAD_INDEX)
-    shapes = list(w.shapes)
-    power = w.powers[0]
-    # two distinct gradient batches (ranks draw from their own seeds: weak scaling)
-    pools = [synth.torch_gradients_for_step(w, 1000 * rank + s, dev) for s in range(2)]
-    L = [torch.zeros((m, m), device=dev) for m, _ in shapes]
-    R = [torch.zeros((n, n), device=dev) for _, n in shapes]
-    out = [torch.empty((m, n), device=dev) for m, n in shapes]
+    w = synth.workload(args.workload)
+    power = args.power if args.power is not None else w.powers[0]
     pc = sr.Preconditioner(local, timing=1)
+    if w.kind == "step":
+        shapes = list(w.shapes)
+        nroots = 2 * len(shapes)
+        # two distinct gradient batches (ranks draw from their own seeds: weak scaling)
+        pools = [synth.torch_gradients_for_step(w, 1000 * rank + s, dev) for s in range(2)]
+        L = [torch.zeros((m, m), device=dev) for m, _ in shapes]
+        R = [torch.zeros((n, n), device=dev) for _, n in shapes]
+        out = [torch.empty((m, n), device=dev) for m, n in shapes]
 
-    def step(i):
-        sr.precond_step(pc.h, pools[i % 2], L, R, w.beta, w.eps, power, out=out, stream=stream)
+        def step(i):
+            sr.precond_step(pc.h, pools[i % 2], L, R, w.beta, w.eps, power, out=out, stream=stream)
+    else:
+        shapes = []
+        nroots = w.count
+        A = synth.torch_spd_inputs(w, dev)
+        Xo = [torch.empty_like(a) for a in A]
+
+        def step(i):
+            sr.precond_inv_root(pc.h, A, Xo, w.eps, power, stream=stream)
 
     for i in range(args.warmup):
         step(i)
@@ -240,12 +270,18 @@ def main():
     ns_ms, ns_flops, gemm_ms, gemm_n, root_flops, issued_flops = 0.0, 0.0, 0.0, 0, 0.0, 0.0
     stage_ms = [0.0, 0.0, 0.0, 0.0]
     iters_seen = []
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # workloads whose data fit in L2 (the single 256x128 matrix) get an L2 flush
+    # (a 256 MB write) between timed steps, outside the steps' events
+    flush = torch.empty((64 << 20,), device=dev) if w.index == 0 else None
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with Clocks(local) as clk:
         barrier()
-        ev0.record(stream)
         for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            evs[i][0].record(stream)
             step(i)
+            evs[i][1].record(stream)
             ms, nl, fl = sr.precond_get_timing(pc.h)     # synchronises the step
             gms, gn, gis = sr.precond_get_gemm_timing(pc.h)
             issued_flops += gis
@@ -254,11 +290,10 @@ def main():
             root_flops += fl
             gemm_ms += gms
             gemm_n += gn
-            it, _, _, _ = sr.precond_get_stats(pc.h, 2 * len(shapes))
+            it, _, _, _ = sr.precond_get_stats(pc.h, nroots)
             iters_seen.append(statistics.mean(it))
-        ev1.record(stream)
         barrier()
-    elapsed = ev0.elapsed_time(ev1) / 1e3
+    elapsed = sum(a.elapsed_time(b) for a, b in evs) / 1e3
     gpu_launches = sr.precond_launch_count(pc.h) - launches0
     if dist is not None:
         t = torch.tensor([elapsed], device=dev)
@@ -271,7 +306,7 @@ def main():
 
     # ---------------- end to end: pinned host gradients in, update out, inside the timed region
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and w.kind == "step":
         host_g = [[g.cpu().pin_memory() for g in pool] for pool in pools]
         host_u = [torch.empty((m, n), dtype=torch.float32).pin_memory() for m, n in shapes]
         dev_g = [torch.empty_like(g) for g in pools[0]]
@@ -311,7 +346,10 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        t_oracle, desc, cores = oracle_sample(w)
+        if w.kind == "step":
+            t_oracle, desc, cores = oracle_sample(w)
+        else:
+            t_oracle, desc, cores = oracle_sample_spd(w, power)
         cpu = {"value": 1.0 / t_oracle, "unit": "preconditioner steps/s", "cores": cores, "kind": "oracle",
                "sample": desc, "ms_per_step_extrapolated": t_oracle * 1e3}
 
@@ -319,10 +357,10 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": "preconditioner steps/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": w.name, "matrices": len(shapes), "roots": 2 * len(shapes),
+                "config": {"workload": w.name, "matrices": w.count, "roots": nroots,
                            "grad_dtype": w.dtype, "power": power, "beta": w.beta, "eps": w.eps,
                            "mean_iterations": statistics.mean(iters_seen) if iters_seen else None,
-                           "l2": "inputs larger than L2 (fp32 Gram state 4.6 GB, gradients 0.6 GB per batch)",
+                           "l2": "inputs larger than L2 (129 MB): the state / input matrices of every workload but the single 256x128 one",
                            "numerics": "bf16 tensor-core digit products, exact fp32 accumulation of leading levels"},
                 "tflops_algorithmic": tflops,
                 "pct_tensor_peak": tflops / peaks["bf16_tflops"],

@@ -60,7 +60,7 @@ struct RootClass {
   std::vector<const float*> src;       // per entry: source matrix (caller)
   std::vector<float*> dst;             // per entry: caller output (inv_root)
   Slab X[2], M[2], D, F, Xf;   // per-row-scaled (tcgen05) or double planes
-  size_t rowabs = 0, diag = 0, rowsq = 0, partials = 0;
+  size_t rowabs = 0, diag = 0, rowsq = 0, rvec = 0, partials = 0;
   long long tiles = 0;
   size_t t_root = 0, t_src = 0, t_dst = 0;   // device tables (offsets)
   int kmax = 0;
@@ -273,6 +273,7 @@ void layout_root_class(Layout& L, RootClass& r, int p) {
   r.rowabs = L.take((size_t)nb * d * sizeof(double));
   r.diag = L.take((size_t)nb * d * sizeof(double));
   r.rowsq = L.take((size_t)nb * d * sizeof(double));
+  r.rvec = L.take((size_t)nb * d * sizeof(float));
 }
 
 int build_plan(precond_ctx* h, Plan& P, bool step, int count, const int64_t* dims2, int dtype, float eps,
@@ -621,6 +622,7 @@ RootArgs root_args(const Ctx& c, const RootClass& r, float eps) {
   a.rowabs = c.at<double>(r.rowabs);
   a.diag = c.at<double>(r.diag);
   a.rowsq = c.at<double>(r.rowsq);
+  a.rvec = c.at<float>(r.rvec);
   a.d = r.d;
   a.eps = eps;
   a.ctl.p = c.P.p;
@@ -644,7 +646,8 @@ int launch_roots_start(const Ctx& c, float eps) {
     RootArgs a = root_args(c, r, eps);
     const int rb = std::min((r.d + 7) / 8, 512);
     root_stats_kernel<<<dim3(rb, nb), 256, 0, c.st>>>(a);
-    root_bound_kernel<<<dim3(rb, nb), 256, 0, c.st>>>(a);
+    root_trace_kernel<<<nb, 256, 0, c.st>>>(a);
+    root_bound_kernel<<<dim3(rb, nb), 256, r.d <= 12288 ? r.d * sizeof(float) : 0, c.st>>>(a);
     dim3 g((r.d + 31) / 32, (r.d + 31) / 32, nb);
     int rc;
     if (r.eng == ENGINE_F64) {
@@ -653,7 +656,7 @@ int launch_roots_start(const Ctx& c, float eps) {
       if ((rc = clear_rowmax(c, r.M[0])) || (rc = clear_rowmax(c, r.X[1]))) return rc;
       root_init_kernel<ENGINE_TC><<<g, 256, 0, c.st>>>(a);
     }
-    c.h->launches += 3;
+    c.h->launches += 4;
     CK(cudaGetLastError());
     if (r.eng == ENGINE_TC && ((rc = slice(c, r.M[0])) || (rc = slice(c, r.X[1])))) return rc;
   }

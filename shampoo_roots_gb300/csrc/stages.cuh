@@ -123,6 +123,18 @@ __device__ __forceinline__ float pow2_ceil(float x) {
   return f == 0.5f ? x : ldexpf(1.f, e);
 }
 
+__device__ __forceinline__ void digits4(float v, float inv, float (&d)[4]) {
+  float r = v * inv * 128.0f;
+  float w = 1.0f;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const float q = rintf(r);
+    d[s] = q * w;                // exact: |q| <= 129, power-of-two weight
+    r = (r - q) * 128.0f;
+    w *= 0.0078125f;
+  }
+}
+
 __global__ void __launch_bounds__(256) slice_rows_kernel(SliceArgs a) {
   const int b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -132,7 +144,28 @@ __global__ void __launch_bounds__(256) slice_rows_kernel(SliceArgs a) {
     const float inv = 1.0f / sigma;          // exact: sigma is a power of two
     const float* src = a.src + (long long)b * a.src_bstride + (long long)r * a.src_ld;
     const long long o = (long long)b * a.dst.bstride + (long long)r * a.dst.ld;
-    for (int c = lane; c < a.cols; c += 32) digits_store(a.dst, o + c, src[c], inv);
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.dst.hi) + o;
+    const int nv = (a.cols / 4) * 4;
+    for (int c = lane * 4; c < nv; c += 128) {          // 4 columns per lane: 16 B in, 8 B out per plane
+      const float4 v = *reinterpret_cast<const float4*>(src + c);
+      float d0[4], d1[4], d2[4], d3[4];
+      digits4(v.x, inv, d0);
+      digits4(v.y, inv, d1);
+      digits4(v.z, inv, d2);
+      digits4(v.w, inv, d3);
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        if (s < a.dst.S) {
+          __nv_bfloat162 lo2 = __floats2bfloat162_rn(d0[s], d1[s]);
+          __nv_bfloat162 hi2 = __floats2bfloat162_rn(d2[s], d3[s]);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+          pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+          *reinterpret_cast<uint2*>(dst + s * a.dst.pstride + c) = pk;
+        }
+      }
+    }
+    for (int c = nv + lane; c < a.cols; c += 32) digits_store(a.dst, o + c, src[c], inv);
   }
 }
 
@@ -147,6 +180,7 @@ struct RootArgs {
   double* rowabs;            // [b][d]  sum_j |src_ij|
   double* diag;              // [b][d]  src_ii
   double* rowsq;             // [b][d]  sum_j src_ij^2
+  float* rvec;               // [b][d]  absolute row sums of A_hat
   int d;
   float eps;
   IterCtl ctl;
@@ -196,40 +230,55 @@ __device__ double block_vec_sum(const double* v, int n) {
   return out;
 }
 
-// Minc's bound on A_hat = src / tr + eps I:  max_i (|A_hat| r)_i / r_i, r = |A_hat| 1.
+// Per root (one block): trace and squared Frobenius norm in a fixed order, and
+// the absolute row sums of A_hat = src / tr + eps I,
+// r_c = sum_j |A_hat_cj| = (rowabs_c - |src_cc|) / tr + |src_cc / tr + eps|.
+__global__ void __launch_bounds__(256) root_trace_kernel(RootArgs a) {
+  const int b = blockIdx.x;
+  RootStat* st = &a.stats[a.root_of[b]];
+  const double t = block_vec_sum(a.diag + (long long)b * a.d, a.d);
+  const double f2 = block_vec_sum(a.rowsq + (long long)b * a.d, a.d);
+  if (threadIdx.x == 0) {
+    st->trace = t;
+    st->frob2 = f2;
+  }
+  const double it = (t > 0.0 && isfinite(t)) ? 1.0 / t : 0.0, eps = (double)a.eps;
+  for (int c = threadIdx.x; c < a.d; c += blockDim.x) {
+    const double dc = a.diag[(long long)b * a.d + c];
+    const double rc = (a.rowabs[(long long)b * a.d + c] - fabs(dc)) * it + fabs(dc * it + eps);
+    a.rvec[(long long)b * a.d + c] = (float)fmax(rc, 1e-12);
+  }
+}
+
+// Minc's bound on A_hat:  max_i (|A_hat| r)_i / r_i  (fp32: it is an upper
+// bound used with a 1.01 margin; the sums' rounding is far below that margin).
 __global__ void __launch_bounds__(256) root_bound_kernel(RootArgs a) {
+  extern __shared__ float rsh[];
   const int b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* A = a.src[b];
   RootStat* st = &a.stats[a.root_of[b]];
-  const double t = block_vec_sum(a.diag + (long long)b * a.d, a.d);
-  if (blockIdx.x == 0) {
-    const double f2 = block_vec_sum(a.rowsq + (long long)b * a.d, a.d);
-    if (threadIdx.x == 0) {
-      st->trace = t;
-      st->frob2 = f2;
-    }
-  }
+  const double t = st->trace;
   if (!(t > 0.0) || !isfinite(t)) return;
-  const double it = 1.0 / t, eps = (double)a.eps;
-  const double* ra = a.rowabs + (long long)b * a.d;
-  const double* dg = a.diag + (long long)b * a.d;
-  double best = 0.0;
-  for (int r = blockIdx.x * 8 + warp; r < a.d; r += gridDim.x * 8) {
-    double y = 0.0;
-    for (int c = lane; c < a.d; c += 32) {
-      const double v = A[(long long)r * a.d + c];
-      const double dc = dg[c];
-      const double rc = (ra[c] - fabs(dc)) * it + fabs(dc * it + eps);   // row sum of |A_hat|, row c
-      const double ahat = (c == r) ? fabs(v * it + eps) : fabs(v) * it;
-      y += ahat * fmax(rc, 1e-12);
-    }
-    y = warp_sum(y);
-    const double dr = dg[r];
-    const double rr = fmax((ra[r] - fabs(dr)) * it + fabs(dr * it + eps), 1e-12);
-    best = fmax(best, y / rr);
+  const float it = (float)(1.0 / t), eps = a.eps;
+  const float* rv = a.rvec + (long long)b * a.d;
+  const bool in_smem = a.d <= 12288;           // 48 KB of dynamic shared memory
+  if (in_smem) {
+    for (int c = threadIdx.x; c < a.d; c += blockDim.x) rsh[c] = rv[c];
+    __syncthreads();
   }
-  if (lane == 0 && isfinite(best)) atomic_max_nonneg(&st->minc, best);
+  const float* rs = in_smem ? rsh : rv;
+  float best = 0.f;
+  for (int r = blockIdx.x * 8 + warp; r < a.d; r += gridDim.x * 8) {
+    const float* row = A + (long long)r * a.d;
+    float y = 0.f;
+    for (int c = lane; c < a.d; c += 32) y = fmaf(fabsf(row[c]), rs[c], y);
+    y = warp_sum(y);
+    const float arr = row[r];
+    y = y * it - fabsf(arr) * it * rs[r] + fabsf(arr * it + eps) * rs[r];   // the diagonal carries + eps
+    best = fmaxf(best, y / rs[r]);
+  }
+  if (lane == 0 && isfinite(best)) atomic_max_nonneg(&st->minc, (double)best);
 }
 
 __device__ __forceinline__ double root_scale(const RootStat& st, int d, double eps) {
@@ -247,33 +296,50 @@ template <int E>
 __global__ void __launch_bounds__(256) root_init_kernel(RootArgs a) {
   const int b = blockIdx.z;
   RootStat* st = &a.stats[a.root_of[b]];
-  const double t = st->trace, eps = (double)a.eps;
-  const double c = root_scale(*st, a.d, eps);
-  const bool bad = st->nonfinite || !(t > 0.0) || !isfinite(t) || !isfinite(c) || !(c > 0.0);
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
-    st->c = c;
-    st->resid = 1e300;
-    st->iters = 0;
-    st->kfinal = 0;
-    st->done = bad ? 1 : 0;
-    st->status = bad ? PRECOND_ENONFINITE : PRECOND_OK;
+  const double eps = (double)a.eps;
+  __shared__ double sh_c, sh_t;
+  __shared__ int sh_bad;
+  if (threadIdx.x == 0) {                 // per-root scalars once per block (fp64 is slow here)
+    const double t = st->trace;
+    const double c = root_scale(*st, a.d, eps);
+    sh_c = c;
+    sh_t = t;
+    sh_bad = st->nonfinite || !(t > 0.0) || !isfinite(t) || !isfinite(c) || !(c > 0.0);
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+      st->c = c;
+      st->resid = 1e300;
+      st->iters = 0;
+      st->kfinal = 0;
+      st->done = sh_bad ? 1 : 0;
+      st->status = sh_bad ? PRECOND_ENONFINITE : PRECOND_OK;
+    }
   }
-  if (bad) return;
+  __syncthreads();
+  if (sh_bad) return;
+  const double t = sh_t, c = sh_c;
   const float* A = a.src[b];
+  __shared__ float tt[32][33];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int q = ty; q < 32; q += 8) {            // mirrored tile (rows c0.., cols r0..), coalesced
+    const int r = c0 + q, col = r0 + tx;
+    tt[q][tx] = (r < a.d && col < a.d) ? A[(long long)r * a.d + col] : 0.f;
+  }
+  __syncthreads();
+  const float s_ac = (float)(0.5 / (t * c)), s_eps = (float)(eps / c);
+  const float al = (float)a.alpha0, be = (float)a.beta0;
   for (int q = ty; q < 32; q += 8) {
     const int r = r0 + q, col = c0 + tx;
     float mx = 0.f, xx = 0.f;
     if (r < a.d && col < a.d) {
-      const double id = (r == col) ? 1.0 : 0.0;
-      const double a_sym = 0.5 * ((double)A[(long long)r * a.d + col] + (double)A[(long long)col * a.d + r]);
-      const double m0 = (a_sym / t + eps * id) / c;
-      const double x1 = a.alpha0 * id - a.beta0 * m0;
+      const bool dgl = (r == col);
+      // M_0 = ((A + A^T)/2 / tr + eps I) / c, exactly symmetric
+      const float m0 = fmaf(A[(long long)r * a.d + col] + tt[tx][q], s_ac, dgl ? s_eps : 0.f);
+      const float x1 = (dgl ? al : 0.f) - be * m0;
       plane_store<E>(a.M0, b, r, col, m0);
       plane_store<E>(a.X1, b, r, col, x1);
-      mx = (float)fabs(m0);
-      xx = (float)fabs(x1);
+      mx = fabsf(m0);
+      xx = fabsf(x1);
     }
     if (E == ENGINE_TC) {
       mx = warp_max(mx);
@@ -289,28 +355,31 @@ __global__ void __launch_bounds__(256) root_init_kernel(RootArgs a) {
 // Result = sym(X_kfinal) * c^(-1/p): to the engine plane Xf (step) or caller fp32 (inv_root).
 template <int E>
 __global__ void __launch_bounds__(256) root_finish_kernel(RootArgs a) {
-  __shared__ double tile[32][33];
+  __shared__ float tile[32][33];
   const int b = blockIdx.z;
   const RootStat* st = &a.stats[a.root_of[b]];
   if (st->status == PRECOND_ENONFINITE || st->kfinal < 1) return;
   const Plane& X = a.X[st->kfinal & 1];
-  const double f = pow(st->c, -1.0 / (double)a.ctl.p);
+  __shared__ float sh_f;
+  if (threadIdx.x == 0) sh_f = (float)pow(st->c, -1.0 / (double)a.ctl.p);   // once per block
+  __syncthreads();
+  const float f = sh_f;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
   // load the transposed tile (rows c0.., cols r0..)
   for (int q = ty; q < 32; q += 8) {
     const int r = c0 + q, col = r0 + tx;
-    tile[q][tx] = (r < a.d && col < a.d) ? plane_load<E>(X, b, r, col) : 0.0;
+    tile[q][tx] = (r < a.d && col < a.d) ? (float)plane_load<E>(X, b, r, col) : 0.f;
   }
   __syncthreads();
   for (int q = ty; q < 32; q += 8) {
     const int r = r0 + q, col = c0 + tx;
     float mx = 0.f;
     if (r < a.d && col < a.d) {
-      const double v = 0.5 * (plane_load<E>(X, b, r, col) + tile[tx][q]) * f;
-      if (a.dst) a.dst[b][(long long)r * a.d + col] = (float)v;
-      else plane_store<E>(a.Xf, b, r, col, v);
-      mx = (float)fabs(v);
+      const float v = 0.5f * ((float)plane_load<E>(X, b, r, col) + tile[tx][q]) * f;
+      if (a.dst) a.dst[b][(long long)r * a.d + col] = v;
+      else plane_store<E>(a.Xf, b, r, col, (double)v);
+      mx = fabsf(v);
     }
     if (E == ENGINE_TC && !a.dst) {
       mx = warp_max(mx);
