@@ -70,7 +70,10 @@ typedef struct precond_ctx* precond_t;
 #define PRECOND_OPT_SMALL_DIM      5  /* auto engine: max(m,n) <= this -> fp64 SIMT engine; default 512 */
 #define PRECOND_OPT_WORKSPACE_MAX  6  /* workspace limit in bytes; 0 = unlimited (default) */
 #define PRECOND_OPT_TIMING         7  /* 1 = record per-stage CUDA events (read by precond_get_timing) */
-#define PRECOND_OPT_USE_GRAPH      8  /* 1 = capture the step as a CUDA graph and replay it (default 0) */
+#define PRECOND_OPT_USE_GRAPH      8  /* 1 = capture each distinct plan (shapes, options, workspace) once as a
+                                         CUDA graph on a handle-owned stream and replay it, ordered after
+                                         and before the caller's stream by events (default 1); 0 = launch
+                                         every kernel on the caller's stream */
 #define PRECOND_OPT_CLASSICAL      9  /* 1 = classical Newton step (p+1)/p I - M/p at every iteration;
                                          0 = per-step minimax step polynomial (default) */
 #define PRECOND_OPT_FOLD          10  /* minimax step: the interval's top may not fall below this
@@ -147,8 +150,9 @@ int precond_get_timing(precond_t h, double ms[4], int64_t* ns_gemm_launches, dou
  * With PRECOND_OPT_TIMING on: total milliseconds of the tcgen05 GEMM launches
  * of the last call's iteration stage (CUDA events around each launch on the
  * call's stream; synchronises), their number, and the bf16 MMA FLOPs they
- * issued (tiles launched x 2 x 128 x 128 x K x digit products per tile step).
- * Any output pointer may be NULL.
+ * issued, counted on the device: for every tile actually computed (tiles of
+ * converged roots are skipped), 2 x 128 x 128 x 32 per K block and digit
+ * product.  Any output pointer may be NULL.
  */
 int precond_get_gemm_timing(precond_t h, double* ms_total, int64_t* launches, double* issued_flops);
 

@@ -45,6 +45,7 @@ struct TcGemmArgs {
   const float* a_rowscale; long long a_rs_stride; float a_scale;
   const float* b_rowscale; long long b_rs_stride; float b_scale;
   unsigned int* err;     // error word (bit 0: a wait timed out)
+  unsigned long long* issued;   // may be null: += (K blocks x digit pairs) of every tile computed
 };
 
 template <int S>
@@ -52,8 +53,9 @@ struct TcSmem {
   static constexpr int A_BYTES = TC_BM * TC_BK * 2;            // 8 KB per digit plane
   static constexpr int B_BYTES = TC_BN * TC_BK * 2;            // 8 KB
   static constexpr int STAGE_BYTES = S * (A_BYTES + B_BYTES);
-  static constexpr int STAGES = (S == 4) ? 2 : 3;
-  static constexpr int STG_LD = TC_BN + 1;                      // staging row stride (floats), bank-conflict free
+  static constexpr int STAGES = (S == 4) ? 3 : 4;
+  static constexpr int STG_LD = TC_BN / 2 + 1;                  // staging: half a tile's columns, row stride
+                                                                // (floats) bank-conflict free
   static constexpr int STAGING_BYTES = TC_BM * STG_LD * 4;
   static constexpr int TMEM_COLS = 512;                        // 3 x 128 used
   static constexpr int BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 1024 /*barriers, scales*/;
@@ -197,6 +199,8 @@ __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: 
 // tensor-memory accumulators of a tile into a shared staging tile, releases
 // tensor memory (the next tile's MMAs start), then runs the element-wise
 // epilogue from shared memory with coalesced global accesses.
+constexpr int EPI_RB = 8;   // epilogue rows per load batch
+
 template <int S>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
@@ -302,6 +306,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
           tc_commit(empty_bar(s));
         }
         tc_commit(accum_bar);
+        if (ok && g.issued) atomicAdd(g.issued, (unsigned long long)nk * Pairs<S>::N);
         ++it;
       }
     }
@@ -329,14 +334,16 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       const bool ok = mbar_wait(accum_bar, it & 1, g.err);
       tc_fence_after();
       epi_bar();
-      // ---- drain: tensor memory -> staging (scaled fp32)
+      // ---- drain: tensor memory -> columns 0..63 to staging, 64..127 to registers (scaled fp32),
+      // after which tensor memory is free for the next tile's products
       const int row = q * 32 + lane;
       const long long gr = tile_m + row;
       const double sa = (gr < g.M) ? (g.a_rowscale ? (double)g.a_rowscale[(long long)za * g.a_rs_stride + gr]
                                                     : (double)g.a_scale) : 0.0;
       const float rs = (float)(c0 * sa);
       float* srow = staging + row * SM::STG_LD;
-#pragma unroll 1
+      float hold[TC_BN / 2];
+#pragma unroll
       for (int ch = 0; ch < TC_BN / 32; ++ch) {
         float v0[32], v1[32], v2[32];
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ch * 32);
@@ -344,104 +351,184 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
         tmem_ld32(taddr + 128, v1);
         tmem_ld32(taddr + 256, v2);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) srow[ch * 32 + j] = ((v0[j] + v1[j]) + v2[j]) * rs * colscale[ch * 32 + j];
+        for (int j = 0; j < 32; ++j) {
+          const float x = ((v0[j] + v1[j]) + v2[j]) * rs * colscale[ch * 32 + j];
+          if (ch < 2) srow[ch * 32 + j] = x;
+          else hold[(ch - 2) * 32 + j] = x;
+        }
       }
       tc_fence_before();
       epi_bar();
       if (et == 0) mbar_arrive(tmem_empty_bar);    // tensor memory may take the next tile
-      // ---- element-wise epilogue from staging
+      // ---- element-wise epilogue, one half of the tile's columns at a time.  Every
+      // barrier below is reached by all 128 epilogue threads (work is guarded, not the barriers).
       float part = 0.f;
-      if (ok) {
+      const bool track = (e.kind == EPI_AFF || e.kind == EPI_M) && e.C.rowmax;
+      const bool need_in = (e.kind == EPI_AFF || e.kind == EPI_M || e.kind == EPI_GRAM);
+      // diagonal tile of a symmetric product: the strict upper triangle is computed and written
+      // to both triangles, so the result is exactly symmetric (the iteration amplifies any
+      // antisymmetric part while M is far from I)
+      const bool diag_fix = g.sym && !mirror && (e.kind == EPI_AFF || e.kind == EPI_M);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const int hc = h * (TC_BN / 2);             // first tile column of this half
+        if (h == 1) {
+          epi_bar();                                // the first half's staging is read
+#pragma unroll
+          for (int j = 0; j < TC_BN / 2; ++j) srow[j] = hold[j];
+          epi_bar();
+        }
         if (e.kind == EPI_VT) {
-          // transposed output: warp ew takes tile columns ew*32.., lanes run over rows
-          for (int cc = 0; cc < 32; ++cc) {
-            const int c = ew * 32 + cc;
-            const long long gc = tile_n + c;
+          // transposed output: warp ew takes 16 of the half's columns, lanes run over rows
+          for (int cc = 0; cc < TC_BN / 8; ++cc) {
+            const int cl = ew * (TC_BN / 8) + cc;
+            const long long gc = tile_n + hc + cl;
             float mx = 0.f;
-            if (gc < g.N) {
+            if (ok && gc < g.N) {
 #pragma unroll
               for (int r4 = 0; r4 < 4; ++r4) {
                 const int r = r4 * 32 + lane;
                 const long long grr = tile_m + r;
                 if (grr < g.M) {
-                  const float v = staging[r * SM::STG_LD + c];
+                  const float v = staging[r * SM::STG_LD + cl];
                   e.C.f32[(long long)b * e.C.bstride + gc * e.C.ld + grr] = v;
                   mx = fmaxf(mx, fabsf(v));
                 }
               }
             }
             mx = warp_max(mx);
-            if (lane == 0 && gc < g.N && e.C.rowmax) atomic_max_nonneg(&e.C.rowmax[(long long)b * e.C.rows + gc], mx);
+            if (ok && lane == 0 && gc < g.N && e.C.rowmax) atomic_max_nonneg(&e.C.rowmax[(long long)b * e.C.rows + gc], mx);
           }
-        } else {
-          const bool track = (e.kind == EPI_AFF || e.kind == EPI_M) && e.C.rowmax;
-          for (int rr = 0; rr < 32; ++rr) {
-            const int r = ew * 32 + rr;
+          continue;
+        }
+        float colmx[2] = {0.f, 0.f};   // diag_fix: per lane column, max |v| of the strict upper part
+        // Rows go in groups of EPI_RB: the group's global inputs are loaded first, so
+        // their latencies overlap instead of adding up row by row (the whole cost of a
+        // product when the grid has only a few tiles).
+#pragma unroll 1
+        for (int r0 = 0; r0 < 32; r0 += EPI_RB) {
+          float in[EPI_RB][2];
+#pragma unroll
+          for (int u = 0; u < EPI_RB; ++u) {
+            const int r = ew * 32 + r0 + u;
+            const long long grr = tile_m + r;
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+              const int c = hc + c2 * 32 + lane;
+              const long long gc = tile_n + c;
+              in[u][c2] = 0.f;
+              if (ok && need_in && grr < g.M && gc < g.N && !(diag_fix && c < r)) {
+                if (e.kind == EPI_GRAM)
+                  in[u][c2] = e.state[b][grr * e.cols + gc];
+                else
+                  in[u][c2] = e.In.f32[(long long)b * e.In.bstride + grr * e.In.ld + gc];
+              }
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < EPI_RB; ++u) {
+            const int r = ew * 32 + r0 + u;
             const long long grr = tile_m + r;
             float mx = 0.f;
-            if (grr < g.M) {
+            if (ok && grr < g.M) {
 #pragma unroll
-              for (int c4 = 0; c4 < 4; ++c4) {
-                const int c = c4 * 32 + lane;
+              for (int c2 = 0; c2 < 2; ++c2) {
+                const int cl = c2 * 32 + lane;
+                const int c = hc + cl;
                 const long long gc = tile_n + c;
-                if (gc < g.N) {
-                  float* sp = &staging[r * SM::STG_LD + c];
+                if (gc < g.N && !(diag_fix && c < r)) {
+                  float* sp = &staging[r * SM::STG_LD + cl];
                   const float acc = *sp;
-                  const float v = epi_apply_tc(e, b, grr, gc, acc);
-                  if (e.kind == EPI_M) {
-                    part += mirror ? 2.f * v : v;
-                    const long long o = (long long)b * e.C.bstride + grr * e.C.ld + gc;
-                    mx = fmaxf(mx, fabsf(e.C.f32[o]));
-                    if (g.sym) *sp = e.C.f32[o];
-                  } else {
-                    mx = fmaxf(mx, v);
-                    if (g.sym && e.kind != EPI_GRAM) *sp = e.C.f32[(long long)b * e.C.bstride + grr * e.C.ld + gc];
+                  const long long o = (long long)b * e.C.bstride + grr * e.C.ld + gc;
+                  const bool up = diag_fix && c > r;     // also written at the transposed position
+                  switch (e.kind) {
+                    case EPI_STORE:
+                      e.C.f32[o] = acc;
+                      break;
+                    case EPI_AFF: {
+                      float v = fmaf((float)e.alpha, acc, (float)e.beta_in * in[u][c2]);
+                      if (grr == gc) v += (float)e.gamma;
+                      e.C.f32[o] = v;
+                      if (up) {
+                        e.C.f32[(long long)b * e.C.bstride + gc * e.C.ld + grr] = v;
+                        colmx[c2] = fmaxf(colmx[c2], fabsf(v));
+                      }
+                      mx = fmaxf(mx, fabsf(v));
+                      *sp = v;
+                      break;
+                    }
+                    case EPI_M: {
+                      const float v = fmaf((float)e.beta_in, in[u][c2], acc);
+                      e.C.f32[o] = v;
+                      const float rd = v - ((grr == gc) ? 1.0f : 0.0f);
+                      if (up) {
+                        e.C.f32[(long long)b * e.C.bstride + gc * e.C.ld + grr] = v;
+                        colmx[c2] = fmaxf(colmx[c2], fabsf(v));
+                      }
+                      part += (mirror || up) ? 2.f * (rd * rd) : rd * rd;
+                      mx = fmaxf(mx, fabsf(v));
+                      *sp = v;
+                      break;
+                    }
+                    case EPI_GRAM:
+                      e.state[b][grr * e.cols + gc] = fmaf(e.beta, in[u][c2], (1.0f - e.beta) * acc);
+                      break;
+                    case EPI_U: {
+                      const long long ou = grr * e.cols + gc;
+                      if (e.out_dtype == PRECOND_BF16)
+                        reinterpret_cast<__nv_bfloat16*>(e.out[b])[ou] = __float2bfloat16_rn(acc);
+                      else
+                        reinterpret_cast<float*>(e.out[b])[ou] = acc;
+                      break;
+                    }
                   }
                 }
               }
             }
             if (track) {
               mx = warp_max(mx);
-              if (lane == 0 && grr < g.M) atomic_max_nonneg(&e.C.rowmax[(long long)b * e.C.rows + grr], mx);
+              if (ok && lane == 0 && grr < g.M) atomic_max_nonneg(&e.C.rowmax[(long long)b * e.C.rows + grr], mx);
             }
           }
-          if (g.sym && !mirror && (e.kind == EPI_AFF || e.kind == EPI_M)) {
-            // diagonal tile: its lower triangle takes the upper triangle's values, so
-            // the result is exactly symmetric (the iteration amplifies any
-            // antisymmetric part while M is far from I)
-            epi_bar();
-            for (int rr = 0; rr < 32; ++rr) {
-              const int r = ew * 32 + rr;
-              const long long grr = tile_m + r;
-              if (grr >= g.M) continue;
+        }
+        if (diag_fix && track && ok) {
+          // rows of the lower triangle: their entries are the upper triangle's columns
 #pragma unroll
-              for (int c4 = 0; c4 < 4; ++c4) {
-                const int c = c4 * 32 + lane;
-                const long long gc = tile_n + c;
-                if (c < r && gc < g.N)
-                  e.C.f32[(long long)b * e.C.bstride + grr * e.C.ld + gc] = staging[c * SM::STG_LD + r];
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const long long gc = tile_n + hc + c2 * 32 + lane;
+            if (gc < g.N && colmx[c2] > 0.f) atomic_max_nonneg(&e.C.rowmax[(long long)b * e.C.rows + gc], colmx[c2]);
+          }
+        }
+        if (mirror) {
+          // the mirrored tile (rows tile_n.., columns tile_m..) = transpose of this one
+          __syncwarp();
+          epi_bar();
+#pragma unroll 1
+          for (int c0 = 0; c0 < TC_BN / 8; c0 += EPI_RB) {
+            float st_in[EPI_RB][4];
+#pragma unroll
+            for (int u = 0; u < EPI_RB; ++u) {
+              const long long gc = tile_n + hc + ew * (TC_BN / 8) + c0 + u;
+#pragma unroll
+              for (int r4 = 0; r4 < 4; ++r4) {
+                const long long grr = tile_m + r4 * 32 + lane;
+                st_in[u][r4] = (ok && e.kind == EPI_GRAM && gc < g.N && grr < g.M) ? e.state[b][gc * e.cols + grr] : 0.f;
               }
             }
-          }
-          if (mirror) {
-            // the mirrored tile (rows tile_n.., columns tile_m..) = transpose of this one
-            __syncwarp();
-            epi_bar();
-            for (int cc = 0; cc < 32; ++cc) {
-              const int c = ew * 32 + cc;                 // tile column = mirrored row
-              const long long gc = tile_n + c;
+#pragma unroll
+            for (int u = 0; u < EPI_RB; ++u) {
+              const int cl = ew * (TC_BN / 8) + c0 + u;     // tile column (in this half) = mirrored row
+              const long long gc = tile_n + hc + cl;
               float mx = 0.f;
-              if (gc < g.N) {
+              if (ok && gc < g.N) {
 #pragma unroll
                 for (int r4 = 0; r4 < 4; ++r4) {
-                  const int r = r4 * 32 + lane;            // tile row = mirrored column
+                  const int r = r4 * 32 + lane;             // tile row = mirrored column
                   const long long grr = tile_m + r;
                   if (grr < g.M) {
-                    const float v = staging[r * SM::STG_LD + c];
+                    const float v = staging[r * SM::STG_LD + cl];
                     if (e.kind == EPI_GRAM) {
-                      float* st = e.state[b];
-                      const long long o = gc * e.cols + grr;
-                      st[o] = fmaf(e.beta, st[o], (1.0f - e.beta) * v);
+                      e.state[b][gc * e.cols + grr] = fmaf(e.beta, st_in[u][r4], (1.0f - e.beta) * v);
                     } else {
                       e.C.f32[(long long)b * e.C.bstride + gc * e.C.ld + grr] = v;
                       mx = fmaxf(mx, fabsf(v));
@@ -451,7 +538,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
               }
               if (track) {
                 mx = warp_max(mx);
-                if (lane == 0 && gc < g.N) atomic_max_nonneg(&e.C.rowmax[(long long)b * e.C.rows + gc], mx);
+                if (ok && lane == 0 && gc < g.N) atomic_max_nonneg(&e.C.rowmax[(long long)b * e.C.rows + gc], mx);
               }
             }
           }

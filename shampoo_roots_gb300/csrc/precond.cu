@@ -20,6 +20,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <sstream>
 #include <string>
 #include <vector>
 
@@ -94,7 +95,7 @@ struct Plan {
 struct precond_ctx {
   int device = -1;
   double tol = 1e-5;
-  int max_iter = 0, min_iter = 4, engine = 0, small_dim = 512, timing = 0, use_graph = 0;
+  int max_iter = 0, min_iter = 4, engine = 0, small_dim = 512, timing = 0, use_graph = 1;
   int classical = 0;                   // 1: classical Newton step polynomial at every iteration
   double fold = 0.3;                   // minimax step: T(1) >= fold * T(l)
   double ws_max = 0;
@@ -116,12 +117,20 @@ struct precond_ctx {
   int64_t launches = 0;
   int64_t ns_launches = 0;
   bool in_ns = false;                  // timing: inside the iteration stage
-  double ns_issued = 0.0;              // issued bf16 MMA FLOPs of the iteration stage (tile work x digit pairs)
   std::vector<cudaEvent_t> gemm_ev;    // timing: start/stop pairs around iteration-stage GEMMs
   size_t gemm_ev_used = 0;
   EncodeTiledFn encode = nullptr;
   bool tc_attr_set = false;
   int num_sms = 148;
+  // CUDA graph of the last plan (replayed on an internal stream joined to the caller's by events)
+  std::string graph_key;
+  cudaGraphExec_t graph_exec = nullptr;
+  void* graph_ws = nullptr;
+  int64_t graph_kernels = 0, graph_ns_launches = 0;
+  size_t graph_gemm_ev = 0;
+  cudaStream_t gstream = nullptr;
+  cudaEvent_t gev_in = nullptr, gev_out = nullptr;
+  bool capturing = false;              // timing events become event-record nodes of the graph
 };
 
 namespace {
@@ -417,10 +426,19 @@ int build_plan(precond_ctx* h, Plan& P, bool step, int count, const int64_t* dim
   return PRECOND_OK;
 }
 
+void drop_graph(precond_ctx* h);
+
+// Timing event record; under capture it becomes a node of the graph, so the
+// events still fire (and can be timed) on every replay.
+cudaError_t record_event(precond_ctx* h, cudaEvent_t ev, cudaStream_t st) {
+  return h->capturing ? cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal) : cudaEventRecord(ev, st);
+}
+
 int ensure_workspace(precond_ctx* h, size_t bytes) {
   if (h->ws_max > 0 && (double)bytes > h->ws_max) return PRECOND_ENOMEM;
   if (bytes <= h->ws_cap) return PRECOND_OK;
   CK(cudaDeviceSynchronize());
+  drop_graph(h);
   if (h->ws) cudaFree(h->ws);
   h->ws = nullptr;
   h->ws_cap = 0;
@@ -564,24 +582,22 @@ int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int 
     e.tiles_per_entry = (unsigned int)tiles;
     dim3 grid((unsigned int)std::min<long long>(tiles * batch, (long long)c.h->num_sms), 1, 1);
     const bool timed = c.h->timing && c.h->events && c.h->in_ns;
-    if (c.h->in_ns) {
-      const long long kpad = (long long)((K + TC_BK - 1) / TC_BK) * TC_BK;
-      c.h->ns_issued += (double)tiles * batch * 2.0 * TC_BM * TC_BN * kpad * (S == 4 ? 10 : 6);
-    }
+    // iteration-stage products count the MMA work they issue (converged roots' tiles are skipped on the device)
+    g.issued = c.h->in_ns ? reinterpret_cast<unsigned long long*>(c.err() + 2) : nullptr;
     if (timed) {
       while (c.h->gemm_ev.size() < c.h->gemm_ev_used + 2) {
         cudaEvent_t ev;
         CK(cudaEventCreate(&ev));
         c.h->gemm_ev.push_back(ev);
       }
-      CK(cudaEventRecord(c.h->gemm_ev[c.h->gemm_ev_used], c.st));
+      CK(record_event(c.h, c.h->gemm_ev[c.h->gemm_ev_used], c.st));
     }
     if (S == 4)
       gemm_tc_kernel<4><<<grid, TC_THREADS, TcSmem<4>::BYTES, c.st>>>(maps, g, e);
     else
       gemm_tc_kernel<3><<<grid, TC_THREADS, TcSmem<3>::BYTES, c.st>>>(maps, g, e);
     if (timed) {
-      CK(cudaEventRecord(c.h->gemm_ev[c.h->gemm_ev_used + 1], c.st));
+      CK(record_event(c.h, c.h->gemm_ev[c.h->gemm_ev_used + 1], c.st));
       c.h->gemm_ev_used += 2;
     }
   }
@@ -666,7 +682,6 @@ int launch_roots_start(const Ctx& c, float eps) {
 int launch_iterations(const Ctx& c) {
   c.h->in_ns = true;
   c.h->gemm_ev_used = 0;
-  c.h->ns_issued = 0.0;
   struct Guard { precond_ctx* h; ~Guard() { h->in_ns = false; } } guard{c.h};
   const int p = c.P.p;
   int kall = 0;
@@ -768,14 +783,15 @@ Plane digits_plane(char* ws, const Slab& s) {
 }
 
 int record(precond_ctx* h, int i, cudaStream_t st) {
-  if (h->timing && h->events) CK(cudaEventRecord(h->ev[i], st));
+  if (h->timing && h->events) CK(record_event(h, h->ev[i], st));
   return PRECOND_OK;
 }
 
 int run_step(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream_t st) {
   Ctx c{h, P, (char*)h->ws, st};
   int rc;
-  CK(cudaMemsetAsync(c.ws + P.stats, 0, sizeof(RootStat) * P.nroots + 64, st));
+  CK(cudaMemsetAsync(c.ws + P.stats, 0, sizeof(RootStat) * P.nroots, st));
+  CK(cudaMemsetAsync(c.ws + P.err, 0, 64, st));
   if ((rc = record(h, 0, st))) return rc;
   // ---- preparation + Gram EMA
   for (const auto& s : P.sc) {
@@ -861,7 +877,8 @@ int run_step(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream_t 
 int run_inv_root(precond_ctx* h, const Plan& P, float eps, cudaStream_t st) {
   Ctx c{h, P, (char*)h->ws, st};
   int rc;
-  CK(cudaMemsetAsync(c.ws + P.stats, 0, sizeof(RootStat) * P.nroots + 64, st));
+  CK(cudaMemsetAsync(c.ws + P.stats, 0, sizeof(RootStat) * P.nroots, st));
+  CK(cudaMemsetAsync(c.ws + P.err, 0, 64, st));
   if ((rc = record(h, 0, st))) return rc;
   if ((rc = record(h, 1, st))) return rc;
   if ((rc = launch_roots_start(c, eps))) return rc;
@@ -900,6 +917,83 @@ void remember(precond_ctx* h, const Plan& P, cudaStream_t st) {
       h->last_root_slot[r] = (int)j;
     }
   h->last_plan = P;
+}
+
+// Everything a captured step's kernel parameters depend on, except the
+// caller's pointers (those live in the uploaded tables).
+std::string plan_key(const precond_ctx* h, const Plan& P, float beta, float eps) {
+  std::ostringstream k;
+  k << P.step << ' ' << P.count << ' ' << P.nroots << ' ' << P.p << ' ' << P.dtype << ' ' << P.out_f32 << ' '
+    << P.total << ' ' << P.meta << ' ' << P.meta_bytes << ' ' << P.max_tiles << ' ' << beta << ' ' << eps << ' '
+    << h->tol << ' ' << h->min_iter << ' ' << h->timing << ' ' << h->ws;
+  for (const auto& r : P.rc) {
+    k << " r" << r.d << ',' << r.eng << ',' << r.roots.size() << ',' << r.kmax;
+    for (size_t i = 0; i < r.steps.alpha.size(); ++i) k << ',' << r.steps.alpha[i] << ':' << r.steps.beta[i];
+  }
+  for (const auto& c : P.sc) k << " s" << c.m << ',' << c.n << ',' << c.eng << ',' << c.mats.size();
+  return k.str();
+}
+
+void drop_graph(precond_ctx* h) {
+  if (h->graph_exec) cudaGraphExecDestroy(h->graph_exec);
+  h->graph_exec = nullptr;
+  h->graph_key.clear();
+}
+
+// Run `fn(stream)` for plan P: directly on the caller's stream, or (graphs on)
+// as a replay of a graph captured once per plan on the handle's own stream,
+// ordered after the caller's earlier work and before its later work.
+template <typename Fn>
+int run_planned(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream_t st, Fn fn) {
+  int rc;
+  if (!h->use_graph) {
+    if ((rc = upload_meta(h, P, st))) return rc;
+    return fn(st);
+  }
+  if (!h->gstream) {
+    CK(cudaStreamCreateWithFlags(&h->gstream, cudaStreamNonBlocking));
+    CK(cudaEventCreateWithFlags(&h->gev_in, cudaEventDisableTiming));
+    CK(cudaEventCreateWithFlags(&h->gev_out, cudaEventDisableTiming));
+  }
+  CK(cudaEventRecord(h->gev_in, st));
+  CK(cudaStreamWaitEvent(h->gstream, h->gev_in, 0));
+  if ((rc = upload_meta(h, P, h->gstream))) return rc;
+  const std::string key = plan_key(h, P, beta, eps);
+  if (!h->graph_exec || key != h->graph_key || h->graph_ws != h->ws) {
+    drop_graph(h);
+    const int64_t l0 = h->launches;
+    CK(cudaStreamBeginCapture(h->gstream, cudaStreamCaptureModeThreadLocal));
+    h->capturing = true;
+    rc = fn(h->gstream);
+    h->capturing = false;
+    cudaGraph_t g = nullptr;
+    const cudaError_t e = cudaStreamEndCapture(h->gstream, &g);
+    if (rc || e != cudaSuccess) {
+      if (g) cudaGraphDestroy(g);
+      cudaGetLastError();
+      h->launches = l0;
+      return rc ? rc : PRECOND_ECUDA;
+    }
+    const cudaError_t ei = cudaGraphInstantiate(&h->graph_exec, g, 0);
+    cudaGraphDestroy(g);
+    if (ei != cudaSuccess) {
+      h->graph_exec = nullptr;
+      return PRECOND_ECUDA;
+    }
+    h->graph_key = key;
+    h->graph_ws = h->ws;
+    h->graph_kernels = h->launches - l0;
+    h->launches = l0;
+    h->graph_ns_launches = h->ns_launches;
+    h->graph_gemm_ev = h->gemm_ev_used;
+  }
+  CK(cudaGraphLaunch(h->graph_exec, h->gstream));
+  h->launches += h->graph_kernels;
+  h->ns_launches = h->graph_ns_launches;
+  h->gemm_ev_used = h->graph_gemm_ev;
+  CK(cudaEventRecord(h->gev_out, h->gstream));
+  CK(cudaStreamWaitEvent(st, h->gev_out, 0));
+  return PRECOND_OK;
 }
 
 }  // namespace
@@ -950,6 +1044,10 @@ int precond_destroy(precond_t h) {
     if (h->events)
       for (auto& e : h->ev) cudaEventDestroy(e);
     for (auto& e : h->gemm_ev) cudaEventDestroy(e);
+    drop_graph(h);
+    if (h->gstream) cudaStreamDestroy(h->gstream);
+    if (h->gev_in) cudaEventDestroy(h->gev_in);
+    if (h->gev_out) cudaEventDestroy(h->gev_out);
   }
   delete h;
   return PRECOND_OK;
@@ -1035,8 +1133,8 @@ int precond_step(precond_t h, int count, void* const grads[], int grad_dtype, co
   if ((rc = prepare_device(h))) return rc;
   if ((rc = ensure_workspace(h, P.total))) return rc;
   cudaStream_t st = (cudaStream_t)stream;
-  if ((rc = upload_meta(h, P, st))) return rc;
-  if ((rc = run_step(h, P, beta, eps, st))) return rc;
+  if ((rc = run_planned(h, P, beta, eps, st, [&](cudaStream_t s2) { return run_step(h, P, beta, eps, s2); })))
+    return rc;
   remember(h, P, st);
   return PRECOND_OK;
 }
@@ -1059,8 +1157,8 @@ int precond_inv_root(precond_t h, int count, const float* const A[], const int64
   if ((rc = prepare_device(h))) return rc;
   if ((rc = ensure_workspace(h, P.total))) return rc;
   cudaStream_t st = (cudaStream_t)stream;
-  if ((rc = upload_meta(h, P, st))) return rc;
-  if ((rc = run_inv_root(h, P, eps, st))) return rc;
+  if ((rc = run_planned(h, P, 0.f, eps, st, [&](cudaStream_t s2) { return run_inv_root(h, P, eps, s2); })))
+    return rc;
   remember(h, P, st);
   return PRECOND_OK;
 }
@@ -1130,7 +1228,11 @@ int precond_get_gemm_timing(precond_t h, double* ms_total, int64_t* launches, do
   }
   if (ms_total) *ms_total = t;
   if (launches) *launches = (int64_t)(h->gemm_ev_used / 2);
-  if (issued_flops) *issued_flops = h->ns_issued;
+  if (issued_flops) {
+    unsigned long long n = 0;   // (K blocks x digit pairs) of the computed tiles, counted on the device
+    CK(cudaMemcpy(&n, (char*)h->ws + h->last_plan.err + 8, sizeof(n), cudaMemcpyDeviceToHost));
+    *issued_flops = (double)n * 2.0 * TC_BM * TC_BN * TC_BK;
+  }
   return PRECOND_OK;
 }
 
@@ -1204,7 +1306,8 @@ int precond_gemm_selftest(precond_t h, int engine, int M, int N, int K, const fl
   if ((rc = ensure_workspace(h, L.top))) return rc;
   cudaStream_t st = (cudaStream_t)stream;
   Ctx c{h, P, (char*)h->ws, st};
-  CK(cudaMemsetAsync(c.ws + P.stats, 0, sizeof(RootStat) + 64, st));
+  CK(cudaMemsetAsync(c.ws + P.stats, 0, sizeof(RootStat), st));
+  CK(cudaMemsetAsync(c.ws + P.err, 0, 64, st));
   if (eng == ENGINE_F64) {
     f32_to_plane_kernel<ENGINE_F64><<<256, 256, 0, st>>>(A, c.plane(sa), M, K);
     f32_to_plane_kernel<ENGINE_F64><<<256, 256, 0, st>>>(B, c.plane(sb), N, K);
