@@ -67,7 +67,8 @@ typedef struct precond_ctx* precond_t;
 #define PRECOND_OPT_MAX_ITER       2  /* iteration cap; 0 = derived from the scalar model (default) */
 #define PRECOND_OPT_MIN_ITER       3  /* stagnation test only after this many iterations; default 4 */
 #define PRECOND_OPT_ENGINE         4  /* 0 auto (default), 1 fp64 SIMT engine, 2 tcgen05 engine */
-#define PRECOND_OPT_SMALL_DIM      5  /* auto engine: max(m,n) <= this -> fp64 SIMT engine; default 512 */
+#define PRECOND_OPT_SMALL_DIM      5  /* auto engine: max(m,n) <= this -> fp64 SIMT engine; default 0
+                                         (the tcgen05 engine for every size) */
 #define PRECOND_OPT_WORKSPACE_MAX  6  /* workspace limit in bytes; 0 = unlimited (default) */
 #define PRECOND_OPT_TIMING         7  /* 1 = record per-stage CUDA events (read by precond_get_timing) */
 #define PRECOND_OPT_USE_GRAPH      8  /* 1 = capture each distinct plan (shapes, options, workspace) once as a
@@ -78,6 +79,11 @@ typedef struct precond_ctx* precond_t;
                                          0 = per-step minimax step polynomial (default) */
 #define PRECOND_OPT_FOLD          10  /* minimax step: the interval's top may not fall below this
                                          fraction of its bottom's factor, T(1) >= fold T(l); [0, 1), default 0.3 */
+#define PRECOND_OPT_BRANCHES      11  /* 1 = when no root class's products fill the GPU (fewer 128 x 128
+                                         tiles than SMs), the iteration stage runs each class's M chain and
+                                         X chain on streams of the handle's own, joined back by events
+                                         (default 1); 0 = everything on the call's stream.  Results are
+                                         identical. */
 
 /*
  * Create a handle bound to `cuda_device` (>= 0).  cuda_device = -1 creates a

@@ -95,7 +95,7 @@ struct Plan {
 struct precond_ctx {
   int device = -1;
   double tol = 1e-5;
-  int max_iter = 0, min_iter = 4, engine = 0, small_dim = 512, timing = 0, use_graph = 1;
+  int max_iter = 0, min_iter = 4, engine = 0, small_dim = 0, timing = 0, use_graph = 1;
   int classical = 0;                   // 1: classical Newton step polynomial at every iteration
   double fold = 0.3;                   // minimax step: T(1) >= fold * T(l)
   double ws_max = 0;
@@ -130,6 +130,9 @@ struct precond_ctx {
   size_t graph_gemm_ev = 0;
   cudaStream_t gstream = nullptr;
   cudaEvent_t gev_in = nullptr, gev_out = nullptr;
+  bool branches = true;                // false: the iteration stage stays on the call's stream
+  std::vector<cudaStream_t> side;      // iteration-stage branches (two per root class)
+  std::vector<cudaEvent_t> sev;        // their fork / join events
   bool capturing = false;              // timing events become event-record nodes of the graph
 };
 
@@ -679,21 +682,69 @@ int launch_roots_start(const Ctx& c, float eps) {
   return PRECOND_OK;
 }
 
+// Streams and events for the iteration stage's branches (created on first use,
+// reused by every later call; events recorded under capture become graph edges).
+int side_streams(precond_ctx* h, size_t n) {
+  while (h->side.size() < n) {
+    cudaStream_t s;
+    CK(cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking));
+    h->side.push_back(s);
+  }
+  return PRECOND_OK;
+}
+
+int next_event(precond_ctx* h, size_t& used, cudaEvent_t* out) {
+  if (used == h->sev.size()) {
+    cudaEvent_t e;
+    CK(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    h->sev.push_back(e);
+  }
+  *out = h->sev[used++];
+  return PRECOND_OK;
+}
+
+// Newton-Schulz iterations of every root class.  When the products are too small
+// to fill the GPU, each class runs on two streams of its own: the M chain (D, F, M') and the X chain (X' = X T).  The X
+// update of iteration k waits for M_k (its operand) and the M' product of
+// iteration k waits for that X update, so the X product overlaps D and F, the
+// convergence flags that M' sets are never seen early by an X update, and the
+// classes (different d) overlap one another.
 int launch_iterations(const Ctx& c) {
   c.h->in_ns = true;
   c.h->gemm_ev_used = 0;
   struct Guard { precond_ctx* h; ~Guard() { h->in_ns = false; } } guard{c.h};
   const int p = c.P.p;
+  const size_t ncls = c.P.rc.size();
   int kall = 0;
   for (const auto& r : c.P.rc) kall = std::max(kall, r.kmax);
+  int rcode;
+  // branch only when no class's product fills the GPU (latency-bound plans): with
+  // full products the branches would only compete for the same SMs
+  bool small = true;
+  for (const auto& r : c.P.rc) {
+    const long long tn = (r.d + TC_BN - 1) / TC_BN;
+    if ((long long)r.roots.size() * tn * (tn + 1) / 2 >= c.h->num_sms) small = false;
+  }
+  const bool br = c.h->branches && small;
+  size_t used = 0;
+  cudaEvent_t fork = nullptr;
+  if (br) {
+    if ((rcode = side_streams(c.h, 2 * ncls))) return rcode;
+    if ((rcode = next_event(c.h, used, &fork))) return rcode;
+    CK(cudaEventRecord(fork, c.st));
+    for (size_t i = 0; i < 2 * ncls; ++i) CK(cudaStreamWaitEvent(c.h->side[i], fork, 0));
+  }
+  std::vector<cudaEvent_t> mready(ncls, fork);     // per class: M_k sliced
   int64_t n = 0;
   for (int k = 0; k < kall; ++k) {
-    for (const auto& r : c.P.rc) {
+    for (size_t ri = 0; ri < ncls; ++ri) {
+      const RootClass& r = c.P.rc[ri];
       if (k >= r.kmax) continue;
+      const Ctx cm{c.h, c.P, c.ws, br ? c.h->side[2 * ri] : c.st};       // M chain
+      const Ctx cx{c.h, c.P, c.ws, br ? c.h->side[2 * ri + 1] : c.st};   // X chain
       const int nb = (int)r.roots.size(), d = r.d, eng = r.eng;
       const int* root_of = c.at<const int>(r.t_root);
       const int cur = k & 1, nxt = (k + 1) & 1;
-      int rcode;
       Epi e = base_epi(c, EPI_STORE, d, d);
       e.root_of = root_of;
       e.partials = c.at<double>(c.P.partials);
@@ -711,29 +762,37 @@ int launch_iterations(const Ctx& c) {
       // so every product operand (M, D, F, X) keeps its information in its own
       // digits instead of next to a dominant identity.
       const double al = r.steps.alpha[k], be = r.steps.beta[k];
-      auto aff = [&](const Slab& A, const Slab& B, const Slab& In, const Slab& C, double alpha, double beta_in,
-                     int digits) -> int {
+      auto aff = [&](const Ctx& cc, const Slab& A, const Slab& B, const Slab& In, const Slab& C, double alpha,
+                     double beta_in, int digits) -> int {
         Epi ea = e;
         ea.kind = EPI_AFF;
-        ea.C = c.plane(C);
-        ea.In = c.plane(In);
+        ea.C = cc.plane(C);
+        ea.In = cc.plane(In);
         ea.alpha = alpha;
         ea.beta_in = beta_in;
         ea.gamma = 0.0;
         int rc2;
-        if (tc && (rc2 = clear_rowmax(c, C))) return rc2;
-        if ((rc2 = gemm(c, eng, A, B, d, d, d, nullptr, nullptr, digits, ea, nb, true))) return rc2;
+        if (tc && (rc2 = clear_rowmax(cc, C))) return rc2;
+        if ((rc2 = gemm(cc, eng, A, B, d, d, d, nullptr, nullptr, digits, ea, nb, true))) return rc2;
         ++n;
-        if (tc && (rc2 = slice(c, C))) return rc2;
+        if (tc && (rc2 = slice(cc, C))) return rc2;
         return PRECOND_OK;
       };
       // T = al I - be M:  T^2 = al^2 I + D, D = be^2 M M - 2 al be M;  T^4 = al^4 I + F,
       // F = D D + 2 al^2 D;  M' = al^p M + (D or F) M;  X' = X T = al X - be X M
-      if (k >= 1 && (rcode = aff(r.X[cur], r.M[cur], r.X[cur], r.X[nxt], -be, al, 4))) return rcode;
-      if ((rcode = aff(r.M[cur], r.M[cur], r.M[cur], r.D, be * be, -2.0 * al * be, 4))) return rcode;
+      cudaEvent_t xdone = nullptr;
+      if (k >= 1) {
+        if (br) CK(cudaStreamWaitEvent(cx.st, mready[ri], 0));
+        if ((rcode = aff(cx, r.X[cur], r.M[cur], r.X[cur], r.X[nxt], -be, al, 4))) return rcode;
+        if (br) {
+          if ((rcode = next_event(c.h, used, &xdone))) return rcode;
+          CK(cudaEventRecord(xdone, cx.st));
+        }
+      }
+      if ((rcode = aff(cm, r.M[cur], r.M[cur], r.M[cur], r.D, be * be, -2.0 * al * be, 4))) return rcode;
       const Slab* Pk = &r.D;
       if (p == 4) {
-        if ((rcode = aff(r.D, r.D, r.D, r.F, 1.0, 2.0 * al * al, 4))) return rcode;
+        if ((rcode = aff(cm, r.D, r.D, r.D, r.F, 1.0, 2.0 * al * al, 4))) return rcode;
         Pk = &r.F;
       }
       Epi em = e;     // M_{k+1} = tau^p M_k + P M_k, residual, convergence
@@ -741,13 +800,25 @@ int launch_iterations(const Ctx& c) {
       em.C = c.plane(r.M[nxt]);
       em.In = c.plane(r.M[cur]);
       em.beta_in = std::pow(al, p);
+      if (xdone) CK(cudaStreamWaitEvent(cm.st, xdone, 0));
       // symmetric product (upper-triangle tiles mirrored): M' is exactly symmetric,
       // which also removes the antisymmetric mode the iteration would amplify
-      if (tc && (rcode = clear_rowmax(c, r.M[nxt]))) return rcode;
-      if ((rcode = gemm(c, eng, *Pk, r.M[cur], d, d, d, nullptr, nullptr, 4, em, nb, true))) return rcode;
+      if (tc && (rcode = clear_rowmax(cm, r.M[nxt]))) return rcode;
+      if ((rcode = gemm(cm, eng, *Pk, r.M[cur], d, d, d, nullptr, nullptr, 4, em, nb, true))) return rcode;
       ++n;
-      if (tc && (rcode = slice(c, r.M[nxt]))) return rcode;
+      if (tc && (rcode = slice(cm, r.M[nxt]))) return rcode;
+      if (br) {
+        if ((rcode = next_event(c.h, used, &mready[ri]))) return rcode;
+        CK(cudaEventRecord(mready[ri], cm.st));
+      }
     }
+  }
+  // join every branch back into the caller's stream
+  for (size_t i = 0; br && i < 2 * ncls; ++i) {
+    cudaEvent_t j;
+    if ((rcode = next_event(c.h, used, &j))) return rcode;
+    CK(cudaEventRecord(j, c.h->side[i]));
+    CK(cudaStreamWaitEvent(c.st, j, 0));
   }
   c.h->ns_launches = n;
   return PRECOND_OK;
@@ -925,7 +996,7 @@ std::string plan_key(const precond_ctx* h, const Plan& P, float beta, float eps)
   std::ostringstream k;
   k << P.step << ' ' << P.count << ' ' << P.nroots << ' ' << P.p << ' ' << P.dtype << ' ' << P.out_f32 << ' '
     << P.total << ' ' << P.meta << ' ' << P.meta_bytes << ' ' << P.max_tiles << ' ' << beta << ' ' << eps << ' '
-    << h->tol << ' ' << h->min_iter << ' ' << h->timing << ' ' << h->ws;
+    << h->tol << ' ' << h->min_iter << ' ' << h->timing << ' ' << h->branches << ' ' << h->ws;
   for (const auto& r : P.rc) {
     k << " r" << r.d << ',' << r.eng << ',' << r.roots.size() << ',' << r.kmax;
     for (size_t i = 0; i < r.steps.alpha.size(); ++i) k << ',' << r.steps.alpha[i] << ':' << r.steps.beta[i];
@@ -1045,6 +1116,8 @@ int precond_destroy(precond_t h) {
       for (auto& e : h->ev) cudaEventDestroy(e);
     for (auto& e : h->gemm_ev) cudaEventDestroy(e);
     drop_graph(h);
+    for (auto& x : h->side) cudaStreamDestroy(x);
+    for (auto& x : h->sev) cudaEventDestroy(x);
     if (h->gstream) cudaStreamDestroy(h->gstream);
     if (h->gev_in) cudaEventDestroy(h->gev_in);
     if (h->gev_out) cudaEventDestroy(h->gev_out);
@@ -1100,6 +1173,10 @@ int precond_set_option(precond_t h, int key, double v) {
     case PRECOND_OPT_USE_GRAPH:
       if (v != 0 && v != 1) return PRECOND_EINVAL;
       h->use_graph = (int)v;
+      return PRECOND_OK;
+    case PRECOND_OPT_BRANCHES:
+      if (v != 0 && v != 1) return PRECOND_EINVAL;
+      h->branches = v != 0;
       return PRECOND_OK;
   }
   return PRECOND_EINVAL;
@@ -1404,6 +1481,7 @@ extern "C" int precond_inv_root_noalloc(const float* A, int64_t d, float eps, fl
   precond_ctx h;          // options only; its workspace points at the scratch
   h.device = dev;
   h.engine = 1;           // fp64 SIMT engine
+  h.branches = false;     // no streams or events of its own: everything on the call's stream
   Plan P;
   const int64_t dims[1] = {d};
   const float* As[1] = {A};

@@ -14,7 +14,7 @@ def to_dev(a, dtype=None):
     return t.to(dtype) if dtype is not None else t
 
 
-def run_steps(shapes, grads_per_step, dtype, beta, eps, power, engine=0, small_dim=512, check_roots=True,
+def run_steps(shapes, grads_per_step, dtype, beta, eps, power, engine=0, small_dim=0, check_roots=True,
               extra_opts=None):
     """Run len(grads_per_step) steps on the GPU and in the oracle; return the
     worst relative Frobenius errors (U, X_L, X_R) and the last stats."""

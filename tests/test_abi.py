@@ -151,3 +151,14 @@ def test_host_handle_has_no_stats(host):
     assert lib.precond_get_stats(host.h, 2, None, None, None, None) == sr.ENODEV
     assert lib.precond_get_root(host.h, 0, ctypes.c_void_p(host.fake()), None) == sr.ENODEV
     assert lib.precond_launch_count(host.h) == 0
+
+
+def test_option_keys_match_header():
+    """Every PRECOND_OPT_* key of the header has the same value in the binding."""
+    import re
+    import shampoo_roots_gb300 as sr
+    text = open(os.path.join(ROOT, "include", "precond.h")).read()
+    keys = dict(re.findall(r"#define PRECOND_OPT_(\w+)\s+(\d+)", text))
+    assert len(keys) >= 11
+    for name, val in keys.items():
+        assert getattr(sr, "OPT_" + name) == int(val), name

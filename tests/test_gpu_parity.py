@@ -160,17 +160,20 @@ def test_bf16_in_place_output():
 @pytest.mark.gpu
 @pytest.mark.parametrize("engine", [1, 2])
 def test_graph_replay_matches_direct_launches(engine):
-    """The graph path replays one capture per plan with fresh pointer tables:
-    it must give bit-identical results to direct launches while the caller's
-    tensors move, the plan changes and comes back, and the caller uses a
-    non-default stream."""
+    """The graph path replays one capture per plan with fresh pointer tables and
+    runs the iteration stage on forked streams: it must give bit-identical
+    results to direct launches on one stream while the caller's tensors move,
+    the plan changes and comes back, and the caller uses a non-default stream."""
     import torch
     import shampoo_roots_gb300 as sr
     rng = np.random.default_rng(11)
     plans = [[(200, 72), (64, 136)], [(96, 40)], [(200, 72), (64, 136)], [(200, 72), (64, 136)]]
     results = {}
-    for use_graph in (0, 1):
-        pc = sr.Preconditioner(0, engine=engine, small_dim=0 if engine == 2 else 512, use_graph=use_graph)
+    # (graph, branches): direct launches on one stream, graph replay with the iteration
+    # stage on forked streams
+    for use_graph, branches in ((0, 0), (1, 1)):
+        pc = sr.Preconditioner(0, engine=engine, small_dim=0 if engine == 2 else 512, use_graph=use_graph,
+                               branches=branches)
         rng = np.random.default_rng(11)
         side = torch.cuda.Stream()
         state = {}
