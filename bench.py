@@ -31,6 +31,27 @@ METRIC = "preconditioner step ms and TFLOP/s (% GB300 tensor peak) vs CPU oracle
 WORKLOAD_INDEX = 1          # default: the 24-layer d=1024 stack, power -1/4
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of every rank's x: a job's time is its slowest rank's."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, steps: int, elapsed: float) -> float:
+    """Whole-job preconditioner steps per second: every rank ran `steps` steps
+    of its own stack (weak scaling) within `elapsed` seconds."""
+    return world * steps / elapsed
+
+
+def rank_step_seed(rank: int, step: int) -> int:
+    """Gradient-draw index of a rank's step: ranks draw disjoint batches."""
+    return 1000 * rank + step
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -240,7 +261,7 @@ def main():
         shapes = list(w.shapes)
         nroots = 2 * len(shapes)
         # two distinct gradient batches (ranks draw from their own seeds: weak scaling)
-        pools = [synth.torch_gradients_for_step(w, 1000 * rank + s, dev) for s in range(2)]
+        pools = [synth.torch_gradients_for_step(w, rank_step_seed(rank, s), dev) for s in range(2)]
         L = [torch.zeros((m, m), device=dev) for m, _ in shapes]
         R = [torch.zeros((n, n), device=dev) for _, n in shapes]
         out = [torch.empty((m, n), device=dev) for m, n in shapes]
@@ -295,12 +316,9 @@ def main():
         barrier()
     elapsed = sum(a.elapsed_time(b) for a, b in evs) / 1e3
     gpu_launches = sr.precond_launch_count(pc.h) - launches0
-    if dist is not None:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(elapsed, dist, dev)
     step_flops = step_flops_outside_roots(shapes) + root_flops / args.steps
-    value = world * args.steps / elapsed                       # preconditioner steps per second, whole job
+    value = job_rate(world, args.steps, elapsed)               # preconditioner steps per second, whole job
     tflops = world * step_flops * args.steps / elapsed / 1e12
     ms_per_step = elapsed / args.steps * 1e3
 
@@ -324,11 +342,8 @@ def main():
         e1.record(stream)
         barrier()
         t_e2e = e0.elapsed_time(e1) / 1e3
-        if dist is not None:
-            t = torch.tensor([t_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            t_e2e = float(t.item())
-        e2e = {"value": world * args.steps / t_e2e, "unit": "preconditioner steps/s",
+        t_e2e = max_over_ranks(t_e2e, dist, dev)
+        e2e = {"value": job_rate(world, args.steps, t_e2e), "unit": "preconditioner steps/s",
                "ms_per_step": t_e2e / args.steps * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     peaks = load_peaks()
