@@ -52,6 +52,33 @@ def rank_step_seed(rank: int, step: int) -> int:
     return 1000 * rank + step
 
 
+# DRAM traffic of the dominant kernel from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum of ten consecutive iteration-stage products of the d = 1024
+# stack; profiles/gemm_tc_kernel_dram_stack24.md), per launch over the step's launch
+# mix (as many 1024^2-class as 4096^2-class products).  Valid only for the kernel
+# sources it was taken on: their SHA-1s.
+TRAFFIC_CAPTURES = {
+    1: {"bytes_per_launch": 16.94e9, "algorithmic_bytes_per_launch": 12.67e9,
+        "sources": {"gemm_tc.cuh": "c25e1bdb09c7070e151cdde7b9cde0f3304ea01b",
+                    "engine.cuh": "4ed3254d617f51583c8c6d6ebfef32cc43e157e2",
+                    "common.cuh": "3a0606569dba3443ad53b51bafe5d746f025bfd7"}},
+}
+
+
+def captured_traffic(workload: int):
+    """(traffic, algorithmic bytes) per launch of the dominant kernel, or
+    (None, None) when no capture exists or the kernel changed since."""
+    import hashlib
+    cap = TRAFFIC_CAPTURES.get(workload)
+    if cap is None:
+        return None, None
+    for name, digest in cap["sources"].items():
+        with open(os.path.join(ROOT, "shampoo_roots_gb300", "csrc", name), "rb") as f:
+            if hashlib.sha1(f.read()).hexdigest() != digest:
+                return None, None
+    return cap["bytes_per_launch"], cap["algorithmic_bytes_per_launch"]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -202,14 +229,20 @@ def run_reference(args):
 
 
 def profile_small(args):
-    """A small case for ncu captures: inverse quarter roots of 4 SPD 2048^2
-    matrices of the conditioning-stress recipe (a few GB on the device)."""
+    """A small case for ncu captures: inverse quarter roots of a few SPD
+    matrices of the conditioning-stress recipe (default 4 of 2048^2; a few GB
+    on the device at most)."""
+    import dataclasses
     import torch
     import shampoo_roots_gb300 as sr
     from workloads import synth
     w = synth.workload(3)
     dev = torch.device("cuda")
-    A = [torch.from_numpy(a).to(dev) for a in synth.spd_inputs(w, matrices=range(4))]
+    if args.profile_dim == 2048 and args.profile_count == 4:
+        A = [torch.from_numpy(a).to(dev) for a in synth.spd_inputs(w, matrices=range(4))]
+    else:
+        wp = dataclasses.replace(w, dims=(args.profile_dim,) * args.profile_count)
+        A = synth.torch_spd_inputs(wp, dev)
     X = [torch.empty_like(a) for a in A]
     pc = sr.Preconditioner(0)
     for _ in range(args.warmup + args.steps):
@@ -231,6 +264,10 @@ def main():
     ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,
                     help="0 single 256x128, 1 stack p=-1/4 (default), 2 stack p=-1/2, 3 SPD 64x2048^2, 4 wide 6144")
     ap.add_argument("--power", type=float, default=None, help="override the workload's power")
+    ap.add_argument("--opt", action="append", default=[], metavar="KEY=VALUE",
+                    help="handle option (PRECOND_OPT_KEY, lower case), e.g. digits3_from=0.04")
+    ap.add_argument("--profile-dim", type=int, default=2048, help="profiling case: matrix side")
+    ap.add_argument("--profile-count", type=int, default=4, help="profiling case: number of matrices")
     ap.add_argument("--profile-small", action="store_true",
                     help="profiling case: roots of 4 SPD 2048^2 matrices, no JSON line")
     args = ap.parse_args()
@@ -256,7 +293,8 @@ def main():
 
     w = synth.workload(args.workload)
     power = args.power if args.power is not None else w.powers[0]
-    pc = sr.Preconditioner(local, timing=1)
+    opts = {k: float(v) for k, v in (o.split("=", 1) for o in args.opt)}
+    pc = sr.Preconditioner(local, timing=1, **opts)
     if w.kind == "step":
         shapes = list(w.shapes)
         nroots = 2 * len(shapes)
@@ -352,8 +390,10 @@ def main():
     peak = peaks["bf16_tflops_sustained"]
     # issued: tiles actually run (upper triangles of symmetric products) x 10 bf16 digit products
     issued = (issued_flops / (gemm_ms / 1e3) / 1e12) if gemm_ms > 0 else None
+    traffic, traffic_alg = captured_traffic(w.index)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": (achieved / peak) if achieved else None, "traffic": None,
+                "frac": (achieved / peak) if achieved else None, "traffic": traffic,
+                "traffic_algorithmic": traffic_alg,
                 "kernel": "gemm_tc_kernel<4> (iteration-stage products)",
                 "peak_kind": f"bf16 dense, sustained ({peaks['source']})",
                 "issued_tflops": issued, "issued_frac": (issued / peak) if issued else None,
@@ -374,6 +414,7 @@ def main():
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": w.name, "matrices": w.count, "roots": nroots,
                            "grad_dtype": w.dtype, "power": power, "beta": w.beta, "eps": w.eps,
+                           "options": opts,
                            "mean_iterations": statistics.mean(iters_seen) if iters_seen else None,
                            "l2": "inputs larger than L2 (129 MB): the state / input matrices of every workload but the single 256x128 one",
                            "numerics": "bf16 tensor-core digit products, exact fp32 accumulation of leading levels"},

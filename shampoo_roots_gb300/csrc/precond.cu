@@ -53,6 +53,7 @@ struct Slab {   // an engine-format matrix batch inside the workspace
 
 struct StepPoly {       // per-iteration step polynomial coefficients T_k = alpha_k I - beta_k M
   std::vector<double> alpha, beta;
+  std::vector<double> lo;   // bottom of the interval holding M_k's spectrum (0: not tracked)
 };
 
 struct RootClass {
@@ -98,6 +99,8 @@ struct precond_ctx {
   int max_iter = 0, min_iter = 4, engine = 0, small_dim = 0, timing = 0, use_graph = 1;
   int classical = 0;                   // 1: classical Newton step polynomial at every iteration
   double fold = 0.3;                   // minimax step: T(1) >= fold * T(l)
+  double digits3_from = 2.0;           // M-chain products use 3 digits once the interval bottom reaches this
+  std::map<std::string, StepPoly> schedules;   // step schedules already computed (keyed by l0, p, fold)
   double ws_max = 0;
   void* ws = nullptr;
   size_t ws_cap = 0;
@@ -206,6 +209,7 @@ static StepPoly step_schedule(double l0, int p, int max_steps, double fold) {
     const double sc = std::pow(gmax, -1.0 / p);
     sp.alpha.push_back(a * sc);
     sp.beta.push_back(sc);
+    sp.lo.push_back(l);
     l = r;
     if (1.0 - l < 1e-9) break;
   }
@@ -363,16 +367,25 @@ int build_plan(precond_ctx* h, Plan& P, bool step, int count, const int64_t* dim
   for (auto& r : P.rc) {
     layout_root_class(L, r, p);
     // interval of M_0's spectrum: [eps / c_max, 1], c_max = 1.01 tr(A_hat) >= c
-    r.steps = step_schedule(eps / (1.01 * (1.0 + r.d * eps)), p, 60, h->fold);
+    {
+      const double l0 = eps / (1.01 * (1.0 + r.d * eps));
+      char key[96];
+      snprintf(key, sizeof(key), "%.17g %d %.17g", l0, p, h->fold);
+      auto it = h->schedules.find(key);
+      if (it == h->schedules.end()) it = h->schedules.emplace(key, step_schedule(l0, p, 60, h->fold)).first;
+      r.steps = it->second;
+    }
     if (h->classical) {
       r.steps.alpha.assign(r.steps.alpha.size(), (p + 1.0) / p);
       r.steps.beta.assign(r.steps.beta.size(), 1.0 / p);
+      r.steps.lo.assign(r.steps.lo.size(), 0.0);
     }
     const int planned = h->classical ? iter_cap(eps, r.d, p, h->tol, 0) : (int)r.steps.alpha.size() + 3;
     r.kmax = h->max_iter > 0 ? h->max_iter : std::min(planned, 60);
     while ((int)r.steps.alpha.size() < std::max(r.kmax, 1)) {   // then Newton steps
       r.steps.alpha.push_back((p + 1.0) / p);
       r.steps.beta.push_back(1.0 / p);
+      r.steps.lo.push_back(h->classical ? 0.0 : 1.0);
     }
     const long long t = r.eng == ENGINE_F64
         ? (long long)((r.d + F64_BM - 1) / F64_BM) * ((r.d + F64_BN - 1) / F64_BN)
@@ -762,6 +775,12 @@ int launch_iterations(const Ctx& c) {
       // so every product operand (M, D, F, X) keeps its information in its own
       // digits instead of next to a dominant identity.
       const double al = r.steps.alpha[k], be = r.steps.beta[k];
+      // The M chain's rounding moves X by about (error) / (p l_k), l_k the bottom of
+      // M_k's spectrum: once l_k is large, 3 digits (6 products, ~2^-21) suffice there.
+      // The last iterations (l_k >= 1/2) keep 4 digits so that the residual reaches its
+      // tolerance, and the X products keep 4 digits (they inherit X's dynamic range).
+      const double lk = r.steps.lo[k];
+      const int mdig = (tc && lk >= c.h->digits3_from && lk < 0.5) ? 3 : 4;
       auto aff = [&](const Ctx& cc, const Slab& A, const Slab& B, const Slab& In, const Slab& C, double alpha,
                      double beta_in, int digits) -> int {
         Epi ea = e;
@@ -789,10 +808,10 @@ int launch_iterations(const Ctx& c) {
           CK(cudaEventRecord(xdone, cx.st));
         }
       }
-      if ((rcode = aff(cm, r.M[cur], r.M[cur], r.M[cur], r.D, be * be, -2.0 * al * be, 4))) return rcode;
+      if ((rcode = aff(cm, r.M[cur], r.M[cur], r.M[cur], r.D, be * be, -2.0 * al * be, mdig))) return rcode;
       const Slab* Pk = &r.D;
       if (p == 4) {
-        if ((rcode = aff(cm, r.D, r.D, r.D, r.F, 1.0, 2.0 * al * al, 4))) return rcode;
+        if ((rcode = aff(cm, r.D, r.D, r.D, r.F, 1.0, 2.0 * al * al, mdig))) return rcode;
         Pk = &r.F;
       }
       Epi em = e;     // M_{k+1} = tau^p M_k + P M_k, residual, convergence
@@ -804,7 +823,7 @@ int launch_iterations(const Ctx& c) {
       // symmetric product (upper-triangle tiles mirrored): M' is exactly symmetric,
       // which also removes the antisymmetric mode the iteration would amplify
       if (tc && (rcode = clear_rowmax(cm, r.M[nxt]))) return rcode;
-      if ((rcode = gemm(cm, eng, *Pk, r.M[cur], d, d, d, nullptr, nullptr, 4, em, nb, true))) return rcode;
+      if ((rcode = gemm(cm, eng, *Pk, r.M[cur], d, d, d, nullptr, nullptr, mdig, em, nb, true))) return rcode;
       ++n;
       if (tc && (rcode = slice(cm, r.M[nxt]))) return rcode;
       if (br) {
@@ -996,7 +1015,7 @@ std::string plan_key(const precond_ctx* h, const Plan& P, float beta, float eps)
   std::ostringstream k;
   k << P.step << ' ' << P.count << ' ' << P.nroots << ' ' << P.p << ' ' << P.dtype << ' ' << P.out_f32 << ' '
     << P.total << ' ' << P.meta << ' ' << P.meta_bytes << ' ' << P.max_tiles << ' ' << beta << ' ' << eps << ' '
-    << h->tol << ' ' << h->min_iter << ' ' << h->timing << ' ' << h->branches << ' ' << h->ws;
+    << h->tol << ' ' << h->min_iter << ' ' << h->timing << ' ' << h->branches << ' ' << h->digits3_from << ' ' << h->ws;
   for (const auto& r : P.rc) {
     k << " r" << r.d << ',' << r.eng << ',' << r.roots.size() << ',' << r.kmax;
     for (size_t i = 0; i < r.steps.alpha.size(); ++i) k << ',' << r.steps.alpha[i] << ':' << r.steps.beta[i];
@@ -1173,6 +1192,10 @@ int precond_set_option(precond_t h, int key, double v) {
     case PRECOND_OPT_USE_GRAPH:
       if (v != 0 && v != 1) return PRECOND_EINVAL;
       h->use_graph = (int)v;
+      return PRECOND_OK;
+    case PRECOND_OPT_DIGITS3_FROM:
+      if (!(v >= 0.0) || !std::isfinite(v)) return PRECOND_EINVAL;
+      h->digits3_from = v;
       return PRECOND_OK;
     case PRECOND_OPT_BRANCHES:
       if (v != 0 && v != 1) return PRECOND_EINVAL;

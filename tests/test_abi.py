@@ -162,3 +162,14 @@ def test_option_keys_match_header():
     assert len(keys) >= 11
     for name, val in keys.items():
         assert getattr(sr, "OPT_" + name) == int(val), name
+
+
+def test_bench_traffic_is_dropped_when_the_kernel_changes(monkeypatch):
+    """bench.py reports the captured DRAM traffic only for the kernel sources it
+    was captured on."""
+    import bench
+    cap = dict(bench.TRAFFIC_CAPTURES[1])
+    cap["sources"] = dict(cap["sources"], **{"gemm_tc.cuh": "0" * 40})
+    monkeypatch.setitem(bench.TRAFFIC_CAPTURES, 1, cap)
+    assert bench.captured_traffic(1) == (None, None)
+    assert bench.captured_traffic(0) == (None, None)

@@ -12,7 +12,7 @@ from workloads import synth
 pytestmark = pytest.mark.gpu
 
 
-def _stack_parity(index, steps, power, sample=None):
+def _stack_parity(index, steps, power, sample=None, opts=None):
     import torch
     import shampoo_roots_gb300 as sr
     w = synth.workload(index)
@@ -24,7 +24,7 @@ def _stack_parity(index, steps, power, sample=None):
     R = [torch.zeros((n, n), device=dev) for _, n in shapes]
     out = [torch.empty((m, n), device=dev) for m, n in shapes]
     st = oracle.OracleState([shapes[i] for i in sample])
-    pc = sr.Preconditioner(0)
+    pc = sr.Preconditioner(0, **(opts or {}))
     worst = {"U": 0.0, "XL": 0.0, "XR": 0.0}
     for s in range(steps):
         grads = synth.torch_gradients_for_step(w, s, dev)
@@ -45,6 +45,7 @@ def _stack_parity(index, steps, power, sample=None):
     pc.close()
     print(f"workload {w.name} power {power}: worst relative Frobenius errors {worst}")
     assert max(worst.values()) <= TOL, worst
+    return worst
 
 
 def test_stack_quarter_power_full_size():
@@ -68,13 +69,17 @@ def test_wide_6144_full_size():
 def test_spd64_2048_full_size(power):
     """64 SPD 2048^2 matrices with log-uniform spectra on [1e-8, 1], eps 1e-6
     relative to the trace; roots of all 64, oracle on 4 of them."""
+    _spd_parity(power)
+
+
+def _spd_parity(power, opts=None):
     import torch
     import shampoo_roots_gb300 as sr
     w = synth.workload(3)
     dev = torch.device("cuda")
     A = synth.torch_spd_inputs(w, dev)
     X = [torch.empty_like(a) for a in A]
-    pc = sr.Preconditioner(0)
+    pc = sr.Preconditioner(0, **(opts or {}))
     sr.precond_inv_root(pc.h, A, X, w.eps, power)
     _, _, status, _ = sr.precond_get_stats(pc.h, len(A))
     pc.close()
@@ -86,3 +91,4 @@ def test_spd64_2048_full_size(power):
     print(f"workload {w.name} power {power}: relative Frobenius errors {errs}")
     for i, err in errs.items():
         assert err <= TOL, (i, err)
+    return errs
