@@ -84,12 +84,6 @@ typedef struct precond_ctx* precond_t;
                                          X chain on streams of the handle's own, joined back by events
                                          (default 1); 0 = everything on the call's stream.  Results are
                                          identical. */
-#define PRECOND_OPT_DIGITS3_FROM  12  /* the M chain's products (M M, D D, F M) use 3 bf16 digits (6 MMAs,
-                                         about 2^-21) instead of 4 (10 MMAs, about 2^-28) in the
-                                         iterations whose interval bottom l_k (the minimax schedule's
-                                         bound on M_k's smallest eigenvalue) lies in [this value, 1/2);
-                                         default 2 (4 digits everywhere).  Experimental: measured to save
-                                         at most 7 % on the d = 1024 stack. */
 
 /*
  * Create a handle bound to `cuda_device` (>= 0).  cuda_device = -1 creates a

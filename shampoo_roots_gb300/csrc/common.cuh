@@ -26,7 +26,10 @@ struct RootStat {
   int kfinal;          // iteration index whose X is the result (X buffer kfinal & 1)
   unsigned int arrivals;  // tiles of the M product finished (cumulative over iterations)
   int nonfinite;       // NaN/Inf seen in the input or the Gram
-  int pad[2];
+  float sac;           // start: 1 / (2 tr c)   (M_0 = (A + A^T) sac + eps / c I)
+  float seps;          // start: eps / c
+  float fin;           // finish: c^(-1/p)
+  int pad;
 };
 
 // Per-matrix scalars of a step.

@@ -53,7 +53,6 @@ struct Slab {   // an engine-format matrix batch inside the workspace
 
 struct StepPoly {       // per-iteration step polynomial coefficients T_k = alpha_k I - beta_k M
   std::vector<double> alpha, beta;
-  std::vector<double> lo;   // bottom of the interval holding M_k's spectrum (0: not tracked)
 };
 
 struct RootClass {
@@ -99,7 +98,6 @@ struct precond_ctx {
   int max_iter = 0, min_iter = 4, engine = 0, small_dim = 0, timing = 0, use_graph = 1;
   int classical = 0;                   // 1: classical Newton step polynomial at every iteration
   double fold = 0.3;                   // minimax step: T(1) >= fold * T(l)
-  double digits3_from = 2.0;           // M-chain products use 3 digits once the interval bottom reaches this
   std::map<std::string, StepPoly> schedules;   // step schedules already computed (keyed by l0, p, fold)
   double ws_max = 0;
   void* ws = nullptr;
@@ -209,7 +207,6 @@ static StepPoly step_schedule(double l0, int p, int max_steps, double fold) {
     const double sc = std::pow(gmax, -1.0 / p);
     sp.alpha.push_back(a * sc);
     sp.beta.push_back(sc);
-    sp.lo.push_back(l);
     l = r;
     if (1.0 - l < 1e-9) break;
   }
@@ -378,14 +375,12 @@ int build_plan(precond_ctx* h, Plan& P, bool step, int count, const int64_t* dim
     if (h->classical) {
       r.steps.alpha.assign(r.steps.alpha.size(), (p + 1.0) / p);
       r.steps.beta.assign(r.steps.beta.size(), 1.0 / p);
-      r.steps.lo.assign(r.steps.lo.size(), 0.0);
     }
     const int planned = h->classical ? iter_cap(eps, r.d, p, h->tol, 0) : (int)r.steps.alpha.size() + 3;
     r.kmax = h->max_iter > 0 ? h->max_iter : std::min(planned, 60);
     while ((int)r.steps.alpha.size() < std::max(r.kmax, 1)) {   // then Newton steps
       r.steps.alpha.push_back((p + 1.0) / p);
       r.steps.beta.push_back(1.0 / p);
-      r.steps.lo.push_back(h->classical ? 0.0 : 1.0);
     }
     const long long t = r.eng == ENGINE_F64
         ? (long long)((r.d + F64_BM - 1) / F64_BM) * ((r.d + F64_BN - 1) / F64_BN)
@@ -623,8 +618,15 @@ int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int 
 }
 
 // Per-row-scaled digits of a slab's fp32 form.
-int slice(const Ctx& c, const Slab& s) {
+// Blocks per root of the start / finish kernels: one per 32-row strip.
+unsigned int tile_blocks(int d) { return (unsigned int)((d + 31) / 32); }
+
+// `root_of` (a root class's batch-entry -> root table, or null): skip the
+// entries of converged roots (iteration stage only).
+int slice(const Ctx& c, const Slab& s, const int* root_of = nullptr) {
   SliceArgs a;
+  a.root_of = root_of;
+  a.stats = c.stats();
   a.src = c.at<const float>(s.f32);
   a.src_bstride = (long long)s.rows * s.ld;
   a.src_ld = s.ld;
@@ -680,7 +682,8 @@ int launch_roots_start(const Ctx& c, float eps) {
     root_stats_kernel<<<dim3(rb, nb), 256, 0, c.st>>>(a);
     root_trace_kernel<<<nb, 256, 0, c.st>>>(a);
     root_bound_kernel<<<dim3(rb, nb), 256, r.d <= 12288 ? r.d * sizeof(float) : 0, c.st>>>(a);
-    dim3 g((r.d + 31) / 32, (r.d + 31) / 32, nb);
+    root_scalar_kernel<<<(nb + 127) / 128, 128, 0, c.st>>>(a, nb);
+    dim3 g(tile_blocks(r.d), 1, nb);
     int rc;
     if (r.eng == ENGINE_F64) {
       root_init_kernel<ENGINE_F64><<<g, 256, 0, c.st>>>(a);
@@ -688,7 +691,7 @@ int launch_roots_start(const Ctx& c, float eps) {
       if ((rc = clear_rowmax(c, r.M[0])) || (rc = clear_rowmax(c, r.X[1]))) return rc;
       root_init_kernel<ENGINE_TC><<<g, 256, 0, c.st>>>(a);
     }
-    c.h->launches += 4;
+    c.h->launches += 5;
     CK(cudaGetLastError());
     if (r.eng == ENGINE_TC && ((rc = slice(c, r.M[0])) || (rc = slice(c, r.X[1])))) return rc;
   }
@@ -775,12 +778,9 @@ int launch_iterations(const Ctx& c) {
       // so every product operand (M, D, F, X) keeps its information in its own
       // digits instead of next to a dominant identity.
       const double al = r.steps.alpha[k], be = r.steps.beta[k];
-      // The M chain's rounding moves X by about (error) / (p l_k), l_k the bottom of
-      // M_k's spectrum: once l_k is large, 3 digits (6 products, ~2^-21) suffice there.
-      // The last iterations (l_k >= 1/2) keep 4 digits so that the residual reaches its
-      // tolerance, and the X products keep 4 digits (they inherit X's dynamic range).
-      const double lk = r.steps.lo[k];
-      const int mdig = (tc && lk >= c.h->digits3_from && lk < 0.5) ? 3 : 4;
+      // every product of the iteration takes 4 digits: 3 (about 2^-21), even only in the
+      // middle iterations, put the roots' errors at 2e-3 to 7e-3
+      const int mdig = 4;
       auto aff = [&](const Ctx& cc, const Slab& A, const Slab& B, const Slab& In, const Slab& C, double alpha,
                      double beta_in, int digits) -> int {
         Epi ea = e;
@@ -794,7 +794,7 @@ int launch_iterations(const Ctx& c) {
         if (tc && (rc2 = clear_rowmax(cc, C))) return rc2;
         if ((rc2 = gemm(cc, eng, A, B, d, d, d, nullptr, nullptr, digits, ea, nb, true))) return rc2;
         ++n;
-        if (tc && (rc2 = slice(cc, C))) return rc2;
+        if (tc && (rc2 = slice(cc, C, root_of))) return rc2;
         return PRECOND_OK;
       };
       // T = al I - be M:  T^2 = al^2 I + D, D = be^2 M M - 2 al be M;  T^4 = al^4 I + F,
@@ -825,7 +825,7 @@ int launch_iterations(const Ctx& c) {
       if (tc && (rcode = clear_rowmax(cm, r.M[nxt]))) return rcode;
       if ((rcode = gemm(cm, eng, *Pk, r.M[cur], d, d, d, nullptr, nullptr, mdig, em, nb, true))) return rcode;
       ++n;
-      if (tc && (rcode = slice(cm, r.M[nxt]))) return rcode;
+      if (tc && (rcode = slice(cm, r.M[nxt], root_of))) return rcode;
       if (br) {
         if ((rcode = next_event(c.h, used, &mready[ri]))) return rcode;
         CK(cudaEventRecord(mready[ri], cm.st));
@@ -847,7 +847,7 @@ int launch_finish(const Ctx& c, float eps) {
   for (const auto& r : c.P.rc) {
     const int nb = (int)r.roots.size();
     RootArgs a = root_args(c, r, eps);
-    dim3 g((r.d + 31) / 32, (r.d + 31) / 32, nb);
+    dim3 g(tile_blocks(r.d), 1, nb);
     int rc;
     if (r.eng == ENGINE_TC && c.P.step && (rc = clear_rowmax(c, r.Xf))) return rc;
     if (r.eng == ENGINE_F64) root_finish_kernel<ENGINE_F64><<<g, 256, 0, c.st>>>(a);
@@ -1015,7 +1015,7 @@ std::string plan_key(const precond_ctx* h, const Plan& P, float beta, float eps)
   std::ostringstream k;
   k << P.step << ' ' << P.count << ' ' << P.nroots << ' ' << P.p << ' ' << P.dtype << ' ' << P.out_f32 << ' '
     << P.total << ' ' << P.meta << ' ' << P.meta_bytes << ' ' << P.max_tiles << ' ' << beta << ' ' << eps << ' '
-    << h->tol << ' ' << h->min_iter << ' ' << h->timing << ' ' << h->branches << ' ' << h->digits3_from << ' ' << h->ws;
+    << h->tol << ' ' << h->min_iter << ' ' << h->timing << ' ' << h->branches << ' ' << h->ws;
   for (const auto& r : P.rc) {
     k << " r" << r.d << ',' << r.eng << ',' << r.roots.size() << ',' << r.kmax;
     for (size_t i = 0; i < r.steps.alpha.size(); ++i) k << ',' << r.steps.alpha[i] << ':' << r.steps.beta[i];
@@ -1192,10 +1192,6 @@ int precond_set_option(precond_t h, int key, double v) {
     case PRECOND_OPT_USE_GRAPH:
       if (v != 0 && v != 1) return PRECOND_EINVAL;
       h->use_graph = (int)v;
-      return PRECOND_OK;
-    case PRECOND_OPT_DIGITS3_FROM:
-      if (!(v >= 0.0) || !std::isfinite(v)) return PRECOND_EINVAL;
-      h->digits3_from = v;
       return PRECOND_OK;
     case PRECOND_OPT_BRANCHES:
       if (v != 0 && v != 1) return PRECOND_EINVAL;

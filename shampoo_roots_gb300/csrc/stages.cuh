@@ -110,6 +110,8 @@ __global__ void __launch_bounds__(256) prep_split_kernel(PrepArgs a) {
 // fp32 rows -> per-row-scaled digits: sigma_i = smallest power of two >= max_j |x_ij|.
 struct SliceArgs {
   const float* src; long long src_bstride; int src_ld;
+  const int* root_of;       // may be null; else batch entry -> root id, and converged roots are skipped
+  const RootStat* stats;
   const float* rowmax;      // [b][rows]
   float* rowscale;          // [b][rows] out
   Plane dst;                // digit form (scale unused)
@@ -137,6 +139,7 @@ __device__ __forceinline__ void digits4(float v, float inv, float (&d)[4]) {
 
 __global__ void __launch_bounds__(256) slice_rows_kernel(SliceArgs a) {
   const int b = blockIdx.y;
+  if (a.root_of && a.stats[a.root_of[b]].done) return;   // no further product reads these digits
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int r = blockIdx.x * 8 + warp; r < a.rows; r += gridDim.x * 8) {
     const float sigma = pow2_ceil(a.rowmax[(long long)b * a.rows + r]);
@@ -199,15 +202,17 @@ __global__ void __launch_bounds__(256) root_stats_kernel(RootArgs a) {
   RootStat* st = &a.stats[a.root_of[b]];
   int bad = 0;
   for (int r = blockIdx.x * 8 + warp; r < a.d; r += gridDim.x * 8) {
-    double s1 = 0.0, s2 = 0.0;
+    // per-lane fp32 partials (at most d/32 terms each), summed across the warp in
+    // fixed order in fp64: the sums feed bounds used with a 1.01 margin
+    float p1 = 0.f, p2 = 0.f;
     for (int c = lane; c < a.d; c += 32) {
-      const double v = A[(long long)r * a.d + c];
+      const float v = A[(long long)r * a.d + c];
       if (!isfinite(v)) bad = 1;
-      s1 += fabs(v);
-      s2 += v * v;
+      p1 += fabsf(v);
+      p2 = fmaf(v, v, p2);
     }
-    s1 = warp_sum(s1);
-    s2 = warp_sum(s2);
+    const double s1 = warp_sum((double)p1);
+    const double s2 = warp_sum((double)p2);
     if (lane == 0) {
       const long long o = (long long)b * a.d + r;
       a.rowabs[o] = s1;
@@ -291,68 +296,84 @@ __device__ __forceinline__ double root_scale(const RootStat& st, int d, double e
   return 1.01 * fmin(ws, st.minc);
 }
 
-// M_0 = A_hat / c and X_1 = X_0 T_0 = T_0 = alpha0 I - beta0 M_0.
+// Per-root scalars of the start and the finish, one thread per root: the start
+// scale c, the flags, 1 / (2 tr c), eps / c and c^(-1/p) (fp64 is slow on this
+// part, so the tile kernels only read these).
+__global__ void root_scalar_kernel(RootArgs a, int nb) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nb) return;
+  RootStat* st = &a.stats[a.root_of[b]];
+  const double eps = (double)a.eps;
+  const double t = st->trace;
+  const double c = root_scale(*st, a.d, eps);
+  const bool bad = st->nonfinite || !(t > 0.0) || !isfinite(t) || !isfinite(c) || !(c > 0.0);
+  st->c = c;
+  st->resid = 1e300;
+  st->iters = 0;
+  st->kfinal = 0;
+  st->done = bad ? 1 : 0;
+  st->status = bad ? PRECOND_ENONFINITE : PRECOND_OK;
+  st->sac = bad ? 0.f : (float)(0.5 / (t * c));
+  st->seps = bad ? 0.f : (float)(eps / c);
+  st->fin = bad ? 0.f : (float)pow(c, -1.0 / (double)a.ctl.p);
+}
+
+// M_0 = A_hat / c and X_1 = X_0 T_0 = T_0 = alpha0 I - beta0 M_0.  A block owns
+// 32-row strips of one root and walks their 32 x 32 tiles, so it holds the
+// strips' row maxima itself and stores them once (no atomics).
 template <int E>
 __global__ void __launch_bounds__(256) root_init_kernel(RootArgs a) {
   const int b = blockIdx.z;
-  RootStat* st = &a.stats[a.root_of[b]];
-  const double eps = (double)a.eps;
-  __shared__ double sh_c, sh_t;
-  __shared__ int sh_bad;
-  if (threadIdx.x == 0) {                 // per-root scalars once per block (fp64 is slow here)
-    const double t = st->trace;
-    const double c = root_scale(*st, a.d, eps);
-    sh_c = c;
-    sh_t = t;
-    sh_bad = st->nonfinite || !(t > 0.0) || !isfinite(t) || !isfinite(c) || !(c > 0.0);
-    if (blockIdx.x == 0 && blockIdx.y == 0) {
-      st->c = c;
-      st->resid = 1e300;
-      st->iters = 0;
-      st->kfinal = 0;
-      st->done = sh_bad ? 1 : 0;
-      st->status = sh_bad ? PRECOND_ENONFINITE : PRECOND_OK;
-    }
-  }
-  __syncthreads();
-  if (sh_bad) return;
-  const double t = sh_t, c = sh_c;
+  const RootStat* st = &a.stats[a.root_of[b]];
+  if (st->done) return;                         // non-finite input or trace
+  const float s_ac = st->sac, s_eps = st->seps;
+  const float al = (float)a.alpha0, be = (float)a.beta0;
   const float* A = a.src[b];
   __shared__ float tt[32][33];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-  for (int q = ty; q < 32; q += 8) {            // mirrored tile (rows c0.., cols r0..), coalesced
-    const int r = c0 + q, col = r0 + tx;
-    tt[q][tx] = (r < a.d && col < a.d) ? A[(long long)r * a.d + col] : 0.f;
-  }
-  __syncthreads();
-  const float s_ac = (float)(0.5 / (t * c)), s_eps = (float)(eps / c);
-  const float al = (float)a.alpha0, be = (float)a.beta0;
-  for (int q = ty; q < 32; q += 8) {
-    const int r = r0 + q, col = c0 + tx;
-    float mx = 0.f, xx = 0.f;
-    if (r < a.d && col < a.d) {
-      const bool dgl = (r == col);
-      // M_0 = ((A + A^T)/2 / tr + eps I) / c, exactly symmetric
-      const float m0 = fmaf(A[(long long)r * a.d + col] + tt[tx][q], s_ac, dgl ? s_eps : 0.f);
-      const float x1 = (dgl ? al : 0.f) - be * m0;
-      plane_store<E>(a.M0, b, r, col, m0);
-      plane_store<E>(a.X1, b, r, col, x1);
-      mx = fabsf(m0);
-      xx = fabsf(x1);
+  const int T = (a.d + 31) / 32;
+  for (int strip = blockIdx.x; strip < T; strip += gridDim.x) {
+    const int r0 = strip * 32;
+    float mx[4] = {0.f, 0.f, 0.f, 0.f}, xx[4] = {0.f, 0.f, 0.f, 0.f};   // rows r0 + ty + 8 j
+    for (int c0 = 0; c0 < a.d; c0 += 32) {
+      __syncthreads();                          // the previous tile's reads of tt are done
+      for (int q = ty; q < 32; q += 8) {        // mirrored tile (rows c0.., cols r0..), coalesced
+        const int r = c0 + q, col = r0 + tx;
+        tt[q][tx] = (r < a.d && col < a.d) ? A[(long long)r * a.d + col] : 0.f;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int q = ty + 8 * j;
+        const int r = r0 + q, col = c0 + tx;
+        if (r < a.d && col < a.d) {
+          const bool dgl = (r == col);
+          // M_0 = ((A + A^T)/2 / tr + eps I) / c, exactly symmetric
+          const float m0 = fmaf(A[(long long)r * a.d + col] + tt[tx][q], s_ac, dgl ? s_eps : 0.f);
+          const float x1 = (dgl ? al : 0.f) - be * m0;
+          plane_store<E>(a.M0, b, r, col, m0);
+          plane_store<E>(a.X1, b, r, col, x1);
+          mx[j] = fmaxf(mx[j], fabsf(m0));
+          xx[j] = fmaxf(xx[j], fabsf(x1));
+        }
+      }
     }
     if (E == ENGINE_TC) {
-      mx = warp_max(mx);
-      xx = warp_max(xx);
-      if (tx == 0 && r < a.d) {
-        atomic_max_nonneg(&a.M0.rowmax[(long long)b * a.d + r], mx);
-        atomic_max_nonneg(&a.X1.rowmax[(long long)b * a.d + r], xx);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = r0 + ty + 8 * j;
+        const float m = warp_max(mx[j]), x = warp_max(xx[j]);
+        if (tx == 0 && r < a.d) {
+          a.M0.rowmax[(long long)b * a.d + r] = m;
+          a.X1.rowmax[(long long)b * a.d + r] = x;
+        }
       }
     }
   }
 }
 
-// Result = sym(X_kfinal) * c^(-1/p): to the engine plane Xf (step) or caller fp32 (inv_root).
+// Result = sym(X_kfinal) * c^(-1/p): to the engine plane Xf (step) or caller fp32
+// (inv_root).  Blocks own 32-row strips, as in the start.
 template <int E>
 __global__ void __launch_bounds__(256) root_finish_kernel(RootArgs a) {
   __shared__ float tile[32][33];
@@ -360,30 +381,39 @@ __global__ void __launch_bounds__(256) root_finish_kernel(RootArgs a) {
   const RootStat* st = &a.stats[a.root_of[b]];
   if (st->status == PRECOND_ENONFINITE || st->kfinal < 1) return;
   const Plane& X = a.X[st->kfinal & 1];
-  __shared__ float sh_f;
-  if (threadIdx.x == 0) sh_f = (float)pow(st->c, -1.0 / (double)a.ctl.p);   // once per block
-  __syncthreads();
-  const float f = sh_f;
+  const float f = st->fin;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-  // load the transposed tile (rows c0.., cols r0..)
-  for (int q = ty; q < 32; q += 8) {
-    const int r = c0 + q, col = r0 + tx;
-    tile[q][tx] = (r < a.d && col < a.d) ? (float)plane_load<E>(X, b, r, col) : 0.f;
-  }
-  __syncthreads();
-  for (int q = ty; q < 32; q += 8) {
-    const int r = r0 + q, col = c0 + tx;
-    float mx = 0.f;
-    if (r < a.d && col < a.d) {
-      const float v = 0.5f * ((float)plane_load<E>(X, b, r, col) + tile[tx][q]) * f;
-      if (a.dst) a.dst[b][(long long)r * a.d + col] = v;
-      else plane_store<E>(a.Xf, b, r, col, (double)v);
-      mx = fabsf(v);
+  const int T = (a.d + 31) / 32;
+  for (int strip = blockIdx.x; strip < T; strip += gridDim.x) {
+    const int r0 = strip * 32;
+    float mx[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int c0 = 0; c0 < a.d; c0 += 32) {
+      __syncthreads();                          // the previous tile's reads are done
+      // load the transposed tile (rows c0.., cols r0..)
+      for (int q = ty; q < 32; q += 8) {
+        const int r = c0 + q, col = r0 + tx;
+        tile[q][tx] = (r < a.d && col < a.d) ? (float)plane_load<E>(X, b, r, col) : 0.f;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int q = ty + 8 * j;
+        const int r = r0 + q, col = c0 + tx;
+        if (r < a.d && col < a.d) {
+          const float v = 0.5f * ((float)plane_load<E>(X, b, r, col) + tile[tx][q]) * f;
+          if (a.dst) a.dst[b][(long long)r * a.d + col] = v;
+          else plane_store<E>(a.Xf, b, r, col, (double)v);
+          mx[j] = fmaxf(mx[j], fabsf(v));
+        }
+      }
     }
     if (E == ENGINE_TC && !a.dst) {
-      mx = warp_max(mx);
-      if (tx == 0 && r < a.d) atomic_max_nonneg(&a.Xf.rowmax[(long long)b * a.d + r], mx);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = r0 + ty + 8 * j;
+        const float m = warp_max(mx[j]);
+        if (tx == 0 && r < a.d) a.Xf.rowmax[(long long)b * a.d + r] = m;
+      }
     }
   }
 }
