@@ -84,6 +84,11 @@ typedef struct precond_ctx* precond_t;
                                          X chain on streams of the handle's own, joined back by events
                                          (default 1); 0 = everything on the call's stream.  Results are
                                          identical. */
+#define PRECOND_OPT_STEP_DEGREE   12  /* degree of the per-step minimax polynomial T_k(M) at p = 4: 2 (default;
+                                         T = a I - b M + c M^2, 5 products per iteration, about 7
+                                         iterations from l_0 = 1e-6) or 1 (T = a I - b M, 4 products, about
+                                         10 iterations).  p = 2 always takes linear steps (both degrees
+                                         need 36 products there). */
 
 /*
  * Create a handle bound to `cuda_device` (>= 0).  cuda_device = -1 creates a
@@ -218,6 +223,21 @@ int precond_debug_plane(precond_t h, int r, int which, float* dst, void* stream)
 #define PRECOND_NOALLOC_MAX_D 256
 int precond_inv_root_noalloc(const float* A, int64_t d, float eps, float power, float* X, void* stream,
                              int* status);
+
+/*
+ * The per-step minimax schedule the iteration uses (host only, no device or
+ * handle needed): for p in {2, 4}, the interval bottom l0 in (0, 1) of M_0's
+ * spectrum, the fold cap in [0, 1) and the polynomial degree (1 or 2), the
+ * coefficients of T_k(m) = alpha_k - beta_k m + gamma_k m^2 and the interval
+ * bottom lo_k each step starts from, up to max_steps steps (the schedule ends
+ * when 1 - lo < 1e-9).  Arrays hold max_steps doubles; *nsteps receives the
+ * number written.  Every step maps [lo_k, 1] into [lo_(k+1), 1] with
+ * max m T_k(m)^p = 1.  The pages have no counterpart: the step polynomials
+ * follow the idea of per-step optimised polynomials (CANS, "Online KL
+ * Shampoo" section 2.3) for the coupled iteration.  EINVAL on bad arguments.
+ */
+int precond_step_schedule(int p, double l0, double fold, int degree, int max_steps, double* alpha, double* beta,
+                          double* gamma, double* lo, int* nsteps);
 
 /* Static text for a status code. */
 const char* precond_error_string(int code);

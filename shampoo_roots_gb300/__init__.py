@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(HERE, "libprecond.so")
 OK, EINVAL, ENOMEM, ECUDA, ENODEV, ENOTCONV, ENONFINITE = 0, -1, -2, -3, -4, -5, -6
 F32, BF16 = 0, 1
 OPT_TOL, OPT_MAX_ITER, OPT_MIN_ITER, OPT_ENGINE, OPT_SMALL_DIM, OPT_WORKSPACE_MAX, OPT_TIMING, OPT_USE_GRAPH, \
-    OPT_CLASSICAL, OPT_FOLD, OPT_BRANCHES = range(1, 12)
+    OPT_CLASSICAL, OPT_FOLD, OPT_BRANCHES, OPT_STEP_DEGREE = range(1, 13)
 
 _lib = None
 
@@ -55,12 +55,14 @@ def load():
     L.precond_debug_plane.argtypes = [vp, i32, i32, vp, vp]
     L.precond_inv_root_noalloc.argtypes = [vp, i64, f32, f32, vp, vp, ctypes.POINTER(i32)]
     L.precond_gemm_selftest.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, i32, vp]
+    L.precond_step_schedule.argtypes = [i32, f64, f64, i32, i32, ctypes.POINTER(f64), ctypes.POINTER(f64),
+                                        ctypes.POINTER(f64), ctypes.POINTER(f64), ctypes.POINTER(i32)]
     L.precond_error_string.argtypes = [i32]
     L.precond_error_string.restype = ctypes.c_char_p
     for name in ("precond_create", "precond_destroy", "precond_step", "precond_inv_root", "precond_get_stats",
                  "precond_set_option", "precond_get_timing", "precond_get_root", "precond_gemm_selftest",
                  "precond_debug_plane", "precond_get_gemm_timing",
-                 "precond_inv_root_noalloc"):
+                 "precond_inv_root_noalloc", "precond_step_schedule"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -71,6 +73,16 @@ def error_string(code: int) -> str:
 
 
 precond_error_string = error_string
+
+
+def precond_step_schedule(p: int, l0: float, fold: float = 0.3, degree: int = 2, max_steps: int = 60):
+    """The iteration's per-step minimax schedule: lists (alpha, beta, gamma, lo)
+    of T_k(m) = alpha_k - beta_k m + gamma_k m^2 and each step's interval bottom."""
+    arrs = [(ctypes.c_double * max_steps)() for _ in range(4)]
+    n = ctypes.c_int()
+    _check(load().precond_step_schedule(int(p), float(l0), float(fold), int(degree), int(max_steps), *arrs,
+                                        ctypes.byref(n)), "precond_step_schedule")
+    return tuple([a[i] for i in range(n.value)] for a in arrs)
 
 
 def _check(code: int, what: str) -> int:

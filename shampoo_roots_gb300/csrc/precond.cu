@@ -51,8 +51,9 @@ struct Slab {   // an engine-format matrix batch inside the workspace
   size_t f32 = 0, rowmax = 0, rowscale = 0;   // fp32 form + per-row max / scale (0: absent)
 };
 
-struct StepPoly {       // per-iteration step polynomial coefficients T_k = alpha_k I - beta_k M
-  std::vector<double> alpha, beta;
+struct StepPoly {       // per-iteration step polynomials T_k = alpha_k I - beta_k M + gamma_k M^2
+  std::vector<double> alpha, beta, gamma;
+  std::vector<double> lo;   // bottom of the interval [lo_k, 1] holding M_k's spectrum
 };
 
 struct RootClass {
@@ -98,7 +99,8 @@ struct precond_ctx {
   int max_iter = 0, min_iter = 4, engine = 0, small_dim = 0, timing = 0, use_graph = 1;
   int classical = 0;                   // 1: classical Newton step polynomial at every iteration
   double fold = 0.3;                   // minimax step: T(1) >= fold * T(l)
-  std::map<std::string, StepPoly> schedules;   // step schedules already computed (keyed by l0, p, fold)
+  std::map<std::string, StepPoly> schedules;   // step schedules already computed (keyed by l0, p, fold, degree)
+  int step_degree = 2;                 // 2: quadratic step polynomials at p = 4; 1: linear
   double ws_max = 0;
   void* ws = nullptr;
   size_t ws_cap = 0;
@@ -207,6 +209,109 @@ static StepPoly step_schedule(double l0, int p, int max_steps, double fold) {
     const double sc = std::pow(gmax, -1.0 / p);
     sp.alpha.push_back(a * sc);
     sp.beta.push_back(sc);
+    sp.gamma.push_back(0.0);
+    sp.lo.push_back(l);
+    l = r;
+    if (1.0 - l < 1e-9) break;
+  }
+  return sp;
+}
+
+// Quadratic steps T(m) = s (1 + u m + v m^2).  The map g(m) = m T(m)^p on [l, 1]
+// has its extrema at l, 1 and the roots of  1 + (p+1) u m + (2p+1) v m^2 = 0
+// (where T + p m T' vanishes), so its range is exact.  Returns min g / max g, or
+// 0 when T is not positive on [l, 1] or folds (min T < fold max T).
+static double quad_ratio(double l, double u, double v, int p, double fold, double* gmax_out) {
+  auto T = [&](double m) { return 1.0 + u * m + v * m * m; };
+  double tmin = std::min(T(l), T(1.0)), tmax = std::max(T(l), T(1.0));
+  if (v != 0.0) {
+    const double ms = -u / (2.0 * v);
+    if (ms > l && ms < 1.0) { tmin = std::min(tmin, T(ms)); tmax = std::max(tmax, T(ms)); }
+  }
+  if (!(tmin > 0.0) || tmin < fold * tmax) return 0.0;
+  auto g = [&](double m) { return m * std::pow(T(m), p); };
+  double gmin = std::min(g(l), g(1.0)), gmax = std::max(g(l), g(1.0));
+  const double A = (2.0 * p + 1.0) * v, B = (p + 1.0) * u, C = 1.0;
+  double roots[2];
+  int nr = 0;
+  if (A == 0.0) {
+    if (B != 0.0) roots[nr++] = -C / B;
+  } else {
+    const double disc = B * B - 4.0 * A * C;
+    if (disc >= 0.0) {
+      const double q = -0.5 * (B + std::copysign(std::sqrt(disc), B));
+      if (q != 0.0) roots[nr++] = q / A;
+      if (q != 0.0) roots[nr++] = C / q;
+    }
+  }
+  for (int i = 0; i < nr; ++i)
+    if (roots[i] > l && roots[i] < 1.0) { gmin = std::min(gmin, g(roots[i])); gmax = std::max(gmax, g(roots[i])); }
+  if (gmax_out) *gmax_out = gmax;
+  return gmin / gmax;
+}
+
+// Nelder-Mead on (u, v) maximising quad_ratio, from a few fixed starts and the
+// previous step's optimum; deterministic.
+static void quad_best(double l, int p, double fold, double& u, double& v) {
+  const double starts[][2] = {{u, v}, {-2.06, 1.52}, {-1.8, 1.3}, {-0.8, 0.38}, {-0.4, 0.111}, {-1.2, 0.6}};
+  double bu = u, bv = v, br = quad_ratio(l, u, v, p, fold, nullptr);
+  for (const auto& st : starts) {
+    double x[3][2] = {{st[0], st[1]}, {st[0] + 0.05, st[1]}, {st[0], st[1] + 0.05}};
+    double f[3];
+    for (int i = 0; i < 3; ++i) f[i] = -quad_ratio(l, x[i][0], x[i][1], p, fold, nullptr);
+    for (int it = 0; it < 600; ++it) {
+      int o[3] = {0, 1, 2};
+      std::sort(o, o + 3, [&](int a, int b) { return f[a] < f[b]; });
+      const int b0 = o[0], b1 = o[1], w = o[2];
+      const double cx = 0.5 * (x[b0][0] + x[b1][0]), cy = 0.5 * (x[b0][1] + x[b1][1]);
+      auto eval = [&](double t, double* px) {
+        px[0] = cx + t * (x[w][0] - cx);
+        px[1] = cy + t * (x[w][1] - cy);
+        return -quad_ratio(l, px[0], px[1], p, fold, nullptr);
+      };
+      double xr[2], xe[2], xc[2];
+      const double fr = eval(-1.0, xr);
+      if (fr < f[b0]) {
+        const double fe = eval(-2.0, xe);
+        if (fe < fr) { x[w][0] = xe[0]; x[w][1] = xe[1]; f[w] = fe; }
+        else { x[w][0] = xr[0]; x[w][1] = xr[1]; f[w] = fr; }
+      } else if (fr < f[b1]) {
+        x[w][0] = xr[0]; x[w][1] = xr[1]; f[w] = fr;
+      } else {
+        const double fc = eval(0.5, xc);
+        if (fc < f[w]) { x[w][0] = xc[0]; x[w][1] = xc[1]; f[w] = fc; }
+        else {
+          for (int i = 0; i < 3; ++i) {
+            if (i == b0) continue;
+            x[i][0] = 0.5 * (x[i][0] + x[b0][0]);
+            x[i][1] = 0.5 * (x[i][1] + x[b0][1]);
+            f[i] = -quad_ratio(l, x[i][0], x[i][1], p, fold, nullptr);
+          }
+        }
+      }
+      if (std::fabs(x[0][0] - x[1][0]) + std::fabs(x[0][1] - x[2][1]) + std::fabs(x[1][0] - x[2][0]) < 1e-13) break;
+    }
+    for (int i = 0; i < 3; ++i)
+      if (-f[i] > br) { br = -f[i]; bu = x[i][0]; bv = x[i][1]; }
+  }
+  u = bu;
+  v = bv;
+}
+
+// Per-step quadratic minimax schedule (see step_schedule for the linear one).
+static StepPoly step_schedule_quad(double l0, int p, int max_steps, double fold) {
+  StepPoly sp;
+  double l = l0, u = -2.06, v = 1.52;
+  for (int k = 0; k < max_steps; ++k) {
+    quad_best(l, p, fold, u, v);
+    double gmax;
+    const double r = quad_ratio(l, u, v, p, fold, &gmax);
+    if (!(r > 0.0)) break;
+    const double sc = std::pow(gmax, -1.0 / p);
+    sp.alpha.push_back(sc);
+    sp.beta.push_back(-sc * u);
+    sp.gamma.push_back(sc * v);
+    sp.lo.push_back(l);
     l = r;
     if (1.0 - l < 1e-9) break;
   }
@@ -366,21 +471,29 @@ int build_plan(precond_ctx* h, Plan& P, bool step, int count, const int64_t* dim
     // interval of M_0's spectrum: [eps / c_max, 1], c_max = 1.01 tr(A_hat) >= c
     {
       const double l0 = eps / (1.01 * (1.0 + r.d * eps));
+      // quadratic steps pay off at p = 4 (7 steps of 5 products instead of 10 of 4);
+      // at p = 2 both degrees need 36 products, so p = 2 keeps linear steps
+      const int deg = (p == 4 && !h->classical) ? h->step_degree : 1;
       char key[96];
-      snprintf(key, sizeof(key), "%.17g %d %.17g", l0, p, h->fold);
+      snprintf(key, sizeof(key), "%.17g %d %.17g %d", l0, p, h->fold, deg);
       auto it = h->schedules.find(key);
-      if (it == h->schedules.end()) it = h->schedules.emplace(key, step_schedule(l0, p, 60, h->fold)).first;
+      if (it == h->schedules.end())
+        it = h->schedules.emplace(key, deg == 2 ? step_schedule_quad(l0, p, 60, h->fold)
+                                                : step_schedule(l0, p, 60, h->fold)).first;
       r.steps = it->second;
     }
     if (h->classical) {
       r.steps.alpha.assign(r.steps.alpha.size(), (p + 1.0) / p);
       r.steps.beta.assign(r.steps.beta.size(), 1.0 / p);
+      r.steps.gamma.assign(r.steps.gamma.size(), 0.0);
     }
     const int planned = h->classical ? iter_cap(eps, r.d, p, h->tol, 0) : (int)r.steps.alpha.size() + 3;
     r.kmax = h->max_iter > 0 ? h->max_iter : std::min(planned, 60);
     while ((int)r.steps.alpha.size() < std::max(r.kmax, 1)) {   // then Newton steps
       r.steps.alpha.push_back((p + 1.0) / p);
       r.steps.beta.push_back(1.0 / p);
+      r.steps.gamma.push_back(0.0);
+      r.steps.lo.push_back(1.0);
     }
     const long long t = r.eng == ENGINE_F64
         ? (long long)((r.d + F64_BM - 1) / F64_BM) * ((r.d + F64_BN - 1) / F64_BN)
@@ -800,17 +913,58 @@ int launch_iterations(const Ctx& c) {
       // T = al I - be M:  T^2 = al^2 I + D, D = be^2 M M - 2 al be M;  T^4 = al^4 I + F,
       // F = D D + 2 al^2 D;  M' = al^p M + (D or F) M;  X' = X T = al X - be X M
       cudaEvent_t xdone = nullptr;
-      if (k >= 1) {
-        if (br) CK(cudaStreamWaitEvent(cx.st, mready[ri], 0));
-        if ((rcode = aff(cx, r.X[cur], r.M[cur], r.X[cur], r.X[nxt], -be, al, 4))) return rcode;
+      const double ga = r.steps.gamma[k];
+      const Slab* Pk = &r.D;
+      if (ga == 0.0) {
+        // linear step T = al I - be M
+        if (k >= 1) {
+          if (br) CK(cudaStreamWaitEvent(cx.st, mready[ri], 0));
+          if ((rcode = aff(cx, r.X[cur], r.M[cur], r.X[cur], r.X[nxt], -be, al, 4))) return rcode;
+          if (br) {
+            if ((rcode = next_event(c.h, used, &xdone))) return rcode;
+            CK(cudaEventRecord(xdone, cx.st));
+          }
+        }
+        if ((rcode = aff(cm, r.M[cur], r.M[cur], r.M[cur], r.D, be * be, -2.0 * al * be, mdig))) return rcode;
+        if (p == 4) {
+          if ((rcode = aff(cm, r.D, r.D, r.D, r.F, 1.0, 2.0 * al * al, mdig))) return rcode;
+          Pk = &r.F;
+        }
+      } else {
+        // quadratic step T = al I + E, E = ga M M - be M (p = 4):  X' = al X + X E,
+        // D = E E + 2 al E (= T^2 - al^2 I), F = D D + 2 al^2 D (= T^4 - al^4 I).
+        // E lives in F's slab: F is written after the last reads of E.
+        const Slab& E = r.F;
+        if ((rcode = aff(cm, r.M[cur], r.M[cur], r.M[cur], E, ga, -be, mdig))) return rcode;
+        if (br) {
+          cudaEvent_t eready;
+          if ((rcode = next_event(c.h, used, &eready))) return rcode;
+          CK(cudaEventRecord(eready, cm.st));
+          CK(cudaStreamWaitEvent(cx.st, eready, 0));
+        }
+        if (k == 0) {            // X_0 = I: X_1 = al I + E_0
+          ShiftArgs sa;
+          sa.src = cx.plane(E);
+          sa.dst = cx.plane(r.X[nxt]);
+          sa.root_of = root_of;
+          sa.stats = c.stats();
+          sa.d = d;
+          sa.alpha = (float)al;
+          dim3 g((unsigned int)std::min((d + 7) / 8, 1024), (unsigned int)nb);
+          if (eng == ENGINE_F64) shift_identity_kernel<ENGINE_F64><<<g, 256, 0, cx.st>>>(sa);
+          else shift_identity_kernel<ENGINE_TC><<<g, 256, 0, cx.st>>>(sa);
+          c.h->launches++;
+          CK(cudaGetLastError());
+          if (tc && (rcode = slice(cx, r.X[nxt], root_of))) return rcode;
+        } else if ((rcode = aff(cx, r.X[cur], E, r.X[cur], r.X[nxt], 1.0, al, 4))) {
+          return rcode;
+        }
         if (br) {
           if ((rcode = next_event(c.h, used, &xdone))) return rcode;
           CK(cudaEventRecord(xdone, cx.st));
         }
-      }
-      if ((rcode = aff(cm, r.M[cur], r.M[cur], r.M[cur], r.D, be * be, -2.0 * al * be, mdig))) return rcode;
-      const Slab* Pk = &r.D;
-      if (p == 4) {
+        if ((rcode = aff(cm, E, E, E, r.D, 1.0, 2.0 * al, mdig))) return rcode;
+        if (xdone) CK(cudaStreamWaitEvent(cm.st, xdone, 0));     // F overwrites E
         if ((rcode = aff(cm, r.D, r.D, r.D, r.F, 1.0, 2.0 * al * al, mdig))) return rcode;
         Pk = &r.F;
       }
@@ -1015,10 +1169,11 @@ std::string plan_key(const precond_ctx* h, const Plan& P, float beta, float eps)
   std::ostringstream k;
   k << P.step << ' ' << P.count << ' ' << P.nroots << ' ' << P.p << ' ' << P.dtype << ' ' << P.out_f32 << ' '
     << P.total << ' ' << P.meta << ' ' << P.meta_bytes << ' ' << P.max_tiles << ' ' << beta << ' ' << eps << ' '
-    << h->tol << ' ' << h->min_iter << ' ' << h->timing << ' ' << h->branches << ' ' << h->ws;
+    << h->tol << ' ' << h->min_iter << ' ' << h->timing << ' ' << h->branches << ' ' << h->step_degree << ' ' << h->ws;
   for (const auto& r : P.rc) {
     k << " r" << r.d << ',' << r.eng << ',' << r.roots.size() << ',' << r.kmax;
-    for (size_t i = 0; i < r.steps.alpha.size(); ++i) k << ',' << r.steps.alpha[i] << ':' << r.steps.beta[i];
+    for (size_t i = 0; i < r.steps.alpha.size(); ++i)
+      k << ',' << r.steps.alpha[i] << ':' << r.steps.beta[i] << ':' << r.steps.gamma[i];
   }
   for (const auto& c : P.sc) k << " s" << c.m << ',' << c.n << ',' << c.eng << ',' << c.mats.size();
   return k.str();
@@ -1193,6 +1348,10 @@ int precond_set_option(precond_t h, int key, double v) {
       if (v != 0 && v != 1) return PRECOND_EINVAL;
       h->use_graph = (int)v;
       return PRECOND_OK;
+    case PRECOND_OPT_STEP_DEGREE:
+      if (v != 1 && v != 2) return PRECOND_EINVAL;
+      h->step_degree = (int)v;
+      return PRECOND_OK;
     case PRECOND_OPT_BRANCHES:
       if (v != 0 && v != 1) return PRECOND_EINVAL;
       h->branches = v != 0;
@@ -1329,6 +1488,23 @@ int precond_get_gemm_timing(precond_t h, double* ms_total, int64_t* launches, do
     CK(cudaMemcpy(&n, (char*)h->ws + h->last_plan.err + 8, sizeof(n), cudaMemcpyDeviceToHost));
     *issued_flops = (double)n * 2.0 * TC_BM * TC_BN * TC_BK;
   }
+  return PRECOND_OK;
+}
+
+int precond_step_schedule(int p, double l0, double fold, int degree, int max_steps, double* alpha, double* beta,
+                          double* gamma, double* lo, int* nsteps) {
+  if ((p != 2 && p != 4) || (degree != 1 && degree != 2) || !(l0 > 0.0 && l0 < 1.0) || !(fold >= 0.0 && fold < 1.0) ||
+      max_steps < 1 || !alpha || !beta || !gamma || !lo || !nsteps)
+    return PRECOND_EINVAL;
+  const StepPoly sp = degree == 2 ? step_schedule_quad(l0, p, max_steps, fold) : step_schedule(l0, p, max_steps, fold);
+  const int n = std::min((int)sp.alpha.size(), max_steps);
+  for (int i = 0; i < n; ++i) {
+    alpha[i] = sp.alpha[i];
+    beta[i] = sp.beta[i];
+    gamma[i] = sp.gamma[i];
+    lo[i] = sp.lo[i];
+  }
+  *nsteps = n;
   return PRECOND_OK;
 }
 

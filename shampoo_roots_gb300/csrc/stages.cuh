@@ -418,6 +418,35 @@ __global__ void __launch_bounds__(256) root_finish_kernel(RootArgs a) {
   }
 }
 
+// X_1 = X_0 T_0 = alpha I + E_0 (X_0 = I) for quadratic steps, E_0 = T_0 - alpha I:
+// one warp per row, row maxima stored directly.  Converged or failed roots skip.
+struct ShiftArgs {
+  Plane src, dst;
+  const int* root_of;
+  const RootStat* stats;
+  int d;
+  float alpha;
+};
+
+template <int E>
+__global__ void __launch_bounds__(256) shift_identity_kernel(ShiftArgs a) {
+  const int b = blockIdx.y;
+  if (a.stats[a.root_of[b]].done) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = blockIdx.x * 8 + warp; r < a.d; r += gridDim.x * 8) {
+    float mx = 0.f;
+    for (int c = lane; c < a.d; c += 32) {
+      const float v = (float)plane_load<E>(a.src, b, r, c) + (r == c ? a.alpha : 0.f);
+      plane_store<E>(a.dst, b, r, c, (double)v);
+      mx = fmaxf(mx, fabsf(v));
+    }
+    if (E == ENGINE_TC) {
+      mx = warp_max(mx);
+      if (lane == 0) a.dst.rowmax[(long long)b * a.d + r] = mx;
+    }
+  }
+}
+
 // Caller fp32 -> engine plane (GEMM self-test inputs).
 template <int E>
 __global__ void f32_to_plane_kernel(const float* src, Plane p, int rows, int cols) {
