@@ -53,15 +53,16 @@ def rank_step_seed(rank: int, step: int) -> int:
 
 
 # DRAM traffic of the dominant kernel from one ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum of ten consecutive iteration-stage products of the d = 1024
-# stack; profiles/gemm_tc_kernel_dram_stack24.md), per launch over the step's launch
-# mix (as many 1024^2-class as 4096^2-class products).  Valid only for the kernel
+# dram__bytes_write.sum of one iteration's products of both root classes of the
+# d = 1024 stack; profiles/gemm_tc_kernel_dram_stack24.md), per launch over a step's
+# launch mix: per class 34 computed products (7 iterations) and 15 launches whose
+# roots have all converged (no tiles, no traffic).  Valid only for the kernel
 # sources it was taken on: their SHA-1s.
 TRAFFIC_CAPTURES = {
-    1: {"bytes_per_launch": 16.94e9, "algorithmic_bytes_per_launch": 12.67e9,
+    1: {"bytes_per_launch": 11.45e9, "algorithmic_bytes_per_launch": 7.04e9,
         "sources": {"gemm_tc.cuh": "c25e1bdb09c7070e151cdde7b9cde0f3304ea01b",
                     "engine.cuh": "4ed3254d617f51583c8c6d6ebfef32cc43e157e2",
-                    "common.cuh": "3a0606569dba3443ad53b51bafe5d746f025bfd7"}},
+                    "common.cuh": "983868160199120ad308ddf0b9fbbdd1021863c0"}},
 }
 
 
@@ -117,6 +118,11 @@ class Clocks:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
                                          stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            # wait (at most 3 s) for the sampler's first line, so that a short region
+            # still has the sample taken as it starts
+            t0 = time.time()
+            while time.time() - t0 < 3.0 and os.path.getsize(self.path) == 0:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self

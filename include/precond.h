@@ -153,7 +153,9 @@ int precond_set_option(precond_t h, int key, double value);
  * Milliseconds spent by stage in the last call when PRECOND_OPT_TIMING is on
  * (synchronises): ms[0] input preparation + Gram EMA, ms[1] bound + start,
  * ms[2] Newton-Schulz iterations, ms[3] finish + apply.  Also the number of
- * GEMM launches of the iteration stage and its algorithmic FLOPs.
+ * GEMM launches of the iteration stage and its algorithmic FLOPs: 2 d^3 per
+ * product each root executed (3 or 4 per linear step at p = 2 or 4, 5 per
+ * quadratic step, one fewer in the first iteration), summed over roots.
  */
 int precond_get_timing(precond_t h, double ms[4], int64_t* ns_gemm_launches, double* ns_flops);
 

@@ -1457,11 +1457,17 @@ int precond_get_timing(precond_t h, double ms[4], int64_t* ns_gemm_launches, dou
     std::vector<RootStat> st(h->last_nroots);
     CK(cudaMemcpy(st.data(), (char*)h->ws + h->last_plan.stats, sizeof(RootStat) * h->last_nroots,
                   cudaMemcpyDeviceToHost));
+    // products per iteration: 3 (p = 2) or 4 (p = 4) for a linear step, 5 for a
+    // quadratic one; iteration 0 has one fewer (X_1 is formed element-wise)
     const int g = h->last_p == 4 ? 4 : 3;
     double f = 0;
     for (int r = 0; r < h->last_nroots; ++r) {
       const double d = h->last_root_d[r];
-      if (st[r].iters > 0) f += 2.0 * d * d * d * (double)(st[r].iters * g - 1);
+      const StepPoly& sp = h->last_plan.rc[h->last_root_class[r]].steps;
+      long long prods = 0;
+      for (int k = 0; k < st[r].iters && k < (int)sp.gamma.size(); ++k)
+        prods += (sp.gamma[k] != 0.0 ? 5 : g) - (k == 0 ? 1 : 0);
+      f += 2.0 * d * d * d * (double)prods;
     }
     *ns_flops = f;
   }
