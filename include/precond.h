@@ -56,7 +56,9 @@ typedef struct precond_ctx* precond_t;
 #define PRECOND_ECUDA      -3  /* a CUDA runtime/driver call failed */
 #define PRECOND_ENODEV     -4  /* host-only handle (created with cuda_device = -1): no GPU work possible */
 #define PRECOND_ENOTCONV   -5  /* per root: residual above tolerance after the iteration cap; output written */
-#define PRECOND_ENONFINITE -6  /* per root: NaN/Inf in the input or the Gram; output not written */
+#define PRECOND_ENONFINITE -6  /* per root: NaN/Inf in the input or the Gram, or a Gram / input whose
+                                  trace is not positive (its unit-trace rescaling is undefined, e.g.
+                                  an all-zero gradient on zero state); output not written */
 
 /* gradient storage types */
 #define PRECOND_F32   0

@@ -201,3 +201,45 @@ def test_graph_replay_matches_direct_launches(engine):
         for x, y in zip(a, b):
             assert torch.equal(x, y)
     assert s0[0] == s1[0] and s0[2] == s1[2]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("engine", [1, 2])
+def test_tiny_and_degenerate_shapes(engine):
+    """Sides of 1, 2, 3 and 17 (single-element Grams, rank-1 Grams, tiles that
+    are almost all padding), two EMA steps, both engines.
+
+    eps is 1e-4 here: the EMA state is fp32 by contract, and its rounding moves
+    the zero eigenvalues of a rank-1 d = 3 Gram by about 2^-24 of its trace.
+    Against eps = 1e-6 that alone changes (lambda + eps)^(-1/4) by about 1.5 %
+    in the directions where X is largest, whatever computes the root.  With
+    large d the perturbation spreads over many directions and the workloads
+    meet the bar at eps = 1e-6."""
+    shapes = [(1, 5), (3, 1), (2, 2), (17, 33)]
+    steps = []
+    for s in range(2):
+        rng = [synth.rng_for(11, s, i) for i in range(len(shapes))]
+        steps.append([synth.gradient(m, n, -0.5, rng[i], synth.F32) for i, (m, n) in enumerate(shapes)])
+    worst, (it, res, status, _) = run_steps(shapes, steps, synth.F32, 0.9, 1e-4, -0.25, engine=engine)
+    assert all(s == 0 for s in status), status
+    assert max(worst.values()) <= TOL, worst
+
+
+@pytest.mark.gpu
+def test_zero_gradient_from_zero_state_is_flagged():
+    """An all-zero gradient on zero state leaves Grams of trace 0, whose unit-trace
+    rescaling is undefined: both roots report ENONFINITE, the output is not
+    written, and the state holds the (zero) EMA."""
+    import torch
+    import shampoo_roots_gb300 as sr
+    pc = sr.Preconditioner(0)
+    g = torch.zeros(48, 24, device="cuda")
+    L = torch.zeros(48, 48, device="cuda")
+    R = torch.zeros(24, 24, device="cuda")
+    out = torch.full((48, 24), 3.0, device="cuda")
+    sr.precond_step(pc.h, [g], [L], [R], 0.9, 1e-6, -0.25, out=[out])
+    _, _, status, _ = sr.precond_get_stats(pc.h, 2)
+    pc.close()
+    assert status == [sr.ENONFINITE, sr.ENONFINITE]
+    assert torch.all(out == 3.0)
+    assert torch.all(L == 0) and torch.all(R == 0)
