@@ -75,8 +75,9 @@ typedef struct precond_ctx* precond_t;
 #define PRECOND_OPT_TIMING         7  /* 1 = record per-stage CUDA events (read by precond_get_timing) */
 #define PRECOND_OPT_USE_GRAPH      8  /* 1 = capture each distinct plan (shapes, options, workspace) once as a
                                          CUDA graph on a handle-owned stream and replay it, ordered after
-                                         and before the caller's stream by events (default 1); 0 = launch
-                                         every kernel on the caller's stream */
+                                         and before the caller's stream by events; the 4 most recently
+                                         used plans stay captured (default 1); 0 = launch every kernel on
+                                         the caller's stream */
 #define PRECOND_OPT_CLASSICAL      9  /* 1 = classical Newton step (p+1)/p I - M/p at every iteration;
                                          0 = per-step minimax step polynomial (default) */
 #define PRECOND_OPT_FOLD          10  /* minimax step: the interval's top may not fall below this

@@ -18,6 +18,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <list>
 #include <map>
 #include <mutex>
 #include <sstream>
@@ -126,11 +127,14 @@ struct precond_ctx {
   bool tc_attr_set = false;
   int num_sms = 148;
   // CUDA graph of the last plan (replayed on an internal stream joined to the caller's by events)
-  std::string graph_key;
-  cudaGraphExec_t graph_exec = nullptr;
-  void* graph_ws = nullptr;
-  int64_t graph_kernels = 0, graph_ns_launches = 0;
-  size_t graph_gemm_ev = 0;
+  struct Graph {                       // one captured plan
+    std::string key;
+    cudaGraphExec_t exec = nullptr;
+    void* ws = nullptr;                // the workspace its kernels point into
+    int64_t kernels = 0, ns_launches = 0;
+    size_t gemm_ev = 0;
+  };
+  std::list<Graph> graphs;             // most recently used first, at most kMaxGraphs
   cudaStream_t gstream = nullptr;
   cudaEvent_t gev_in = nullptr, gev_out = nullptr;
   bool branches = true;                // false: the iteration stage stays on the call's stream
@@ -1180,10 +1184,11 @@ std::string plan_key(const precond_ctx* h, const Plan& P, float beta, float eps)
 }
 
 void drop_graph(precond_ctx* h) {
-  if (h->graph_exec) cudaGraphExecDestroy(h->graph_exec);
-  h->graph_exec = nullptr;
-  h->graph_key.clear();
+  for (auto& g : h->graphs) cudaGraphExecDestroy(g.exec);
+  h->graphs.clear();
 }
+
+constexpr size_t kMaxGraphs = 4;     // plans a handle keeps captured (callers with a few parameter groups)
 
 // Run `fn(stream)` for plan P: directly on the caller's stream, or (graphs on)
 // as a replay of a graph captured once per plan on the handle's own stream,
@@ -1204,8 +1209,11 @@ int run_planned(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream
   CK(cudaStreamWaitEvent(h->gstream, h->gev_in, 0));
   if ((rc = upload_meta(h, P, h->gstream))) return rc;
   const std::string key = plan_key(h, P, beta, eps);
-  if (!h->graph_exec || key != h->graph_key || h->graph_ws != h->ws) {
-    drop_graph(h);
+  auto it = h->graphs.begin();
+  while (it != h->graphs.end() && !(it->key == key && it->ws == h->ws)) ++it;
+  if (it != h->graphs.end()) {
+    h->graphs.splice(h->graphs.begin(), h->graphs, it);      // most recently used first
+  } else {
     const int64_t l0 = h->launches;
     CK(cudaStreamBeginCapture(h->gstream, cudaStreamCaptureModeThreadLocal));
     h->capturing = true;
@@ -1219,23 +1227,27 @@ int run_planned(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream
       h->launches = l0;
       return rc ? rc : PRECOND_ECUDA;
     }
-    const cudaError_t ei = cudaGraphInstantiate(&h->graph_exec, g, 0);
+    precond_ctx::Graph ge;
+    const cudaError_t ei = cudaGraphInstantiate(&ge.exec, g, 0);
     cudaGraphDestroy(g);
-    if (ei != cudaSuccess) {
-      h->graph_exec = nullptr;
-      return PRECOND_ECUDA;
-    }
-    h->graph_key = key;
-    h->graph_ws = h->ws;
-    h->graph_kernels = h->launches - l0;
+    if (ei != cudaSuccess) return PRECOND_ECUDA;
+    ge.key = key;
+    ge.ws = h->ws;
+    ge.kernels = h->launches - l0;
     h->launches = l0;
-    h->graph_ns_launches = h->ns_launches;
-    h->graph_gemm_ev = h->gemm_ev_used;
+    ge.ns_launches = h->ns_launches;
+    ge.gemm_ev = h->gemm_ev_used;
+    h->graphs.push_front(ge);
+    while (h->graphs.size() > kMaxGraphs) {
+      cudaGraphExecDestroy(h->graphs.back().exec);
+      h->graphs.pop_back();
+    }
   }
-  CK(cudaGraphLaunch(h->graph_exec, h->gstream));
-  h->launches += h->graph_kernels;
-  h->ns_launches = h->graph_ns_launches;
-  h->gemm_ev_used = h->graph_gemm_ev;
+  const precond_ctx::Graph& gr = h->graphs.front();
+  CK(cudaGraphLaunch(gr.exec, h->gstream));
+  h->launches += gr.kernels;
+  h->ns_launches = gr.ns_launches;
+  h->gemm_ev_used = gr.gemm_ev;
   CK(cudaEventRecord(h->gev_out, h->gstream));
   CK(cudaStreamWaitEvent(st, h->gev_out, 0));
   return PRECOND_OK;

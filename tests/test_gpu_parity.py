@@ -168,7 +168,10 @@ def test_graph_replay_matches_direct_launches(engine):
     import torch
     import shampoo_roots_gb300 as sr
     rng = np.random.default_rng(11)
-    plans = [[(200, 72), (64, 136)], [(96, 40)], [(200, 72), (64, 136)], [(200, 72), (64, 136)]]
+    # the first plan comes back while cached, and again after five other plans
+    # have evicted it (the handle keeps four)
+    plans = [[(200, 72), (64, 136)], [(96, 40)], [(200, 72), (64, 136)], [(200, 72), (64, 136)],
+             [(40, 24)], [(48, 24)], [(56, 24)], [(64, 24)], [(72, 24)], [(200, 72), (64, 136)]]
     results = {}
     # (graph, branches): direct launches on one stream, graph replay with the iteration
     # stage on forked streams
