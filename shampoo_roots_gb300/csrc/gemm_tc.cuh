@@ -173,19 +173,45 @@ struct TcMaps {
 
 // Tile `tl` of a batch entry -> (row block, column block); symmetric products
 // enumerate the upper triangle row by row.
-__device__ __forceinline__ void tile_coords(int tl, int tiles_n, int sym, int& ti, int& tj) {
+// Tile order within one batch entry: groups of TC_GROUP tile-rows, and inside a
+// group column by column (rows fastest), so that the tiles in flight at once
+// (one per SM) share a few row panels and column panels that stay in L2.
+// Symmetric products enumerate the upper triangle (ti <= tj) only; the group's
+// diagonal block comes first (column c holds c + 1 of its rows), then full
+// columns of the group's rows.
+constexpr int TC_GROUP = 8;
+
+__host__ __device__ __forceinline__ void tile_coords(int tl, int tiles_m, int tiles_n, int sym, int& ti, int& tj) {
   if (!sym) {
-    ti = tl / tiles_n;
-    tj = tl % tiles_n;
+    const int per_group = TC_GROUP * tiles_n;
+    const int g = tl / per_group, first = g * TC_GROUP;
+    const int gm = min(tiles_m - first, TC_GROUP);
+    const int loc = tl - g * per_group;
+    ti = first + loc % gm;
+    tj = loc / gm;
     return;
   }
-  int r = 0;
-  while (tl >= tiles_n - r) {
-    tl -= tiles_n - r;
-    ++r;
+  int first = 0;
+  for (;;) {                                   // find the group holding tl
+    const int gm = min(tiles_n - first, TC_GROUP);
+    const int diag = gm * (gm + 1) / 2;
+    const int count = diag + (tiles_n - first - gm) * gm;
+    if (tl < count) {
+      if (tl < diag) {
+        int c = 0;
+        while ((c + 1) * (c + 2) / 2 <= tl) ++c;
+        tj = first + c;
+        ti = first + (tl - c * (c + 1) / 2);
+      } else {
+        const int loc = tl - diag;
+        tj = first + gm + loc / gm;
+        ti = first + loc % gm;
+      }
+      return;
+    }
+    tl -= count;
+    first += gm;
   }
-  ti = r;
-  tj = r + tl;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -255,7 +281,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
         const int b = t / tiles_per_entry, tl = t % tiles_per_entry;
         if (epi_skip(e, b)) continue;
         int ti, tj;
-        tile_coords(tl, tiles_n, g.sym, ti, tj);
+        tile_coords(tl, tiles_m, tiles_n, g.sym, ti, tj);
         const int tile_m = ti * TC_BM, tile_n = tj * TC_BN;
         const int za = g.a_index ? g.a_index[b] : b;
         const int zb = g.b_index ? g.b_index[b] : b;
@@ -321,7 +347,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       const int b = t / tiles_per_entry, tl = t % tiles_per_entry;
       if (epi_skip(e, b)) continue;
       int ti, tj;
-      tile_coords(tl, tiles_n, g.sym, ti, tj);
+      tile_coords(tl, tiles_m, tiles_n, g.sym, ti, tj);
       const int tile_m = ti * TC_BM, tile_n = tj * TC_BN;
       const bool mirror = g.sym && ti != tj;
       const int za = g.a_index ? g.a_index[b] : b;
