@@ -457,50 +457,6 @@ __global__ void f32_to_plane_kernel(const float* src, Plane p, int rows, int col
   }
 }
 
-// After the product M_{k+1} (tcgen05 engine): M <- (M + M^T) / 2 in place.  M
-// is symmetric in exact arithmetic, and the iteration amplifies any
-// antisymmetric rounding by up to ((p+1)/p)^p per step while M is far from I,
-// so it is projected back every step; also writes the row maxima for slicing.
-// Each block handles a pair of mirrored 32 x 32 tiles (bx <= by).
-struct SymArgs {
-  Plane M;          // fp32 form (f32, rowmax)
-  const int* root_of;
-  const RootStat* stats;
-  int d;
-};
-
-__global__ void __launch_bounds__(256) sym_m_kernel(SymArgs a) {
-  const int bx = blockIdx.x, by = blockIdx.y, b = blockIdx.z;
-  if (bx > by) return;
-  if (a.stats[a.root_of[b]].done) return;
-  __shared__ float ta[32][33], tb[32][33];
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  float* M = a.M.f32 + (long long)b * a.M.bstride;
-  const int ld = a.M.ld;
-  const int ra = by * 32, ca = bx * 32;      // tile A rows ra.., cols ca..; tile B = mirrored
-  for (int q = ty; q < 32; q += 8) {
-    const int r = ra + q, c = ca + tx;
-    ta[q][tx] = (r < a.d && c < a.d) ? M[(long long)r * ld + c] : 0.f;
-    const int r2 = ca + q, c2 = ra + tx;
-    tb[q][tx] = (r2 < a.d && c2 < a.d) ? M[(long long)r2 * ld + c2] : 0.f;
-  }
-  __syncthreads();
-  for (int half = 0; half < 2; ++half) {
-    if (half == 1 && bx == by) break;
-    const int rbase = half == 0 ? ra : ca, cbase = half == 0 ? ca : ra;
-    for (int q = ty; q < 32; q += 8) {
-      const int r = rbase + q, c = cbase + tx;
-      float mx = 0.f;
-      if (r < a.d && c < a.d) {
-        const float m = half == 0 ? 0.5f * (ta[q][tx] + tb[tx][q]) : 0.5f * (tb[q][tx] + ta[tx][q]);
-        M[(long long)r * ld + c] = m;
-        mx = fabsf(m);
-      }
-      mx = warp_max(mx);
-      if (tx == 0 && r < a.d) atomic_max_nonneg(&a.M.rowmax[(long long)b * a.d + r], mx);
-    }
-  }
-}
 
 // Engine plane -> caller fp32 (debug / test read-back of a root).
 template <int E>
