@@ -197,8 +197,9 @@ int precond_gemm_selftest(precond_t h, int engine, int M, int N, int K, const fl
 /*
  * Diagnostic read-back (no counterpart in the method) of a work matrix of
  * root `r` of the last call into a d x d fp32 device buffer:
- * which = 0/1 X buffers, 2/3 M buffers, 4 D (the T^2 - tau^2 I term), 5 F
- * (the T^4 - tau^4 I term, p = 4), 8 the final root (step calls).  Iteration k reads buffers k & 1 and writes
+ * which = 0/1 X buffers, 2/3 M buffers, 4 D (the T^2 - a^2 I term), 5 F
+ * (the T^4 - a^4 I term, p = 4; with quadratic steps it holds E = T - a I
+ * between E's product and F's), 8 the final root (step calls).  Iteration k reads buffers k & 1 and writes
  * (k + 1) & 1.  Enqueued on `stream`.
  */
 int precond_debug_plane(precond_t h, int r, int which, float* dst, void* stream);
@@ -215,7 +216,9 @@ int precond_debug_plane(precond_t h, int r, int which, float* dst, void* stream)
  *
  * All scratch lives in one fixed file-scope device array of 4 MiB that every
  * GPU which loads this library holds until the process exits; no cudaMalloc,
- * cudaFree or other allocating routine is called.  d above
+ * cudaFree or other device-memory allocating routine is called, and no
+ * stream, event or graph is created (the host side plans in small heap
+ * buffers, as any C++ code does).  d above
  * PRECOND_NOALLOC_MAX_D is rejected with PRECOND_EINVAL (and a message on
  * stderr).  The first call on each device looks up the array's device address
  * (with that device current); make that first call before any stream capture.
