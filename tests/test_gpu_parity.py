@@ -246,3 +246,40 @@ def test_zero_gradient_from_zero_state_is_flagged():
     assert status == [sr.ENONFINITE, sr.ENONFINITE]
     assert torch.all(out == 3.0)
     assert torch.all(L == 0) and torch.all(R == 0)
+
+
+@pytest.mark.gpu
+def test_two_handles_on_two_streams_match_their_solo_runs():
+    """Two handles used at the same time on two streams (one per thread of a
+    training job, say) share nothing: each gives bit-identical results to the
+    same calls made alone."""
+    import torch
+    import shampoo_roots_gb300 as sr
+    shapes = [[(160, 96), (96, 160)], [(256, 64)]]
+    rngs = [synth.rng_for(13, 0, i) for i in range(3)]
+    grads = [[torch.from_numpy(synth.gradient(m, n, -0.7, rngs[j + 2 * k], synth.F32)).cuda()
+              for j, (m, n) in enumerate(sh)] for k, sh in enumerate(shapes)]
+
+    def run(concurrent):
+        hs = [sr.Preconditioner(0) for _ in shapes]
+        streams = [torch.cuda.Stream() for _ in shapes]
+        state = [([torch.zeros((m, m), device="cuda") for m, _ in sh],
+                  [torch.zeros((n, n), device="cuda") for _, n in sh]) for sh in shapes]
+        outs = [[torch.empty((m, n), device="cuda") for m, n in sh] for sh in shapes]
+        for step in range(3):
+            for k in range(len(shapes)):
+                with torch.cuda.stream(streams[k]):
+                    sr.precond_step(hs[k].h, grads[k], state[k][0], state[k][1], 0.9, 1e-6, -0.25, out=outs[k],
+                                    stream=streams[k])
+                if not concurrent:
+                    torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        res = [[o.cpu() for o in ok] for ok in outs]
+        for h in hs:
+            h.close()
+        return res
+
+    solo, both = run(False), run(True)
+    for a, b in zip(solo, both):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
