@@ -30,7 +30,8 @@
 namespace precond {
 
 constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 32;
-constexpr int TC_THREADS = 192;
+constexpr int EPI_WARPS = 8;                       // two per tensor-memory lane quadrant
+constexpr int TC_THREADS = 64 + 32 * EPI_WARPS;    // producer warp, MMA warp, epilogue warps
 constexpr int DIGIT_BITS = 7;
 constexpr unsigned long long TC_WAIT_CYCLES = 4000000000ull;   // ~2 s at 2 GHz
 
@@ -57,7 +58,8 @@ struct TcSmem {
   static constexpr int STG_LD = TC_BN / 2 + 1;                  // staging: half a tile's columns, row stride
                                                                 // (floats) bank-conflict free
   static constexpr int STAGING_BYTES = TC_BM * STG_LD * 4;
-  static constexpr int TMEM_COLS = 512;                        // 3 x 128 used
+  static constexpr int TMEM_COLS = 512;                        // 3 x 128 accumulators + 128 parking columns
+  static constexpr int PARK_COL = 384;                         // drained second half of a tile waits here
   static constexpr int BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 1024 /*barriers, scales*/;
 };
 
@@ -150,6 +152,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// Store 32 consecutive fp32 columns of this warp's 32 lanes into tensor memory.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])), "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 
 // Digit-pair schedule (0-based digit indices), ordered by level s + t; the
 // first 6 pairs are the S = 3 schedule.  Accumulator: level 0 -> 0, level 1 -> 1,
@@ -217,7 +227,7 @@ __host__ __device__ __forceinline__ void tile_coords(int tl, int tiles_m, int ti
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }   // the 8 epilogue warps
 
 // Persistent: CTA c takes tiles c, c + gridDim.x, ...; tile t = (entry, row block,
 // column block) with the column block fastest.  The producer and the MMA
@@ -244,7 +254,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
   const uint32_t tmem_empty_bar = accum_bar + 8u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + 8 * (2 * SM::STAGES + 2));
   float* colscale = reinterpret_cast<float*>(tail + 512);      // 128 floats
-  __shared__ double red[4];
+  __shared__ double red[EPI_WARPS];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -337,10 +347,14 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       }
     }
   } else {
-    // ------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------ epilogue (warps 2..9)
+    // Warps w and w + 4 share a tensor-memory lane quadrant: the first drains the
+    // tile's columns 0..63 (to the staging tile), the second columns 64..127 (held
+    // in registers until the second half); both then split the element-wise work.
     const int q = warp & 3;                 // TMEM lane quadrant of this warp (rows q*32 ..)
-    const int ew = warp - 2;                // epilogue warp index 0..3
-    const int et = threadIdx.x - 64;        // epilogue thread index 0..127
+    const int ew = warp - 2;                // epilogue warp index 0..7
+    const int own = ew >> 2;                // column half this warp drains
+    const int et = threadIdx.x - 64;        // epilogue thread index 0..255
     const double c0 = (double)e.inv_scale * ldexp(1.0, -2 * DIGIT_BITS);
     uint32_t it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -353,7 +367,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       const int za = g.a_index ? g.a_index[b] : b;
       const int zb = g.b_index ? g.b_index[b] : b;
       // column scales of this tile
-      {
+      if (et < TC_BN) {
         const long long gc = tile_n + et;
         colscale[et] = (gc < g.N) ? (g.b_rowscale ? g.b_rowscale[(long long)zb * g.b_rs_stride + gc] : g.b_scale) : 0.f;
       }
@@ -368,26 +382,31 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
                                                     : (double)g.a_scale) : 0.0;
       const float rs = (float)(c0 * sa);
       float* srow = staging + row * SM::STG_LD;
-      float hold[TC_BN / 2];
+      const uint32_t tlane = tmem + ((uint32_t)(q * 32) << 16);
 #pragma unroll
-      for (int ch = 0; ch < TC_BN / 32; ++ch) {
-        float v0[32], v1[32], v2[32];
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ch * 32);
+      for (int cc = 0; cc < TC_BN / 64; ++cc) {
+        const int ch = own * (TC_BN / 64) + cc;
+        float v0[32], v1[32];
+        const uint32_t taddr = tlane + (uint32_t)(ch * 32);
         tmem_ld32(taddr, v0);
         tmem_ld32(taddr + 128, v1);
-        tmem_ld32(taddr + 256, v2);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float x = ((v0[j] + v1[j]) + v2[j]) * rs * colscale[ch * 32 + j];
-          if (ch < 2) srow[ch * 32 + j] = x;
-          else hold[(ch - 2) * 32 + j] = x;
+        for (int j = 0; j < 32; ++j) v0[j] += v1[j];
+        tmem_ld32(taddr + 256, v1);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v0[j] = (v0[j] + v1[j]) * rs * colscale[ch * 32 + j];
+        if (own == 0) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) srow[cc * 32 + j] = v0[j];
+        } else {
+          tmem_st32(tlane + SM::PARK_COL + cc * 32, v0);   // outside the accumulators
         }
       }
       tc_fence_before();
       epi_bar();
       if (et == 0) mbar_arrive(tmem_empty_bar);    // tensor memory may take the next tile
       // ---- element-wise epilogue, one half of the tile's columns at a time.  Every
-      // barrier below is reached by all 128 epilogue threads (work is guarded, not the barriers).
+      // barrier below is reached by all 256 epilogue threads (work is guarded, not the barriers).
       float part = 0.f;
       const bool track = (e.kind == EPI_AFF || e.kind == EPI_M) && e.C.rowmax;
       const bool need_in = (e.kind == EPI_AFF || e.kind == EPI_M || e.kind == EPI_GRAM);
@@ -400,14 +419,21 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
         const int hc = h * (TC_BN / 2);             // first tile column of this half
         if (h == 1) {
           epi_bar();                                // the first half's staging is read
+          if (own == 1) {
 #pragma unroll
-          for (int j = 0; j < TC_BN / 2; ++j) srow[j] = hold[j];
+            for (int cc = 0; cc < TC_BN / 64; ++cc) {
+              float v[32];
+              tmem_ld32(tlane + SM::PARK_COL + cc * 32, v);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) srow[cc * 32 + j] = v[j];
+            }
+          }
           epi_bar();
         }
         if (e.kind == EPI_VT) {
-          // transposed output: warp ew takes 16 of the half's columns, lanes run over rows
-          for (int cc = 0; cc < TC_BN / 8; ++cc) {
-            const int cl = ew * (TC_BN / 8) + cc;
+          // transposed output: warp ew takes 8 of the half's columns, lanes run over rows
+          for (int cc = 0; cc < TC_BN / 2 / EPI_WARPS; ++cc) {
+            const int cl = ew * (TC_BN / 2 / EPI_WARPS) + cc;
             const long long gc = tile_n + hc + cl;
             float mx = 0.f;
             if (ok && gc < g.N) {
@@ -432,11 +458,11 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
         // their latencies overlap instead of adding up row by row (the whole cost of a
         // product when the grid has only a few tiles).
 #pragma unroll 1
-        for (int r0 = 0; r0 < 32; r0 += EPI_RB) {
+        for (int r0 = 0; r0 < TC_BM / EPI_WARPS; r0 += EPI_RB) {
           float in[EPI_RB][2];
 #pragma unroll
           for (int u = 0; u < EPI_RB; ++u) {
-            const int r = ew * 32 + r0 + u;
+            const int r = ew * (TC_BM / EPI_WARPS) + r0 + u;
             const long long grr = tile_m + r;
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
@@ -453,7 +479,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
           }
 #pragma unroll
           for (int u = 0; u < EPI_RB; ++u) {
-            const int r = ew * 32 + r0 + u;
+            const int r = ew * (TC_BM / EPI_WARPS) + r0 + u;
             const long long grr = tile_m + r;
             float mx = 0.f;
             if (ok && grr < g.M) {
@@ -530,11 +556,11 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
           __syncwarp();
           epi_bar();
 #pragma unroll 1
-          for (int c0 = 0; c0 < TC_BN / 8; c0 += EPI_RB) {
+          for (int c0 = 0; c0 < TC_BN / 2 / EPI_WARPS; c0 += EPI_RB) {
             float st_in[EPI_RB][4];
 #pragma unroll
             for (int u = 0; u < EPI_RB; ++u) {
-              const long long gc = tile_n + hc + ew * (TC_BN / 8) + c0 + u;
+              const long long gc = tile_n + hc + ew * (TC_BN / 2 / EPI_WARPS) + c0 + u;
 #pragma unroll
               for (int r4 = 0; r4 < 4; ++r4) {
                 const long long grr = tile_m + r4 * 32 + lane;
@@ -543,7 +569,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
             }
 #pragma unroll
             for (int u = 0; u < EPI_RB; ++u) {
-              const int cl = ew * (TC_BN / 8) + c0 + u;     // tile column (in this half) = mirrored row
+              const int cl = ew * (TC_BN / 2 / EPI_WARPS) + c0 + u;   // tile column (in this half) = mirrored row
               const long long gc = tile_n + hc + cl;
               float mx = 0.f;
               if (ok && gc < g.N) {
@@ -575,7 +601,12 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
         if (lane == 0) red[ew] = pd;
       }
       epi_bar();                          // staging free; residual parts visible
-      if (e.kind == EPI_M && ew == 0) epi_m_finish(e, b, red[0] + red[1] + red[2] + red[3], g.M, tl);
+      if (e.kind == EPI_M && ew == 0) {
+        double sum = 0.0;
+#pragma unroll
+        for (int w = 0; w < EPI_WARPS; ++w) sum += red[w];     // fixed order: deterministic
+        epi_m_finish(e, b, sum, g.M, tl);
+      }
       ++it;
     }
   }
