@@ -57,10 +57,11 @@ def rank_step_seed(rank: int, step: int) -> int:
 # d = 1024 stack; profiles/gemm_tc_kernel_dram_stack24.md), per launch over a step's
 # launch mix: per class 34 computed products (7 iterations) and 15 launches whose
 # roots have all converged (no tiles, no traffic).  Valid only for the kernel
-# sources it was taken on: their SHA-1s.
+# sources it was taken on: their SHA-1s (the gemm_tc.cuh one after a comment-only
+# edit of its header).
 TRAFFIC_CAPTURES = {
     1: {"bytes_per_launch": 10.71e9, "algorithmic_bytes_per_launch": 7.04e9,
-        "sources": {"gemm_tc.cuh": "3facbf0bd6b37b0f140164b5a5b16aaf6074eb31",
+        "sources": {"gemm_tc.cuh": "38c0b49c103fc7d7dec1f31db160d9196aaabf8d",
                     "engine.cuh": "4ed3254d617f51583c8c6d6ebfef32cc43e157e2",
                     "common.cuh": "983868160199120ad308ddf0b9fbbdd1021863c0"}},
 }

@@ -18,10 +18,11 @@
 // Pipeline: TMA (3-D tensor maps {K, rows, batch}, 64-byte swizzle, K block
 // 32) into a 3-4 stage shared-memory ring; one elected thread issues
 // tcgen05.mma (kind::f16, bf16, M = 128, N = 128, K = 16) into three fp32
-// accumulators in tensor memory; four epilogue warps read them back with
-// tcgen05.ld.  Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM
-// owner and MMA issuer, warps 2..5 epilogue.  Every mbarrier wait is
-// bounded; on time-out the kernel records an error word and leaves the tile.
+// accumulators in tensor memory; eight epilogue warps (two per tensor-memory
+// lane quadrant) read them back with tcgen05.ld.  Warp roles (320 threads):
+// warp 0 TMA producer, warp 1 TMEM owner and MMA issuer, warps 2..9 epilogue.
+// Every mbarrier wait is bounded; on time-out the kernel records an error word
+// and leaves the tile.
 #pragma once
 
 #include <cuda.h>
