@@ -283,3 +283,18 @@ def test_two_handles_on_two_streams_match_their_solo_runs():
     for a, b in zip(solo, both):
         for x, y in zip(a, b):
             assert torch.equal(x, y)
+
+
+@pytest.mark.gpu
+def test_many_small_matrices_in_one_call():
+    """300 gradients of four small shapes in one call (large batch dimensions
+    in every grid, long pointer tables), two EMA steps, against the oracle on
+    every matrix."""
+    shapes = [(32, 16), (16, 48), (40, 40), (24, 8)] * 75
+    steps = []
+    for s in range(2):
+        steps.append([synth.gradient(m, n, -0.5, synth.rng_for(17, s, i), synth.F32)
+                      for i, (m, n) in enumerate(shapes)])
+    worst, (it, res, status, _) = run_steps(shapes, steps, synth.F32, 0.9, 1e-4, -0.25, check_roots=False)
+    assert all(s == 0 for s in status), status
+    assert worst["U"] <= TOL, worst
