@@ -149,22 +149,33 @@ __global__ void __launch_bounds__(256) slice_rows_kernel(SliceArgs a) {
     const long long o = (long long)b * a.dst.bstride + (long long)r * a.dst.ld;
     __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.dst.hi) + o;
     const int nv = (a.cols / 4) * 4;
-    for (int c = lane * 4; c < nv; c += 128) {          // 4 columns per lane: 16 B in, 8 B out per plane
-      const float4 v = *reinterpret_cast<const float4*>(src + c);
-      float d0[4], d1[4], d2[4], d3[4];
-      digits4(v.x, inv, d0);
-      digits4(v.y, inv, d1);
-      digits4(v.z, inv, d2);
-      digits4(v.w, inv, d3);
+    // 4 columns per lane (16 B in, 8 B out per plane), two such groups per
+    // iteration with both loads issued before any store, so that each lane keeps
+    // 32 B in flight
+    for (int c = lane * 4; c < nv; c += 256) {
+      float4 v[2];
+      const bool two = c + 128 < nv;
+      v[0] = *reinterpret_cast<const float4*>(src + c);
+      if (two) v[1] = *reinterpret_cast<const float4*>(src + c + 128);
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        if (s < a.dst.S) {
-          __nv_bfloat162 lo2 = __floats2bfloat162_rn(d0[s], d1[s]);
-          __nv_bfloat162 hi2 = __floats2bfloat162_rn(d2[s], d3[s]);
-          uint2 pk;
-          pk.x = *reinterpret_cast<uint32_t*>(&lo2);
-          pk.y = *reinterpret_cast<uint32_t*>(&hi2);
-          *reinterpret_cast<uint2*>(dst + s * a.dst.pstride + c) = pk;
+      for (int h = 0; h < 2; ++h) {
+        if (h == 1 && !two) break;
+        const int cc = c + h * 128;
+        float d0[4], d1[4], d2[4], d3[4];
+        digits4(v[h].x, inv, d0);
+        digits4(v[h].y, inv, d1);
+        digits4(v[h].z, inv, d2);
+        digits4(v[h].w, inv, d3);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          if (s < a.dst.S) {
+            __nv_bfloat162 lo2 = __floats2bfloat162_rn(d0[s], d1[s]);
+            __nv_bfloat162 hi2 = __floats2bfloat162_rn(d2[s], d3[s]);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+            pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+            *reinterpret_cast<uint2*>(dst + s * a.dst.pstride + cc) = pk;
+          }
         }
       }
     }
