@@ -340,34 +340,43 @@ __global__ void __launch_bounds__(256) root_init_kernel(RootArgs a) {
   const float s_ac = st->sac, s_eps = st->seps;
   const float al = (float)a.alpha0, be = (float)a.beta0;
   const float* A = a.src[b];
-  __shared__ float tt[32][33];
+  __shared__ float tt[2][32][33];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int T = (a.d + 31) / 32;
   for (int strip = blockIdx.x; strip < T; strip += gridDim.x) {
     const int r0 = strip * 32;
     float mx[4] = {0.f, 0.f, 0.f, 0.f}, xx[4] = {0.f, 0.f, 0.f, 0.f};   // rows r0 + ty + 8 j
-    for (int c0 = 0; c0 < a.d; c0 += 32) {
-      __syncthreads();                          // the previous tile's reads of tt are done
-      for (int q = ty; q < 32; q += 8) {        // mirrored tile (rows c0.., cols r0..), coalesced
-        const int r = c0 + q, col = r0 + tx;
-        tt[q][tx] = (r < a.d && col < a.d) ? A[(long long)r * a.d + col] : 0.f;
-      }
+    for (int c0 = 0; c0 < a.d; c0 += 64) {     // two 32-column tiles per pass, loads first
+      __syncthreads();                          // the previous pass's reads of tt are done
+      float av[2][4];
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int q = ty + 8 * j;
+          const int rm = c0 + 32 * t + q, cm = r0 + tx;             // mirrored tile (rows c0.., cols r0..)
+          tt[t][q][tx] = (rm < a.d && cm < a.d) ? A[(long long)rm * a.d + cm] : 0.f;
+          const int r = r0 + q, col = c0 + 32 * t + tx;             // this strip's own elements
+          av[t][j] = (r < a.d && col < a.d) ? A[(long long)r * a.d + col] : 0.f;
+        }
       __syncthreads();
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int q = ty + 8 * j;
-        const int r = r0 + q, col = c0 + tx;
-        if (r < a.d && col < a.d) {
-          const bool dgl = (r == col);
-          // M_0 = ((A + A^T)/2 / tr + eps I) / c, exactly symmetric
-          const float m0 = fmaf(A[(long long)r * a.d + col] + tt[tx][q], s_ac, dgl ? s_eps : 0.f);
-          const float x1 = (dgl ? al : 0.f) - be * m0;
-          plane_store<E>(a.M0, b, r, col, m0);
-          plane_store<E>(a.X1, b, r, col, x1);
-          mx[j] = fmaxf(mx[j], fabsf(m0));
-          xx[j] = fmaxf(xx[j], fabsf(x1));
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int q = ty + 8 * j;
+          const int r = r0 + q, col = c0 + 32 * t + tx;
+          if (r < a.d && col < a.d) {
+            const bool dgl = (r == col);
+            // M_0 = ((A + A^T)/2 / tr + eps I) / c, exactly symmetric
+            const float m0 = fmaf(av[t][j] + tt[t][tx][q], s_ac, dgl ? s_eps : 0.f);
+            const float x1 = (dgl ? al : 0.f) - be * m0;
+            plane_store<E>(a.M0, b, r, col, m0);
+            plane_store<E>(a.X1, b, r, col, x1);
+            mx[j] = fmaxf(mx[j], fabsf(m0));
+            xx[j] = fmaxf(xx[j], fabsf(x1));
+          }
         }
-      }
     }
     if (E == ENGINE_TC) {
 #pragma unroll
@@ -387,7 +396,7 @@ __global__ void __launch_bounds__(256) root_init_kernel(RootArgs a) {
 // (inv_root).  Blocks own 32-row strips, as in the start.
 template <int E>
 __global__ void __launch_bounds__(256) root_finish_kernel(RootArgs a) {
-  __shared__ float tile[32][33];
+  __shared__ float tile[2][32][33];
   const int b = blockIdx.z;
   const RootStat* st = &a.stats[a.root_of[b]];
   if (st->status == PRECOND_ENONFINITE || st->kfinal < 1) return;
@@ -398,25 +407,33 @@ __global__ void __launch_bounds__(256) root_finish_kernel(RootArgs a) {
   for (int strip = blockIdx.x; strip < T; strip += gridDim.x) {
     const int r0 = strip * 32;
     float mx[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int c0 = 0; c0 < a.d; c0 += 32) {
-      __syncthreads();                          // the previous tile's reads are done
-      // load the transposed tile (rows c0.., cols r0..)
-      for (int q = ty; q < 32; q += 8) {
-        const int r = c0 + q, col = r0 + tx;
-        tile[q][tx] = (r < a.d && col < a.d) ? (float)plane_load<E>(X, b, r, col) : 0.f;
-      }
+    for (int c0 = 0; c0 < a.d; c0 += 64) {     // two 32-column tiles per pass, loads first
+      __syncthreads();                          // the previous pass's reads are done
+      float xv[2][4];
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int q = ty + 8 * j;
+          const int rm = c0 + 32 * t + q, cm = r0 + tx;             // transposed tile (rows c0.., cols r0..)
+          tile[t][q][tx] = (rm < a.d && cm < a.d) ? (float)plane_load<E>(X, b, rm, cm) : 0.f;
+          const int r = r0 + q, col = c0 + 32 * t + tx;
+          xv[t][j] = (r < a.d && col < a.d) ? (float)plane_load<E>(X, b, r, col) : 0.f;
+        }
       __syncthreads();
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int q = ty + 8 * j;
-        const int r = r0 + q, col = c0 + tx;
-        if (r < a.d && col < a.d) {
-          const float v = 0.5f * ((float)plane_load<E>(X, b, r, col) + tile[tx][q]) * f;
-          if (a.dst) a.dst[b][(long long)r * a.d + col] = v;
-          else plane_store<E>(a.Xf, b, r, col, (double)v);
-          mx[j] = fmaxf(mx[j], fabsf(v));
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int q = ty + 8 * j;
+          const int r = r0 + q, col = c0 + 32 * t + tx;
+          if (r < a.d && col < a.d) {
+            const float v = 0.5f * (xv[t][j] + tile[t][tx][q]) * f;
+            if (a.dst) a.dst[b][(long long)r * a.d + col] = v;
+            else plane_store<E>(a.Xf, b, r, col, (double)v);
+            mx[j] = fmaxf(mx[j], fabsf(v));
+          }
         }
-      }
     }
     if (E == ENGINE_TC && !a.dst) {
 #pragma unroll
