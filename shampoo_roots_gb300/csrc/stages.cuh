@@ -463,7 +463,30 @@ __global__ void __launch_bounds__(256) shift_identity_kernel(ShiftArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int r = blockIdx.x * 8 + warp; r < a.d; r += gridDim.x * 8) {
     float mx = 0.f;
-    for (int c = lane; c < a.d; c += 32) {
+    int c0 = 0;
+    if (E == ENGINE_TC) {
+      // fp32 rows start 256 B aligned (ld is a multiple of 64): 16-byte vectors, two in flight
+      const float* src = a.src.f32 + (long long)b * a.src.bstride + (long long)r * a.src.ld;
+      float* dst = a.dst.f32 + (long long)b * a.dst.bstride + (long long)r * a.dst.ld;
+      const int nv = (a.d / 4) * 4;
+      for (int c = lane * 4; c < nv; c += 256) {
+        float4 v[2];
+        const bool two = c + 128 < nv;
+        v[0] = *reinterpret_cast<const float4*>(src + c);
+        if (two) v[1] = *reinterpret_cast<const float4*>(src + c + 128);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (h == 1 && !two) break;
+          const int cc = c + h * 128;
+          float4 w = v[h];
+          if (r >= cc && r < cc + 4) (&w.x)[r - cc] += a.alpha;
+          *reinterpret_cast<float4*>(dst + cc) = w;
+          mx = fmaxf(mx, fmaxf(fmaxf(fabsf(w.x), fabsf(w.y)), fmaxf(fabsf(w.z), fabsf(w.w))));
+        }
+      }
+      c0 = nv;
+    }
+    for (int c = c0 + lane; c < a.d; c += 32) {
       const float v = (float)plane_load<E>(a.src, b, r, c) + (r == c ? a.alpha : 0.f);
       plane_store<E>(a.dst, b, r, c, (double)v);
       mx = fmaxf(mx, fabsf(v));
