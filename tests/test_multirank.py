@@ -77,3 +77,24 @@ def test_rank_seeds_are_disjoint():
     import bench
     seeds = {bench.rank_step_seed(r, s) for r in range(8) for s in range(10)}
     assert len(seeds) == 80
+
+
+def test_reference_arm_json_line(capsys, monkeypatch):
+    """The reference arm (the float64 oracle) prints one JSON line with the
+    fields the benchmark contract names."""
+    import argparse
+    import json
+    import bench
+    monkeypatch.setenv("RANK", "0")
+    args = argparse.Namespace(workload=0, power=None, warmup=1, steps=2, gpus=1)
+    bench.run_reference(args)
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    assert d["value"] > 0 and d["unit"] == "preconditioner steps/s" and d["higher_is_better"] is True
+    assert d["steps"] == 2 and d["warmup"] == 1 and d["n_gpus"] == 1
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == "single-256x128"
