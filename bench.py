@@ -2,8 +2,10 @@
 
 A step = one call of the whole hot path (Gram EMAs, statistics and bound,
 coupled Newton-Schulz roots, two-sided apply) over one batch of synthetic
-gradients of the 24-layer d = 1024 transformer stack (bf16 gradients, fp32
-Grams, power -1/4): 144 weight matrices, 288 roots.
+gradients.  The default workload is the largest one that fits one GPU, the
+wide stack: 16 fp32 gradients of 6144 x 6144 and 16 of 6144 x 3072
+(s_i ~ i^-0.5), fp32 Grams, power -1/4: 32 weight matrices, 64 roots
+(48 of side 6144, 16 of side 3072).  `--workload N` selects the others.
 
 Prints ONE JSON line (rank 0).  `value` is whole-job throughput in
 preconditioner steps per second (1000 / ms_per_step per GPU, summed over
@@ -11,7 +13,8 @@ ranks); `tflops_algorithmic` is the step's algorithmic FLOPs (2mnk per logical
 GEMM, iterations actually executed) over its time; `e2e` is the throughput
 with the gradients copied from pinned host memory and the update copied back
 inside the timed region.  `--impl reference` times the float64 CPU oracle on
-a bounded sample of the same workload.
+whole preconditioner steps of the same workload (as many as fit a few
+minutes, at least one) and says how many it ran.
 """
 from __future__ import annotations
 
@@ -28,7 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "preconditioner step ms and TFLOP/s (% GB300 tensor peak) vs CPU oracle"
-WORKLOAD_INDEX = 1          # default: the 24-layer d=1024 stack, power -1/4
+WORKLOAD_INDEX = 4          # default: the wide stack (16 x 6144^2 + 16 x 6144x3072), power -1/4
 
 
 def max_over_ranks(x: float, dist, device) -> float:
@@ -54,7 +57,7 @@ def rank_step_seed(rank: int, step: int) -> int:
 
 # DRAM traffic of the dominant kernel from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum of one iteration's products of both root classes of the
-# d = 1024 stack; profiles/gemm_tc_kernel_dram_stack24.md), per launch over a step's
+# d = 1024 stack), per launch over a step's
 # launch mix: per class 34 computed products (7 iterations) and 15 launches whose
 # roots have all converged (no tiles, no traffic).  Valid only for the kernel
 # sources it was taken on: their SHA-1s (the gemm_tc.cuh one after a comment-only
@@ -205,33 +208,114 @@ def oracle_sample_spd(w, power, n=2):
     return dt / n * w.count, f"{n} of the {w.count} SPD {w.dims[0]}^2 matrices ({dt:.1f} s), extrapolated", os.cpu_count()
 
 
+# The arithmetic of the path: fp32 values, every product on bf16 tensor cores as
+# exact products of per-row-scaled bf16 digits (4 digits of 7 bits, the leading
+# product levels accumulated exactly), fp32 storage between products.
+DTYPE = "fp32 (bf16x4 exact digit products)"
+DTYPE_NOTE = ("fp32 matrices; products as exact bf16 digit products on tensor cores (4 digits of 7 bits, "
+              "leading levels accumulated exactly in fp32), about 2^-28 relative to the row scales")
+SM_COUNT = 152
+BF16_FLOPS_PER_CLK_SM = 8192.0     # dense bf16 tensor-core rate per SM and clock (2 x 4096 FMA)
+
+REFERENCE_BUDGET_S = 300.0     # reference arm: time budget for whole oracle steps
+
+L2_NOTE = ("inputs larger than L2 (129 MB): the state and input matrices of every workload but the "
+           "single 256x128 one, which flushes L2 with a 256 MB write between timed steps")
+
+
+def synth_workload(index):
+    from workloads import synth
+    return synth.workload(index)
+
+
+def parse_opts(args):
+    return {k: float(v) for k, v in (o.split("=", 1) for o in args.opt)}
+
+
+def workload_config(w, power, opts):
+    """The `config` object of both arms' JSON lines (identical for the same run)."""
+    nroots = 2 * w.count if w.kind == "step" else w.count
+    return {"workload": w.name, "matrices": w.count, "roots": nroots, "grad_dtype": w.dtype,
+            "power": power, "beta": w.beta if w.kind == "step" else None, "eps": w.eps,
+            "options": opts, "l2": L2_NOTE}
+
+
+def _reference_inputs(w):
+    """Inputs of one step of workload `w` for the reference arm, drawn on the host
+    with the torch backend of the same recipe (fp32 QR).  Step workloads draw one
+    gradient per shape class and pass it for every matrix of that class: the
+    oracle's work does not depend on the values, and the float64 draws of the
+    largest stacks would otherwise take minutes.  Returns float64 arrays."""
+    import numpy as np
+    from workloads import synth
+    if w.kind == "step":
+        first = {}
+        for i, s in enumerate(w.shapes):
+            first.setdefault(s, i)
+        drawn = dict(zip(first.keys(), synth.torch_gradients_for_step(w, 0, "cpu", matrices=list(first.values()))))
+        return [drawn[s].float().numpy().astype(np.float64) for s in w.shapes]
+    return [a.numpy().astype(np.float64) for a in synth.torch_spd_inputs(w, "cpu")]
+
+
 def run_reference(args):
-    """Reference arm: the float64 CPU oracle on a bounded sample per step."""
+    """Reference arm: the float64 CPU oracle, as it stands, on whole steps of the
+    workload.  Small workloads run the requested warm-up and timed steps; when one
+    oracle step takes long (the largest stacks need minutes), the arm runs as many
+    whole steps as fit REFERENCE_BUDGET_S (at least one, no warm-up: the oracle
+    has nothing to warm up) and reports the counts it actually ran."""
+    from oracle import roots as oracle
     from workloads import synth
     w = synth.workload(args.workload)
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    secs = []
-    desc = ""
-    cores = os.cpu_count()
     power = args.power if args.power is not None else w.powers[0]
-    for _ in range(args.warmup + args.steps):
+    inputs = _reference_inputs(w)
+    state = [None]
+
+    def one_step():
+        t0 = time.perf_counter()
         if w.kind == "step":
-            t, desc, cores = oracle_sample(w, seconds_budget=8.0)
+            if state[0] is None:
+                state[0] = oracle.OracleState(list(w.shapes))
+            oracle.precond_step(state[0], inputs, w.beta, w.eps, power)
         else:
-            t, desc, cores = oracle_sample_spd(w, power, n=1)
-        secs.append(t)
-    timed = secs[args.warmup:]
+            for a in inputs:
+                oracle.inv_root(a, w.eps, power)
+        return time.perf_counter() - t0
+
+    first = one_step()                 # a whole step; decides how many more fit
+    warm_run, timed = 0, []
+    if first * (args.warmup + args.steps) <= REFERENCE_BUDGET_S:
+        warm_run = 1
+        for _ in range(args.warmup - 1):
+            one_step()
+            warm_run += 1
+        for _ in range(args.steps):
+            timed.append(one_step())
+    else:
+        timed.append(first)
+        used = first
+        while len(timed) < args.steps and used + first <= REFERENCE_BUDGET_S:
+            timed.append(one_step())
+            used += timed[-1]
     per_step = statistics.median(timed)
     value = 1.0 / per_step
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "preconditioner steps/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+    sample = (f"{len(timed)} whole oracle step(s) of all {w.count} matrices "
+              f"(EMA state carried from step to step; the same inputs every step"
+              f"{', one drawn gradient per shape class' if w.kind == 'step' else ''}), "
+              f"{warm_run} warm-up step(s); timed {sum(timed):.1f} s")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "preconditioner steps/s",
+            "n_gpus": args.gpus, "steps": len(timed), "warmup": warm_run,
+            "requested": {"steps": args.steps, "warmup": args.warmup},
+            "ms_per_step": per_step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "matrices": w.count, "grad_dtype": w.dtype, "power": power},
-            "cpu_baseline": {"value": value, "unit": "preconditioner steps/s", "cores": cores, "kind": "oracle",
-                             "sample": desc},
-            "e2e": {"value": value, "unit": "preconditioner steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "extrapolated": False,
+            "config": workload_config(w, power, parse_opts(args)),
+            "cpu_baseline": {"value": value, "unit": "preconditioner steps/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "preconditioner steps/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
@@ -300,7 +384,7 @@ def main():
 
     w = synth.workload(args.workload)
     power = args.power if args.power is not None else w.powers[0]
-    opts = {k: float(v) for k, v in (o.split("=", 1) for o in args.opt)}
+    opts = parse_opts(args)
     pc = sr.Preconditioner(local, timing=1, **opts)
     if w.kind == "step":
         shapes = list(w.shapes)
@@ -432,6 +516,14 @@ def main():
                 "peak_kind": f"bf16 dense, sustained ({peaks['source']})",
                 "issued_tflops": issued, "issued_frac": (issued / peak) if issued else None,
                 "avg_launch_ms": gemm_ms / gemm_n if gemm_n else None}
+    clk_summary = clk.summary()
+    if clk_summary.get("sm_mhz") and achieved:
+        # secondary view: against the tensor cores' nominal dense bf16 rate at the
+        # sampled median SM clock (the measured peak above is a torch.matmul rate)
+        nominal = SM_COUNT * BF16_FLOPS_PER_CLK_SM * clk_summary["sm_mhz"] * 1e6 / 1e12
+        roofline["nominal_at_clock"] = {"peak": nominal, "sm_mhz": clk_summary["sm_mhz"],
+                                        "frac_algorithmic": achieved / nominal,
+                                        "frac_issued": (issued / nominal) if issued else None}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -445,20 +537,17 @@ def main():
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "preconditioner steps/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": w.name, "matrices": w.count, "roots": nroots,
-                           "grad_dtype": w.dtype, "power": power, "beta": w.beta, "eps": w.eps,
-                           "options": opts,
-                           "mean_iterations": statistics.mean(iters_seen) if iters_seen else None,
-                           "l2": "inputs larger than L2 (129 MB): the state / input matrices of every workload but the single 256x128 one",
-                           "numerics": "bf16 tensor-core digit products, exact fp32 accumulation of leading levels"},
+                "vs_baseline": None, "dtype": DTYPE, "data": "synthetic",
+                "config": workload_config(w, power, opts),
+                "mean_iterations": statistics.mean(iters_seen) if iters_seen else None,
+                "numerics": DTYPE_NOTE,
                 "tflops_algorithmic": tflops,
                 "pct_tensor_peak": tflops / peaks["bf16_tflops"],
                 "stages_ms_per_step": {k: v / args.steps for k, v in zip(
                     ("prep_gram", "bound_start", "iterations", "finish_apply"), stage_ms)},
                 "iteration_gemm_ms_per_step": gemm_ms / args.steps,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
-                "clocks": clk.summary()}
+                "clocks": clk_summary}
         print(json.dumps(line), flush=True)
     pc.close()
     if dist is not None:

@@ -65,7 +65,7 @@ typedef struct precond_ctx* precond_t;
 #define PRECOND_BF16  1
 
 /* option keys for precond_set_option */
-#define PRECOND_OPT_TOL            1  /* stop when ||M - I||_F <= tol*sqrt(d); default 1e-5 */
+#define PRECOND_OPT_TOL            1  /* stop when ||M - I||_F <= tol*sqrt(d); default 1e-4 */
 #define PRECOND_OPT_MAX_ITER       2  /* iteration cap; 0 = derived from the scalar model (default) */
 #define PRECOND_OPT_MIN_ITER       3  /* stagnation test only after this many iterations; default 4 */
 #define PRECOND_OPT_ENGINE         4  /* 0 auto (default), 1 fp64 SIMT engine, 2 tcgen05 engine */
@@ -225,8 +225,11 @@ int precond_debug_plane(precond_t h, int r, int which, float* dst, void* stream)
  * Every call shares the array and overwrites it, so calls whose GPU work
  * overlaps (other streams, other host threads, unsynchronised loops on
  * different streams) race: order them on one stream.  `status` (host, may be
- * NULL): when given, the call synchronises `stream` and stores the root's
- * PRECOND_OK / ENOTCONV / ENONFINITE.
+ * NULL): when given, the call synchronises `stream`, stores the root's
+ * PRECOND_OK / ENOTCONV / ENONFINITE there and returns PRECOND_ECUDA if the
+ * device recorded an error.  When NULL, the call does not synchronise and
+ * reports nothing found on the device: a caller who needs to know whether the
+ * root converged or the input was finite must pass `status`.
  */
 #define PRECOND_NOALLOC_MAX_D 256
 int precond_inv_root_noalloc(const float* A, int64_t d, float eps, float power, float* X, void* stream,

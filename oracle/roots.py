@@ -32,10 +32,12 @@ Also here, each following its passage:
   page's (a, b) = (3/2, -1/2) step at p = 2).  A debug reference for the
   iteration, not the parity target.
 * ``scalar_iterations``: the scalar model of that iteration on one eigenvalue,
-  used to bound the iteration count ("roughly 21 iterations", section 2.2).
+  used to bound the iteration count (section 2.2 puts the classical
+  iteration at about 21 steps).
 
 Readings of points the pages leave open:
-* "rescales the Grams" = divide by the trace (unit trace).
+* the rescaling of the Grams before the root (Background) = divide by the
+  trace (unit trace).
 * the regulariser is added to the eigenvalues of the rescaled Gram, with no
   clamp of tiny negative eigenvalues; lam + eps <= 0 raises.
 * the EMA state is stored raw; rescaling applies to a copy at each update.
@@ -63,7 +65,8 @@ def gram_ema(L: np.ndarray, R: np.ndarray, G: np.ndarray, beta: float) -> Tuple[
 # step 2: rescale
 # --------------------------------------------------------------------------
 def trace_normalise(A: np.ndarray) -> np.ndarray:
-    """A / tr(A): the Gram rescaled to unit trace (reading of "rescales the Grams")."""
+    """A / tr(A): the Gram rescaled to unit trace (the reading taken of the
+    rescaling step of "Sharding EMA-Gram eigensolves", Background)."""
     A = np.asarray(A, dtype=np.float64)
     t = np.trace(A)
     if not np.isfinite(t) or t <= 0.0:
@@ -91,7 +94,8 @@ def inv_root_eigh(A_hat: np.ndarray, eps: float, power: float) -> np.ndarray:
 # step 4: two-sided apply
 # --------------------------------------------------------------------------
 def precondition(X_L: np.ndarray, G: np.ndarray, X_R: np.ndarray) -> np.ndarray:
-    """U = X_L G X_R (the powers "shape the direction of the weight update")."""
+    """U = X_L G X_R: both powers applied to the gradient to form the update
+    ("Sharding EMA-Gram eigensolves", Background)."""
     return X_L @ np.asarray(G, dtype=np.float64) @ X_R
 
 

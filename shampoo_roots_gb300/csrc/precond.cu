@@ -96,7 +96,7 @@ struct Plan {
 
 struct precond_ctx {
   int device = -1;
-  double tol = 1e-5;
+  double tol = 1e-4;
   int max_iter = 0, min_iter = 4, engine = 0, small_dim = 0, timing = 0, use_graph = 1;
   int classical = 0;                   // 1: classical Newton step polynomial at every iteration
   double fold = 0.3;                   // minimax step: T(1) >= fold * T(l)

@@ -60,9 +60,10 @@ def test_stack_inverse_sqrt_full_size():
 
 def test_wide_6144_full_size():
     """16 fp32 gradients of 6144^2 and 16 of 6144x3072 (alpha -0.5), power -1/4,
-    4 EMA steps; the oracle recomputes one 6144x3072 matrix (its 6144^2 left
-    and 3072^2 right Grams) at every step."""
-    _stack_parity(4, 4, -0.25, sample=[16])
+    4 EMA steps; the oracle recomputes one matrix of each shape at every step:
+    matrix 0 (6144^2, both Grams full-rank 6144^2) and matrix 16 (6144x3072,
+    its rank-deficient 6144^2 left and full-rank 3072^2 right Grams)."""
+    _stack_parity(4, 4, -0.25, sample=[0, 16])
 
 
 @pytest.mark.parametrize("power", [-0.25, -0.5])

@@ -229,6 +229,48 @@ def test_tiny_and_degenerate_shapes(engine):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("engine", [1, 2])
+def test_tiny_and_degenerate_shapes_root_of_the_fp32_state(engine):
+    """The same tiny and rank-deficient shapes at the workloads' eps = 1e-6.
+
+    Here the oracle roots the GPU's own fp32 EMA state (read back after each
+    step and upcast exactly), so the state's rounding, which the caller's fp32
+    layout fixes, is not part of the comparison: what is compared is the root
+    of the Gram the step actually held ("Sharding EMA-Gram eigensolves",
+    Background: rescale, add eps to the eigenvalues, raise to the power,
+    reconstruct), element by element, and the update built from it."""
+    import torch
+    import shampoo_roots_gb300 as sr
+    shapes = [(1, 5), (3, 1), (2, 2), (17, 33)]
+    eps, power, beta = 1e-6, -0.25, 0.9
+    pc = sr.Preconditioner(0, engine=engine)
+    L = [torch.zeros((m, m), device="cuda") for m, _ in shapes]
+    R = [torch.zeros((n, n), device="cuda") for _, n in shapes]
+    worst = {"U": 0.0, "XL": 0.0, "XR": 0.0}
+    for s in range(2):
+        G = [synth.gradient(m, n, -0.5, synth.rng_for(11, s, i), synth.F32) for i, (m, n) in enumerate(shapes)]
+        g = [to_dev(x) for x in G]
+        out = [torch.empty(x.shape, device="cuda") for x in G]
+        sr.precond_step(pc.h, g, L, R, beta, eps, power, out=out)
+        _, _, status, _ = sr.precond_get_stats(pc.h, 2 * len(shapes))
+        assert all(x == 0 for x in status), (s, status)
+        for i, (m, n) in enumerate(shapes):
+            xl = torch.empty((m, m), device="cuda")
+            xr = torch.empty((n, n), device="cuda")
+            sr.precond_get_root(pc.h, 2 * i, xl)
+            sr.precond_get_root(pc.h, 2 * i + 1, xr)
+            xlo = oracle.inv_root_eigh(oracle.trace_normalise(L[i].cpu().numpy().astype(np.float64)), eps, power)
+            xro = oracle.inv_root_eigh(oracle.trace_normalise(R[i].cpu().numpy().astype(np.float64)), eps, power)
+            uo = oracle.precondition(xlo, G[i].astype(np.float64), xro)
+            worst["XL"] = max(worst["XL"], oracle.rel_fro(xl.cpu().numpy(), xlo))
+            worst["XR"] = max(worst["XR"], oracle.rel_fro(xr.cpu().numpy(), xro))
+            worst["U"] = max(worst["U"], oracle.rel_fro(out[i].cpu().numpy(), uo))
+    pc.close()
+    print(f"engine {engine}: worst relative Frobenius errors against the root of the fp32 state {worst}")
+    assert max(worst.values()) <= TOL, worst
+
+
+@pytest.mark.gpu
 def test_zero_gradient_from_zero_state_is_flagged():
     """An all-zero gradient on zero state leaves Grams of trace 0, whose unit-trace
     rescaling is undefined: both roots report ENONFINITE, the output is not

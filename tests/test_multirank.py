@@ -86,7 +86,7 @@ def test_reference_arm_json_line(capsys, monkeypatch):
     import json
     import bench
     monkeypatch.setenv("RANK", "0")
-    args = argparse.Namespace(workload=0, power=None, warmup=1, steps=2, gpus=1)
+    args = argparse.Namespace(workload=0, power=None, warmup=1, steps=2, gpus=1, opt=[])
     bench.run_reference(args)
     lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
     assert len(lines) == 1
@@ -98,3 +98,23 @@ def test_reference_arm_json_line(capsys, monkeypatch):
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"] == "single-256x128"
+    # the same config object as the main arm's line for the same arguments
+    assert d["config"] == bench.workload_config(bench.synth_workload(0), -0.25, {})
+
+
+def test_reference_arm_reports_the_steps_it_ran(capsys, monkeypatch):
+    """When whole oracle steps do not fit the arm's time budget, the line says
+    how many steps it actually ran (at least one, no warm-up) next to the
+    requested counts, and ms_per_step is the measured whole-step time."""
+    import argparse
+    import json
+    import bench
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setattr(bench, "REFERENCE_BUDGET_S", 0.0)
+    args = argparse.Namespace(workload=0, power=None, warmup=3, steps=5, gpus=1, opt=[])
+    bench.run_reference(args)
+    d = json.loads([l for l in capsys.readouterr().out.splitlines() if l.strip()][0])
+    assert d["steps"] == 1 and d["warmup"] == 0
+    assert d["requested"] == {"steps": 5, "warmup": 3}
+    assert d["extrapolated"] is False
+    assert abs(d["ms_per_step"] * d["value"] - 1e3) < 1e-6 * 1e3
