@@ -69,8 +69,12 @@ typedef struct precond_ctx* precond_t;
 #define PRECOND_OPT_MAX_ITER       2  /* iteration cap; 0 = derived from the scalar model (default) */
 #define PRECOND_OPT_MIN_ITER       3  /* stagnation test only after this many iterations; default 4 */
 #define PRECOND_OPT_ENGINE         4  /* 0 auto (default), 1 fp64 SIMT engine, 2 tcgen05 engine */
-#define PRECOND_OPT_SMALL_DIM      5  /* auto engine: max(m,n) <= this -> fp64 SIMT engine; default 0
-                                         (the tcgen05 engine for every size) */
+#define PRECOND_OPT_SMALL_DIM      5  /* auto engine: max(m,n) <= this -> fp64 SIMT engine; default 64.
+                                         Tiny Grams go there: with eps = 1e-6 on a unit-trace Gram of a
+                                         few rows, a rank-deficient Gram's root is set by eigenvalues
+                                         1e-6 below entries of order 1, finer than the tcgen05 engine's
+                                         27-bit digits resolve (larger Grams spread that error over
+                                         many directions and meet 1e-3) */
 #define PRECOND_OPT_WORKSPACE_MAX  6  /* workspace limit in bytes; 0 = unlimited (default) */
 #define PRECOND_OPT_TIMING         7  /* 1 = record per-stage CUDA events (read by precond_get_timing) */
 #define PRECOND_OPT_USE_GRAPH      8  /* 1 = capture each distinct plan (shapes, options, workspace) once as a
@@ -187,9 +191,10 @@ int precond_get_root(precond_t h, int r, float* dst, void* stream);
 /*
  * Self-test of the GEMM core (no counterpart in the method: it checks the
  * library's building block).  C = A . B^T with A (M x K), B (N x K), C (M x N)
- * fp32 device buffers, through engine 1 (fp64 SIMT) or 2 (tcgen05, operands
- * split into per-row-scaled bf16 digits); `passes` = digits used per operand
- * (3 or 4; ignored by engine 1).  Synchronises `stream`.
+ * fp32 device buffers, through engine 1 (fp64 SIMT) or 2 (tcgen05: operands as
+ * three bf16 digits with a scale per row and 128-column block, exact digit
+ * products); `passes` = digits per operand, 3 for engine 2 (ignored by
+ * engine 1).  Synchronises `stream`.
  */
 int precond_gemm_selftest(precond_t h, int engine, int M, int N, int K, const float* A, const float* B,
                           float* C, int passes, void* stream);

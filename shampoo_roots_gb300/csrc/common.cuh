@@ -30,14 +30,8 @@ struct RootStat {
   float seps;          // start: eps / c
   float fin;           // finish: c^(-1/p)
   int pad;
-};
-
-// Per-matrix scalars of a step.
-struct MatStat {
-  float gmax;          // max |G_ij|
-  float rownorm2_max;  // max_i sum_j G_ij^2
-  float sG;            // power-of-two scale of the fp16 split of G
-  float sV;            // power-of-two scale of the fp16 split of V = G X_R
+  double sac_d;        // the start scalars in fp64 (M_0 is formed to more than fp32 precision:
+  double seps_d;       // its smallest eigenvalues are eps / c, far below its largest)
 };
 
 // Convergence control of the Newton-Schulz stage (same for every root of a call).
@@ -92,12 +86,6 @@ __device__ __forceinline__ float load_grad(const void* g, int dtype, long long i
   if (dtype == PRECOND_BF16)
     return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(g)[idx]);
   return reinterpret_cast<const float*>(g)[idx];
-}
-
-// Split y (already scaled) into fp16 hi + lo with y ~= hi + lo.
-__device__ __forceinline__ void split_f16(float y, __half& hi, __half& lo) {
-  hi = __float2half_rn(y);
-  lo = __float2half_rn(y - __half2float(hi));
 }
 
 }  // namespace precond

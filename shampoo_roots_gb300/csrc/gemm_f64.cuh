@@ -65,7 +65,6 @@ gemm_f64_kernel(GemmF64Args g, Epi e) {
     __syncthreads();
   }
 
-  const double sc = (double)e.inv_scale * epi_matrix_scale(e, b);
   double part = 0.0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -75,7 +74,7 @@ gemm_f64_kernel(GemmF64Args g, Epi e) {
     for (int j = 0; j < 4; ++j) {
       const int c = tile_n + tx + 16 * j;
       if (c >= g.N) continue;
-      const double v = epi_apply<ENGINE_F64>(e, b, r, c, acc[i][j] * sc);
+      const double v = epi_apply_f64(e, b, r, c, acc[i][j]);
       if (e.kind == EPI_M) part += v;
     }
   }

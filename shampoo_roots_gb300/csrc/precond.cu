@@ -7,7 +7,8 @@
 //    same side d and engine, batched in the bound, start, iteration and finish
 //    launches.
 // Matrices with max(m, n) <= small_dim use the fp64 SIMT engine, the others
-// the tcgen05 engine (fp16 split operands, fp32 tensor-memory accumulators).
+// the tcgen05 engine (three bf16 digit planes per matrix with per-(row,
+// 128-column block) scales, exact digit products on the tensor cores).
 // Everything is enqueued on the caller's stream; the only host <-> device
 // traffic of a call is one upload of its pointer / index tables.
 
@@ -45,11 +46,10 @@ inline int ld16(int cols) { return (int)align_up((size_t)cols, 64); }   // 16-bi
 
 struct Slab {   // an engine-format matrix batch inside the workspace
   size_t off = 0;        // double plane (fp64 engine) or first bf16 digit plane (tcgen05 engine)
-  int digits = 0;        // digit planes allocated
   long long pstride = 0; // elements between digit planes
   int rows = 0, cols = 0, ld = 0, batch = 0;
-  float scale = 1.f;     // fixed power-of-two digit scale (0: per-row scales in `rowscale`)
-  size_t f32 = 0, rowmax = 0, rowscale = 0;   // fp32 form + per-row max / scale (0: absent)
+  size_t scale = 0;      // tcgen05: block scales [batch][nblk][srows]
+  int nblk = 0, srows = 0;
 };
 
 struct StepPoly {       // per-iteration step polynomials T_k = alpha_k I - beta_k M + gamma_k M^2
@@ -76,8 +76,7 @@ struct ShapeClass {
   int lrc = -1, rrc = -1;
   std::vector<int> lslot, rslot;
   Slab Gd, GTd, VTd;                    // fp64 engine
-  Slab Gq, GTq, VTq;                    // tcgen05 engine: per-row-scaled digits (+ fp32 form)
-  size_t mstat = 0;
+  Slab Gq, GTq, VTq;                    // tcgen05 engine: digits with block scales
   size_t t_g = 0, t_L = 0, t_R = 0, t_out = 0, t_roots2 = 0, t_lslot = 0, t_rslot = 0;
 };
 
@@ -97,7 +96,7 @@ struct Plan {
 struct precond_ctx {
   int device = -1;
   double tol = 1e-4;
-  int max_iter = 0, min_iter = 4, engine = 0, small_dim = 0, timing = 0, use_graph = 1;
+  int max_iter = 0, min_iter = 4, engine = 0, small_dim = 64, timing = 0, use_graph = 1;
   int classical = 0;                   // 1: classical Newton step polynomial at every iteration
   double fold = 0.3;                   // minimax step: T(1) >= fold * T(l)
   std::map<std::string, StepPoly> schedules;   // step schedules already computed (keyed by l0, p, fold, degree)
@@ -331,7 +330,7 @@ struct Layout {
   }
 };
 
-Slab make_slab(Layout& L, int eng, int batch, int rows, int cols, int digits = 4, bool per_row = false) {
+Slab make_slab(Layout& L, int eng, int batch, int rows, int cols) {
   Slab s;
   s.rows = rows;
   s.cols = cols;
@@ -341,15 +340,11 @@ Slab make_slab(Layout& L, int eng, int batch, int rows, int cols, int digits = 4
     s.off = L.take((size_t)batch * rows * cols * sizeof(double));
   } else {
     s.ld = ld16(cols);
-    s.digits = digits;
     s.pstride = (long long)batch * rows * s.ld;
-    s.off = L.take((size_t)s.pstride * 2 * digits);
-    if (per_row) {
-      s.scale = 0.f;
-      s.f32 = L.take((size_t)s.pstride * sizeof(float));
-      s.rowmax = L.take((size_t)batch * rows * sizeof(float));
-      s.rowscale = L.take((size_t)batch * rows * sizeof(float));
-    }
+    s.off = L.take((size_t)s.pstride * 2 * DIGITS);
+    s.nblk = (cols + DIG_BLK - 1) / DIG_BLK;
+    s.srows = (int)align_up((size_t)rows, 128);
+    s.scale = L.take((size_t)batch * s.nblk * s.srows * sizeof(float));
   }
   return s;
 }
@@ -381,16 +376,16 @@ int pick_engine(const precond_ctx* h, int64_t maxdim) {
 }
 
 // Root-class planes.  The iteration is written without identity offsets in
-// any product operand (see launch_iterations), so every tcgen05 operand is a
-// per-row-scaled digit split of an fp32 matrix.
+// any product operand (see launch_iterations), so every tcgen05 operand holds
+// its own information in its digits.
 void layout_root_class(Layout& L, RootClass& r, int p) {
   const int nb = (int)r.roots.size(), d = r.d, e = r.eng;
   for (int i = 0; i < 2; ++i) {
-    r.X[i] = make_slab(L, e, nb, d, d, 4, true);
-    r.M[i] = make_slab(L, e, nb, d, d, 4, true);
+    r.X[i] = make_slab(L, e, nb, d, d);
+    r.M[i] = make_slab(L, e, nb, d, d);
   }
-  r.D = make_slab(L, e, nb, d, d, 4, true);
-  if (p == 4) r.F = make_slab(L, e, nb, d, d, 4, true);
+  r.D = make_slab(L, e, nb, d, d);
+  if (p == 4) r.F = make_slab(L, e, nb, d, d);
   r.Xf = r.D;   // D is free once the iteration ends; the finished root takes its place
   r.rowabs = L.take((size_t)nb * d * sizeof(double));
   r.diag = L.take((size_t)nb * d * sizeof(double));
@@ -512,11 +507,10 @@ int build_plan(precond_ctx* h, Plan& P, bool step, int count, const int64_t* dim
       c.GTd = make_slab(L, ENGINE_F64, nb, c.n, c.m);
       c.VTd = make_slab(L, ENGINE_F64, nb, c.n, c.m);
     } else {
-      c.Gq = make_slab(L, ENGINE_TC, nb, c.m, c.n, 4, true);
-      c.GTq = make_slab(L, ENGINE_TC, nb, c.n, c.m, 4, true);
-      c.VTq = make_slab(L, ENGINE_TC, nb, c.n, c.m, 4, true);
+      c.Gq = make_slab(L, ENGINE_TC, nb, c.m, c.n);
+      c.GTq = make_slab(L, ENGINE_TC, nb, c.n, c.m);
+      c.VTq = make_slab(L, ENGINE_TC, nb, c.n, c.m);
     }
-    c.mstat = L.take(sizeof(MatStat) * nb);
   }
   // meta tables
   P.meta = L.top;
@@ -598,6 +592,22 @@ int upload_meta(precond_ctx* h, const Plan& P, cudaStream_t st) {
 }
 
 // --------------------------------------------------------------------------- launch helpers
+Plane slab_plane(char* ws, const Slab& s) {
+  Plane p;
+  memset(&p, 0, sizeof(p));
+  p.hi = ws + s.off;
+  p.pstride = s.pstride;
+  p.bstride = (long long)s.rows * s.ld;
+  p.ld = s.ld;
+  p.rows = s.rows;
+  if (s.nblk) {
+    p.scale = reinterpret_cast<float*>(ws + s.scale);
+    p.sbstride = (long long)s.nblk * s.srows;
+    p.srows = s.srows;
+  }
+  return p;
+}
+
 struct Ctx {
   precond_ctx* h;
   const Plan& P;
@@ -607,30 +617,7 @@ struct Ctx {
   T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
   RootStat* stats() const { return at<RootStat>(P.stats); }
   unsigned int* err() const { return at<unsigned int>(P.err); }
-  // Store target: the digit form, or the fp32 form for per-row-scaled slabs.
-  Plane plane(const Slab& s) const {
-    Plane p;
-    memset(&p, 0, sizeof(p));
-    p.hi = ws + s.off;
-    p.pstride = s.pstride;
-    p.bstride = (long long)s.rows * s.ld;
-    p.ld = s.ld;
-    p.scale = s.scale;
-    p.S = s.digits;
-    p.rows = s.rows;
-    if (s.f32) {
-      p.f32 = reinterpret_cast<float*>(ws + s.f32);
-      p.rowmax = reinterpret_cast<float*>(ws + s.rowmax);
-    }
-    return p;
-  }
-  // Load source: always the digit form (or the double plane).
-  Plane digits(const Slab& s) const {
-    Plane p = plane(s);
-    p.f32 = nullptr;
-    p.rowmax = nullptr;
-    return p;
-  }
+  Plane plane(const Slab& s) const { return slab_plane(ws, s); }
 };
 
 Epi base_epi(const Ctx& c, int kind, int rows, int cols) {
@@ -640,17 +627,20 @@ Epi base_epi(const Ctx& c, int kind, int rows, int cols) {
   e.rows = rows;
   e.cols = cols;
   e.stats = c.stats();
-  e.inv_scale = 1.f;
+  e.alpha = 1.0;
   return e;
 }
 
-int encode_map(precond_ctx* h, CUtensorMap* map, void* base, const Slab& s, int box_rows) {
+// Tensor map of one digit plane of a slab: operand boxes {K block 32, 128 rows}
+// with 64-byte swizzle (the MMA operand layout), or epilogue boxes {64, 64}
+// with 128-byte swizzle (the staging area of the epilogue's input and output).
+int encode_map(precond_ctx* h, CUtensorMap* map, void* base, const Slab& s, int box_rows, bool epilogue = false) {
   cuuint64_t dims[3] = {(cuuint64_t)s.cols, (cuuint64_t)s.rows, (cuuint64_t)s.batch};
   cuuint64_t strides[2] = {(cuuint64_t)s.ld * 2, (cuuint64_t)s.ld * 2 * s.rows};
-  cuuint32_t box[3] = {(cuuint32_t)TC_BK, (cuuint32_t)box_rows, 1};
+  cuuint32_t box[3] = {(cuuint32_t)(epilogue ? 64 : TC_BK), (cuuint32_t)(epilogue ? 64 : box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, epilogue ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     fprintf(stderr, "libprecond: cuTensorMapEncodeTiled failed (%d)\n", (int)r);
@@ -659,10 +649,12 @@ int encode_map(precond_ctx* h, CUtensorMap* map, void* base, const Slab& s, int 
   return PRECOND_OK;
 }
 
-// Batched product C_b = A_b B_b^T in the engine of the operands; the tcgen05
-// engine uses the first `S` digit planes of each operand (S = 3 or 4).
+// Batched product C_b = A_b B_b^T in the engine of the operands.
+// Cs / Ins: the slabs of a digit output (EPI_AFF, EPI_M, EPI_VT) and of the
+// element-wise input (EPI_AFF, EPI_M) of the tcgen05 engine, for their tensor maps.
 int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int K, const int* aidx,
-         const int* bidx, int S, const Epi& e0, int batch, bool sym = false) {
+         const int* bidx, const Epi& e0, int batch, bool sym = false, const Slab* Cs = nullptr,
+         const Slab* Ins = nullptr) {
   Epi e = e0;
   if (eng == ENGINE_F64) {
     GemmF64Args g;
@@ -681,13 +673,16 @@ int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int 
     e.tiles_per_entry = grid.x * grid.y;
     gemm_f64_kernel<<<grid, 256, 0, c.st>>>(g, e);
   } else {
-    if (S > A.digits || S > B.digits) return PRECOND_EINVAL;
     TcMaps maps;
     memset(&maps, 0, sizeof(maps));
     int rc;
-    for (int q = 0; q < S; ++q) {
+    for (int q = 0; q < DIGITS; ++q) {
       if ((rc = encode_map(c.h, &maps.a[q], c.ws + A.off + (size_t)q * A.pstride * 2, A, TC_BM))) return rc;
       if ((rc = encode_map(c.h, &maps.b[q], c.ws + B.off + (size_t)q * B.pstride * 2, B, TC_BN))) return rc;
+      if (Cs && (rc = encode_map(c.h, &maps.c[q], c.ws + Cs->off + (size_t)q * Cs->pstride * 2, *Cs, TC_BM, true)))
+        return rc;
+      if (Ins && (rc = encode_map(c.h, &maps.in[q], c.ws + Ins->off + (size_t)q * Ins->pstride * 2, *Ins, TC_BM, true)))
+        return rc;
     }
     TcGemmArgs g;
     memset(&g, 0, sizeof(g));
@@ -696,12 +691,12 @@ int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int 
     g.K = K;
     g.a_index = aidx;
     g.b_index = bidx;
-    g.a_rowscale = A.rowscale ? c.at<const float>(A.rowscale) : nullptr;
-    g.a_rs_stride = A.rows;
-    g.a_scale = A.scale;
-    g.b_rowscale = B.rowscale ? c.at<const float>(B.rowscale) : nullptr;
-    g.b_rs_stride = B.rows;
-    g.b_scale = B.scale;
+    g.a_scale = c.at<const float>(A.scale);
+    g.a_sbstride = (long long)A.nblk * A.srows;
+    g.a_srows = A.srows;
+    g.b_scale = c.at<const float>(B.scale);
+    g.b_sbstride = (long long)B.nblk * B.srows;
+    g.b_srows = B.srows;
     g.err = c.err();
     g.batch = batch;
     g.sym = (sym && M == N) ? 1 : 0;
@@ -720,10 +715,7 @@ int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int 
       }
       CK(record_event(c.h, c.h->gemm_ev[c.h->gemm_ev_used], c.st));
     }
-    if (S == 4)
-      gemm_tc_kernel<4><<<grid, TC_THREADS, TcSmem<4>::BYTES, c.st>>>(maps, g, e);
-    else
-      gemm_tc_kernel<3><<<grid, TC_THREADS, TcSmem<3>::BYTES, c.st>>>(maps, g, e);
+    gemm_tc_kernel<<<grid, TC_THREADS, TcSmem::BYTES, c.st>>>(maps, g, e);
     if (timed) {
       CK(record_event(c.h, c.h->gemm_ev[c.h->gemm_ev_used + 1], c.st));
       c.h->gemm_ev_used += 2;
@@ -734,35 +726,8 @@ int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int 
   return PRECOND_OK;
 }
 
-// Per-row-scaled digits of a slab's fp32 form.
-// Blocks per root of the start / finish kernels: one per 32-row strip.
+// Blocks per root of the fp64 start / finish kernels: one per 32-row strip.
 unsigned int tile_blocks(int d) { return (unsigned int)((d + 31) / 32); }
-
-// `root_of` (a root class's batch-entry -> root table, or null): skip the
-// entries of converged roots (iteration stage only).
-int slice(const Ctx& c, const Slab& s, const int* root_of = nullptr) {
-  SliceArgs a;
-  a.root_of = root_of;
-  a.stats = c.stats();
-  a.src = c.at<const float>(s.f32);
-  a.src_bstride = (long long)s.rows * s.ld;
-  a.src_ld = s.ld;
-  a.rowmax = c.at<const float>(s.rowmax);
-  a.rowscale = c.at<float>(s.rowscale);
-  a.dst = c.digits(s);
-  a.rows = s.rows;
-  a.cols = s.cols;
-  const int rb = std::min((s.rows + 7) / 8, 1024);
-  slice_rows_kernel<<<dim3(rb, s.batch), 256, 0, c.st>>>(a);
-  c.h->launches++;
-  CK(cudaGetLastError());
-  return PRECOND_OK;
-}
-
-int clear_rowmax(const Ctx& c, const Slab& s) {
-  if (s.rowmax) CK(cudaMemsetAsync(c.ws + s.rowmax, 0, (size_t)s.batch * s.rows * sizeof(float), c.st));
-  return PRECOND_OK;
-}
 
 RootArgs root_args(const Ctx& c, const RootClass& r, float eps) {
   RootArgs a;
@@ -780,11 +745,12 @@ RootArgs root_args(const Ctx& c, const RootClass& r, float eps) {
   a.ctl.kmin = c.h->min_iter;
   a.ctl.kmax = r.kmax;
   a.ctl.tol = (float)c.h->tol;
-  a.M0 = c.plane(r.M[0]);     // fp32 form (tcgen05 engine), sliced after the start
+  a.M0 = c.plane(r.M[0]);
   a.X1 = c.plane(r.X[1]);
   a.alpha0 = r.steps.alpha[0];
   a.beta0 = r.steps.beta[0];
-  a.X[0] = c.plane(r.X[0]);   // read in fp32 form by the finish
+  a.write_x1 = r.steps.gamma[0] == 0.0 ? 1 : 0;   // quadratic first steps form X_1 from E_0
+  a.X[0] = c.plane(r.X[0]);
   a.X[1] = c.plane(r.X[1]);
   a.Xf = c.plane(r.Xf);
   a.dst = c.P.step ? nullptr : c.at<float* const>(r.t_dst);
@@ -800,17 +766,12 @@ int launch_roots_start(const Ctx& c, float eps) {
     root_trace_kernel<<<nb, 256, 0, c.st>>>(a);
     root_bound_kernel<<<dim3(rb, nb), 256, r.d <= 12288 ? r.d * sizeof(float) : 0, c.st>>>(a);
     root_scalar_kernel<<<(nb + 127) / 128, 128, 0, c.st>>>(a, nb);
-    dim3 g(tile_blocks(r.d), 1, nb);
-    int rc;
-    if (r.eng == ENGINE_F64) {
-      root_init_kernel<ENGINE_F64><<<g, 256, 0, c.st>>>(a);
-    } else {
-      if ((rc = clear_rowmax(c, r.M[0])) || (rc = clear_rowmax(c, r.X[1]))) return rc;
-      root_init_kernel<ENGINE_TC><<<g, 256, 0, c.st>>>(a);
-    }
+    if (r.eng == ENGINE_F64)
+      root_init_f64_kernel<<<dim3(tile_blocks(r.d), 1, nb), 256, 0, c.st>>>(a);
+    else
+      root_init_tc_kernel<<<dim3((r.d + 127) / 128, (r.d + 31) / 32, nb), 256, 0, c.st>>>(a);
     c.h->launches += 5;
     CK(cudaGetLastError());
-    if (r.eng == ENGINE_TC && ((rc = slice(c, r.M[0])) || (rc = slice(c, r.X[1])))) return rc;
   }
   return PRECOND_OK;
 }
@@ -887,7 +848,6 @@ int launch_iterations(const Ctx& c) {
       e.ctl.kmax = r.kmax;
       e.ctl.tol = (float)c.h->tol;
       e.k = k;
-      const bool tc = eng == ENGINE_TC;
       // Identity-free form of  T = tau I - M/p,  tau = (p+1)/p:
       //   p = 2:  T^2 = tau^2 I + D,   D = M M / p^2 - (2 tau / p) M,   M' = tau^2 M + D M
       //   p = 4:  T^2 = tau^2 I + D,   T^4 = tau^4 I + F,   F = D D + 2 tau^2 D,   M' = tau^4 M + F M
@@ -895,11 +855,8 @@ int launch_iterations(const Ctx& c) {
       // so every product operand (M, D, F, X) keeps its information in its own
       // digits instead of next to a dominant identity.
       const double al = r.steps.alpha[k], be = r.steps.beta[k];
-      // every product of the iteration takes 4 digits: 3 (about 2^-21), even only in the
-      // middle iterations, put the roots' errors at 2e-3 to 7e-3
-      const int mdig = 4;
       auto aff = [&](const Ctx& cc, const Slab& A, const Slab& B, const Slab& In, const Slab& C, double alpha,
-                     double beta_in, int digits) -> int {
+                     double beta_in) -> int {
         Epi ea = e;
         ea.kind = EPI_AFF;
         ea.C = cc.plane(C);
@@ -908,10 +865,8 @@ int launch_iterations(const Ctx& c) {
         ea.beta_in = beta_in;
         ea.gamma = 0.0;
         int rc2;
-        if (tc && (rc2 = clear_rowmax(cc, C))) return rc2;
-        if ((rc2 = gemm(cc, eng, A, B, d, d, d, nullptr, nullptr, digits, ea, nb, true))) return rc2;
+        if ((rc2 = gemm(cc, eng, A, B, d, d, d, nullptr, nullptr, ea, nb, true, &C, &In))) return rc2;
         ++n;
-        if (tc && (rc2 = slice(cc, C, root_of))) return rc2;
         return PRECOND_OK;
       };
       // T = al I - be M:  T^2 = al^2 I + D, D = be^2 M M - 2 al be M;  T^4 = al^4 I + F,
@@ -923,15 +878,15 @@ int launch_iterations(const Ctx& c) {
         // linear step T = al I - be M
         if (k >= 1) {
           if (br) CK(cudaStreamWaitEvent(cx.st, mready[ri], 0));
-          if ((rcode = aff(cx, r.X[cur], r.M[cur], r.X[cur], r.X[nxt], -be, al, 4))) return rcode;
+          if ((rcode = aff(cx, r.X[cur], r.M[cur], r.X[cur], r.X[nxt], -be, al))) return rcode;
           if (br) {
             if ((rcode = next_event(c.h, used, &xdone))) return rcode;
             CK(cudaEventRecord(xdone, cx.st));
           }
         }
-        if ((rcode = aff(cm, r.M[cur], r.M[cur], r.M[cur], r.D, be * be, -2.0 * al * be, mdig))) return rcode;
+        if ((rcode = aff(cm, r.M[cur], r.M[cur], r.M[cur], r.D, be * be, -2.0 * al * be))) return rcode;
         if (p == 4) {
-          if ((rcode = aff(cm, r.D, r.D, r.D, r.F, 1.0, 2.0 * al * al, mdig))) return rcode;
+          if ((rcode = aff(cm, r.D, r.D, r.D, r.F, 1.0, 2.0 * al * al))) return rcode;
           Pk = &r.F;
         }
       } else {
@@ -939,7 +894,7 @@ int launch_iterations(const Ctx& c) {
         // D = E E + 2 al E (= T^2 - al^2 I), F = D D + 2 al^2 D (= T^4 - al^4 I).
         // E lives in F's slab: F is written after the last reads of E.
         const Slab& E = r.F;
-        if ((rcode = aff(cm, r.M[cur], r.M[cur], r.M[cur], E, ga, -be, mdig))) return rcode;
+        if ((rcode = aff(cm, r.M[cur], r.M[cur], r.M[cur], E, ga, -be))) return rcode;
         if (br) {
           cudaEvent_t eready;
           if ((rcode = next_event(c.h, used, &eready))) return rcode;
@@ -954,22 +909,23 @@ int launch_iterations(const Ctx& c) {
           sa.stats = c.stats();
           sa.d = d;
           sa.alpha = (float)al;
-          dim3 g((unsigned int)std::min((d + 7) / 8, 1024), (unsigned int)nb);
-          if (eng == ENGINE_F64) shift_identity_kernel<ENGINE_F64><<<g, 256, 0, cx.st>>>(sa);
-          else shift_identity_kernel<ENGINE_TC><<<g, 256, 0, cx.st>>>(sa);
+          if (eng == ENGINE_F64)
+            shift_identity_f64_kernel<<<dim3((unsigned int)std::min((d + 7) / 8, 1024), (unsigned int)nb), 256, 0,
+                                        cx.st>>>(sa);
+          else
+            shift_identity_tc_kernel<<<dim3((d + 127) / 128, (d + 7) / 8, nb), 256, 0, cx.st>>>(sa);
           c.h->launches++;
           CK(cudaGetLastError());
-          if (tc && (rcode = slice(cx, r.X[nxt], root_of))) return rcode;
-        } else if ((rcode = aff(cx, r.X[cur], E, r.X[cur], r.X[nxt], 1.0, al, 4))) {
+        } else if ((rcode = aff(cx, r.X[cur], E, r.X[cur], r.X[nxt], 1.0, al))) {
           return rcode;
         }
         if (br) {
           if ((rcode = next_event(c.h, used, &xdone))) return rcode;
           CK(cudaEventRecord(xdone, cx.st));
         }
-        if ((rcode = aff(cm, E, E, E, r.D, 1.0, 2.0 * al, mdig))) return rcode;
+        if ((rcode = aff(cm, E, E, E, r.D, 1.0, 2.0 * al))) return rcode;
         if (xdone) CK(cudaStreamWaitEvent(cm.st, xdone, 0));     // F overwrites E
-        if ((rcode = aff(cm, r.D, r.D, r.D, r.F, 1.0, 2.0 * al * al, mdig))) return rcode;
+        if ((rcode = aff(cm, r.D, r.D, r.D, r.F, 1.0, 2.0 * al * al))) return rcode;
         Pk = &r.F;
       }
       Epi em = e;     // M_{k+1} = tau^p M_k + P M_k, residual, convergence
@@ -980,10 +936,11 @@ int launch_iterations(const Ctx& c) {
       if (xdone) CK(cudaStreamWaitEvent(cm.st, xdone, 0));
       // symmetric product (upper-triangle tiles mirrored): M' is exactly symmetric,
       // which also removes the antisymmetric mode the iteration would amplify
-      if (tc && (rcode = clear_rowmax(cm, r.M[nxt]))) return rcode;
-      if ((rcode = gemm(cm, eng, *Pk, r.M[cur], d, d, d, nullptr, nullptr, mdig, em, nb, true))) return rcode;
+      // M' = M P (P = D or F, a polynomial in M: it commits with M), so that the element-wise
+      // input M is the product's first operand
+      if ((rcode = gemm(cm, eng, r.M[cur], *Pk, d, d, d, nullptr, nullptr, em, nb, true, &r.M[nxt], &r.M[cur])))
+        return rcode;
       ++n;
-      if (tc && (rcode = slice(cm, r.M[nxt], root_of))) return rcode;
       if (br) {
         if ((rcode = next_event(c.h, used, &mready[ri]))) return rcode;
         CK(cudaEventRecord(mready[ri], cm.st));
@@ -1005,29 +962,14 @@ int launch_finish(const Ctx& c, float eps) {
   for (const auto& r : c.P.rc) {
     const int nb = (int)r.roots.size();
     RootArgs a = root_args(c, r, eps);
-    dim3 g(tile_blocks(r.d), 1, nb);
-    int rc;
-    if (r.eng == ENGINE_TC && c.P.step && (rc = clear_rowmax(c, r.Xf))) return rc;
-    if (r.eng == ENGINE_F64) root_finish_kernel<ENGINE_F64><<<g, 256, 0, c.st>>>(a);
-    else root_finish_kernel<ENGINE_TC><<<g, 256, 0, c.st>>>(a);
+    if (r.eng == ENGINE_F64)
+      root_finish_f64_kernel<<<dim3(tile_blocks(r.d), 1, nb), 256, 0, c.st>>>(a);
+    else
+      root_finish_tc_kernel<<<dim3((r.d + 127) / 128, (r.d + 31) / 32, nb), 256, 0, c.st>>>(a);
     c.h->launches++;
     CK(cudaGetLastError());
-    if (r.eng == ENGINE_TC && c.P.step && (rc = slice(c, r.Xf))) return rc;
   }
   return PRECOND_OK;
-}
-
-Plane digits_plane(char* ws, const Slab& s) {
-  Plane p;
-  memset(&p, 0, sizeof(p));
-  p.hi = ws + s.off;
-  p.pstride = s.pstride;
-  p.bstride = (long long)s.rows * s.ld;
-  p.ld = s.ld;
-  p.scale = s.scale;
-  p.S = s.digits;
-  p.rows = s.rows;
-  return p;
 }
 
 int record(precond_ctx* h, int i, cudaStream_t st) {
@@ -1044,7 +986,6 @@ int run_step(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream_t 
   // ---- preparation + Gram EMA
   for (const auto& s : P.sc) {
     const int nb = (int)s.mats.size();
-    CK(cudaMemsetAsync(c.ws + s.mstat, 0, sizeof(MatStat) * nb, st));
     PrepArgs a;
     memset(&a, 0, sizeof(a));
     a.g = c.at<const void* const>(s.t_g);
@@ -1053,31 +994,18 @@ int run_step(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream_t 
     a.n = s.n;
     a.roots2 = c.at<const int>(s.t_roots2);
     a.stats = c.stats();
-    a.mstat = c.at<MatStat>(s.mstat);
     const bool tc = s.eng == ENGINE_TC;
     if (tc) {
-      a.Gf = c.at<float>(s.Gq.f32);
-      a.ldn = s.Gq.ld;
-      a.GTf = c.at<float>(s.GTq.f32);
-      a.ldm = s.GTq.ld;
-      a.rowmax_G = c.at<float>(s.Gq.rowmax);
-      a.rowmax_GT = c.at<float>(s.GTq.rowmax);
-      if ((rc = clear_rowmax(c, s.GTq))) return rc;
+      a.G = c.plane(s.Gq);
+      a.GT = c.plane(s.GTq);
+      prep_tc_kernel<<<dim3((s.n + 127) / 128, (s.m + 127) / 128, nb), 256, PREP_SMEM, st>>>(a);
     } else {
-      a.Gd = c.at<double>(s.Gd.off);
-      a.GTd = c.at<double>(s.GTd.off);
+      a.G = c.plane(s.Gd);
+      a.GT = c.plane(s.GTd);
+      prep_f64_kernel<<<dim3((s.n + 31) / 32, (s.m + 31) / 32, nb), 256, 0, st>>>(a);
     }
-    dim3 gs((s.n + 31) / 32, (s.m + 31) / 32, nb);
-    const int rb = std::min((s.m + 7) / 8, 512);
-    prep_reduce_kernel<<<dim3(rb, nb), 256, 0, st>>>(a);
-    if (tc) prep_split_kernel<ENGINE_TC><<<gs, 256, 0, st>>>(a);
-    else prep_split_kernel<ENGINE_F64><<<gs, 256, 0, st>>>(a);
-    h->launches += 2;
+    h->launches++;
     CK(cudaGetLastError());
-    if (tc) {
-      if ((rc = slice(c, s.Gq))) return rc;
-      if ((rc = slice(c, s.GTq))) return rc;
-    }
     for (int side = 0; side < 2; ++side) {
       const int dim = side == 0 ? s.m : s.n, K = side == 0 ? s.n : s.m;
       Epi e = base_epi(c, EPI_GRAM, dim, dim);
@@ -1085,7 +1013,7 @@ int run_step(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream_t 
       e.beta = beta;
       e.nonfinite_of = c.at<const int>(s.t_roots2);
       const Slab& G = tc ? (side == 0 ? s.Gq : s.GTq) : (side == 0 ? s.Gd : s.GTd);
-      if ((rc = gemm(c, s.eng, G, G, dim, dim, K, nullptr, nullptr, 4, e, nb, true))) return rc;
+      if ((rc = gemm(c, s.eng, G, G, dim, dim, K, nullptr, nullptr, e, nb, true))) return rc;
     }
   }
   if ((rc = record(h, 1, st))) return rc;
@@ -1106,17 +1034,12 @@ int run_step(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream_t 
     eu.nonfinite_of = c.at<const int>(s.t_roots2);
     const int* lsl = c.at<const int>(s.t_lslot);
     const int* rsl = c.at<const int>(s.t_rslot);
-    if (s.eng == ENGINE_F64) {
-      ev.C = c.plane(s.VTd);
-      if ((rc = gemm(c, ENGINE_F64, s.Gd, r.Xf, s.m, s.n, s.n, nullptr, rsl, 4, ev, nb))) return rc;
-      if ((rc = gemm(c, ENGINE_F64, l.Xf, s.VTd, s.m, s.n, s.m, lsl, nullptr, 4, eu, nb))) return rc;
-    } else {
-      ev.C = c.plane(s.VTq);
-      if ((rc = clear_rowmax(c, s.VTq))) return rc;
-      if ((rc = gemm(c, ENGINE_TC, s.Gq, r.Xf, s.m, s.n, s.n, nullptr, rsl, 4, ev, nb))) return rc;
-      if ((rc = slice(c, s.VTq))) return rc;
-      if ((rc = gemm(c, ENGINE_TC, l.Xf, s.VTq, s.m, s.n, s.m, lsl, nullptr, 4, eu, nb))) return rc;
-    }
+    const bool tc = s.eng == ENGINE_TC;
+    const Slab& G = tc ? s.Gq : s.Gd;
+    const Slab& VT = tc ? s.VTq : s.VTd;
+    ev.C = c.plane(VT);
+    if ((rc = gemm(c, s.eng, G, r.Xf, s.m, s.n, s.n, nullptr, rsl, ev, nb, false, &VT))) return rc;
+    if ((rc = gemm(c, s.eng, l.Xf, VT, s.m, s.n, s.m, lsl, nullptr, eu, nb))) return rc;
   }
   if ((rc = record(h, 4, st))) return rc;
   return PRECOND_OK;
@@ -1141,8 +1064,8 @@ int run_inv_root(precond_ctx* h, const Plan& P, float eps, cudaStream_t st) {
 int prepare_device(precond_ctx* h) {
   CK(cudaSetDevice(h->device));
   if (!h->tc_attr_set) {
-    CK(cudaFuncSetAttribute(gemm_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<4>::BYTES));
-    CK(cudaFuncSetAttribute(gemm_tc_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<3>::BYTES));
+    CK(cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::BYTES));
+    CK(cudaFuncSetAttribute(prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM));
     CK(cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device));
     h->tc_attr_set = true;
   }
@@ -1547,8 +1470,7 @@ int precond_get_root(precond_t h, int r, float* dst, void* stream) {
   if (!h->have_last || r < 0 || r >= h->last_nroots) return PRECOND_EINVAL;
   const RootClass& rc = h->last_plan.rc[h->last_root_class[r]];
   const int slot = h->last_root_slot[r];
-  Plane p = digits_plane((char*)h->ws, rc.Xf);
-  if (rc.Xf.f32) p.f32 = reinterpret_cast<float*>((char*)h->ws + rc.Xf.f32);   // fp32 form of the root
+  Plane p = slab_plane((char*)h->ws, rc.Xf);
   cudaStream_t st = (cudaStream_t)stream;
   if (rc.eng == ENGINE_F64) plane_to_f32_kernel<ENGINE_F64><<<256, 256, 0, st>>>(p, slot, rc.d, rc.d, dst);
   else plane_to_f32_kernel<ENGINE_TC><<<256, 256, 0, st>>>(p, slot, rc.d, rc.d, dst);
@@ -1567,8 +1489,7 @@ int precond_debug_plane(precond_t h, int r, int which, float* dst, void* stream)
   const Slab* sl[9] = {&rc.X[0], &rc.X[1], &rc.M[0], &rc.M[1], &rc.D, &rc.F, nullptr, nullptr, &rc.Xf};
   const Slab& S = *sl[which];
   if (S.batch == 0) return PRECOND_EINVAL;
-  Plane p = digits_plane((char*)h->ws, S);
-  if (S.f32) p.f32 = reinterpret_cast<float*>((char*)h->ws + S.f32);   // per-row matrices: read the fp32 form
+  Plane p = slab_plane((char*)h->ws, S);
   cudaStream_t st = (cudaStream_t)stream;
   const int slot = h->last_root_slot[r];
   if (rc.eng == ENGINE_F64) plane_to_f32_kernel<ENGINE_F64><<<256, 256, 0, st>>>(p, slot, rc.d, rc.d, dst);
@@ -1582,7 +1503,7 @@ int precond_debug_plane(precond_t h, int r, int which, float* dst, void* stream)
 int precond_gemm_selftest(precond_t h, int engine, int M, int N, int K, const float* A, const float* B, float* C,
                           int passes, void* stream) {
   if (!h || !A || !B || !C || M < 1 || N < 1 || K < 1 || (engine != 1 && engine != 2)) return PRECOND_EINVAL;
-  if (passes != 3 && passes != 4) return PRECOND_EINVAL;
+  if (engine == 2 && passes != DIGITS) return PRECOND_EINVAL;
   if (h->device < 0) return PRECOND_ENODEV;
   int rc;
   if ((rc = prepare_device(h))) return rc;
@@ -1591,27 +1512,22 @@ int precond_gemm_selftest(precond_t h, int engine, int M, int N, int K, const fl
   Plan P;
   P.stats = L.take(sizeof(RootStat));
   P.err = L.take(64);
-  Slab sa = make_slab(L, eng, 1, M, K, 4, true), sb = make_slab(L, eng, 1, N, K, 4, true);
-  Slab sc = make_slab(L, eng, 1, M, N, 4, true);
+  Slab sa = make_slab(L, eng, 1, M, K), sb = make_slab(L, eng, 1, N, K);
   if ((rc = ensure_workspace(h, L.top))) return rc;
   cudaStream_t st = (cudaStream_t)stream;
   Ctx c{h, P, (char*)h->ws, st};
   CK(cudaMemsetAsync(c.ws + P.stats, 0, sizeof(RootStat), st));
   CK(cudaMemsetAsync(c.ws + P.err, 0, 64, st));
   if (eng == ENGINE_F64) {
-    f32_to_plane_kernel<ENGINE_F64><<<256, 256, 0, st>>>(A, c.plane(sa), M, K);
-    f32_to_plane_kernel<ENGINE_F64><<<256, 256, 0, st>>>(B, c.plane(sb), N, K);
+    f32_to_f64_kernel<<<256, 256, 0, st>>>(A, c.plane(sa), M, K);
+    f32_to_f64_kernel<<<256, 256, 0, st>>>(B, c.plane(sb), N, K);
   } else {
-    if ((rc = clear_rowmax(c, sa)) || (rc = clear_rowmax(c, sb))) return rc;
-    f32_to_plane_kernel<ENGINE_TC><<<256, 256, 0, st>>>(A, c.plane(sa), M, K);
-    f32_to_plane_kernel<ENGINE_TC><<<256, 256, 0, st>>>(B, c.plane(sb), N, K);
-    if ((rc = slice(c, sa)) || (rc = slice(c, sb))) return rc;
+    f32_to_tc_kernel<<<dim3((K + 127) / 128, (M + 7) / 8), 256, 0, st>>>(A, c.plane(sa), M, K);
+    f32_to_tc_kernel<<<dim3((K + 127) / 128, (N + 7) / 8), 256, 0, st>>>(B, c.plane(sb), N, K);
   }
   Epi e = base_epi(c, EPI_STORE, M, N);
-  e.C = c.plane(sc);
-  if ((rc = gemm(c, eng, sa, sb, M, N, K, nullptr, nullptr, passes, e, 1))) return rc;
-  if (eng == ENGINE_F64) plane_to_f32_kernel<ENGINE_F64><<<256, 256, 0, st>>>(c.plane(sc), 0, M, N, C);
-  else plane_to_f32_kernel<ENGINE_TC><<<256, 256, 0, st>>>(c.plane(sc), 0, M, N, C);
+  e.f32out = C;
+  if ((rc = gemm(c, eng, sa, sb, M, N, K, nullptr, nullptr, e, 1))) return rc;
   CK(cudaGetLastError());
   CK(cudaStreamSynchronize(st));
   unsigned int err = 0;

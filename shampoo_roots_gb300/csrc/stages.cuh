@@ -1,6 +1,10 @@
 // Element-wise and reduction stages of the preconditioner step:
 // gradient preparation, Gram statistics, the largest-eigenvalue bound, the
 // start of the iteration and its finish.  All O(d^2), HBM-bound.
+//
+// The tcgen05 engine's kernels work on (row, 128-column block) units: one warp
+// owns a row's block, forms its values, takes the block maximum for the scale
+// and writes the digits (engine.cuh).
 #pragma once
 
 #include "engine.cuh"
@@ -16,170 +20,82 @@ struct PrepArgs {
   int m, n;
   const int* roots2;      // per batch entry: the two root ids (left, right)
   RootStat* stats;
-  MatStat* mstat;
-  // fp64 engine outputs
-  double* Gd; double* GTd;            // [b][m][n], [b][n][m]
-  // tcgen05 engine outputs: fp32 copies (rows padded to ld) and row maxima
-  float* Gf; int ldn;                 // [b][m][ldn]
-  float* GTf; int ldm;                // [b][n][ldm]
-  float* rowmax_G;                    // [b][m]   max_j |G_ij|
-  float* rowmax_GT;                   // [b][n]   max_i |G_ij|
+  Plane G, GT;            // engine copies of G (m x n) and G^T (n x m)
 };
 
-__device__ __forceinline__ float pow2_scale(float target, float maxabs) {
-  // largest power of two s with maxabs * s <= target (1 when maxabs is 0)
-  if (!(maxabs > 0.0f) || !isfinite(maxabs)) return 1.0f;
-  int e;
-  frexpf(target / maxabs, &e);     // target/maxabs = f * 2^e, f in [0.5, 1)
-  return ldexpf(1.0f, e - 1);
-}
-
-// Per batch entry: max |G|, max row sum of squares, non-finite check.
-__global__ void __launch_bounds__(256) prep_reduce_kernel(PrepArgs a) {
-  const int b = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const void* g = a.g[b];
-  float gmax = 0.f, rmax = 0.f;
-  int bad = 0;
-  for (int r = blockIdx.x * 8 + warp; r < a.m; r += gridDim.x * 8) {
-    float s2 = 0.f, mx = 0.f;
-    for (int c = lane; c < a.n; c += 32) {
-      const float v = load_grad(g, a.dtype, (long long)r * a.n + c);
-      if (!isfinite(v)) bad = 1;
-      s2 = fmaf(v, v, s2);
-      mx = fmaxf(mx, fabsf(v));
-    }
-    s2 = warp_sum(s2);
-    mx = warp_max(mx);
-    rmax = fmaxf(rmax, s2);
-    gmax = fmaxf(gmax, mx);
-    if (a.rowmax_G && lane == 0) a.rowmax_G[(long long)b * a.m + r] = isfinite(mx) ? mx : 0.f;
-  }
-  bad = __any_sync(0xffffffffu, bad);
-  if (lane == 0) {
-    if (isfinite(gmax)) atomic_max_nonneg(&a.mstat[b].gmax, gmax);
-    if (isfinite(rmax)) atomic_max_nonneg(&a.mstat[b].rownorm2_max, rmax);
-    if (bad) {
-      a.stats[a.roots2[2 * b]].nonfinite = 1;
-      a.stats[a.roots2[2 * b + 1]].nonfinite = 1;
-    }
-  }
-}
-
-// 32 x 32 tiles: writes the engine copies of G and G^T.
-template <int E>
-__global__ void __launch_bounds__(256) prep_split_kernel(PrepArgs a) {
-  __shared__ float tile[32][33];
-  __shared__ float cmax[8][32];
+// fp64 engine: 32 x 32 tiles, double copies of G and G^T and the non-finite check.
+__global__ void __launch_bounds__(256) prep_f64_kernel(PrepArgs a) {
+  __shared__ double tile[32][33];
   const int b = blockIdx.z;
   const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
   const void* g = a.g[b];
-  float cm = 0.f;
+  int bad = 0;
   for (int q = ty; q < 32; q += 8) {
     const int r = r0 + q, c = c0 + tx;
-    float v = 0.f;
+    double v = 0.0;
     if (r < a.m && c < a.n) {
-      v = load_grad(g, a.dtype, (long long)r * a.n + c);
-      if constexpr (E == ENGINE_F64) a.Gd[((long long)b * a.m + r) * a.n + c] = (double)v;
-      else a.Gf[((long long)b * a.m + r) * a.ldn + c] = v;
+      const float f = load_grad(g, a.dtype, (long long)r * a.n + c);
+      if (!isfinite(f)) bad = 1;
+      v = (double)f;
+      f64_store(a.G, b, r, c, v);
     }
     tile[q][tx] = v;
-    if (isfinite(v)) cm = fmaxf(cm, fabsf(v));
-  }
-  if constexpr (E == ENGINE_TC) {
-    cmax[ty][tx] = cm;
-    __syncthreads();
-    if (ty == 0 && c0 + tx < a.n) {
-      float m = cmax[0][tx];
-      for (int q = 1; q < 8; ++q) m = fmaxf(m, cmax[q][tx]);
-      atomic_max_nonneg(&a.rowmax_GT[(long long)b * a.n + c0 + tx], m);
-    }
   }
   __syncthreads();
   for (int q = ty; q < 32; q += 8) {
-    const int c = c0 + q, r = r0 + tx;   // output row c of G^T, column r
-    if (c < a.n && r < a.m) {
-      const float v = tile[tx][q];
-      if constexpr (E == ENGINE_F64) a.GTd[((long long)b * a.n + c) * a.m + r] = (double)v;
-      else a.GTf[((long long)b * a.n + c) * a.ldm + r] = v;
-    }
+    const int c = c0 + q, r = r0 + tx;
+    if (c < a.n && r < a.m) f64_store(a.GT, b, c, r, tile[tx][q]);
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) {
+    a.stats[a.roots2[2 * b]].nonfinite = 1;
+    a.stats[a.roots2[2 * b + 1]].nonfinite = 1;
   }
 }
 
-// fp32 rows -> per-row-scaled digits: sigma_i = smallest power of two >= max_j |x_ij|.
-struct SliceArgs {
-  const float* src; long long src_bstride; int src_ld;
-  const int* root_of;       // may be null; else batch entry -> root id, and converged roots are skipped
-  const RootStat* stats;
-  const float* rowmax;      // [b][rows]
-  float* rowscale;          // [b][rows] out
-  Plane dst;                // digit form (scale unused)
-  int rows, cols;
-};
+// tcgen05 engine: one 128 x 128 tile of G per block (staged in shared memory),
+// written as digits of G (rows of the tile, one block) and of G^T (columns of
+// the tile become rows, one block), plus the non-finite check.
+constexpr int PREP_LD = 129;
+constexpr int PREP_SMEM = 128 * PREP_LD * 4;
 
-__device__ __forceinline__ float pow2_ceil(float x) {
-  if (!(x > 0.f) || !isfinite(x)) return 1.f;
-  int e;
-  const float f = frexpf(x, &e);          // x = f 2^e, f in [0.5, 1)
-  return f == 0.5f ? x : ldexpf(1.f, e);
-}
-
-__device__ __forceinline__ void digits4(float v, float inv, float (&d)[4]) {
-  float r = v * inv * 128.0f;
-  float w = 1.0f;
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    const float q = rintf(r);
-    d[s] = q * w;                // exact: |q| <= 129, power-of-two weight
-    r = (r - q) * 128.0f;
-    w *= 0.0078125f;
-  }
-}
-
-__global__ void __launch_bounds__(256) slice_rows_kernel(SliceArgs a) {
-  const int b = blockIdx.y;
-  if (a.root_of && a.stats[a.root_of[b]].done) return;   // no further product reads these digits
+__global__ void __launch_bounds__(256) prep_tc_kernel(PrepArgs a) {
+  extern __shared__ float tile[];   // [128][PREP_LD]
+  const int b = blockIdx.z;
+  const int r0 = blockIdx.y * 128, c0 = blockIdx.x * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = blockIdx.x * 8 + warp; r < a.rows; r += gridDim.x * 8) {
-    const float sigma = pow2_ceil(a.rowmax[(long long)b * a.rows + r]);
-    if (lane == 0) a.rowscale[(long long)b * a.rows + r] = sigma;
-    const float inv = 1.0f / sigma;          // exact: sigma is a power of two
-    const float* src = a.src + (long long)b * a.src_bstride + (long long)r * a.src_ld;
-    const long long o = (long long)b * a.dst.bstride + (long long)r * a.dst.ld;
-    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.dst.hi) + o;
-    const int nv = (a.cols / 4) * 4;
-    // 4 columns per lane (16 B in, 8 B out per plane), two such groups per
-    // iteration with both loads issued before any store, so that each lane keeps
-    // 32 B in flight
-    for (int c = lane * 4; c < nv; c += 256) {
-      float4 v[2];
-      const bool two = c + 128 < nv;
-      v[0] = *reinterpret_cast<const float4*>(src + c);
-      if (two) v[1] = *reinterpret_cast<const float4*>(src + c + 128);
+  const void* g = a.g[b];
+  int bad = 0;
+  for (int i = warp; i < 128; i += 8) {
+    const int r = r0 + i;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (h == 1 && !two) break;
-        const int cc = c + h * 128;
-        float d0[4], d1[4], d2[4], d3[4];
-        digits4(v[h].x, inv, d0);
-        digits4(v[h].y, inv, d1);
-        digits4(v[h].z, inv, d2);
-        digits4(v[h].w, inv, d3);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          if (s < a.dst.S) {
-            __nv_bfloat162 lo2 = __floats2bfloat162_rn(d0[s], d1[s]);
-            __nv_bfloat162 hi2 = __floats2bfloat162_rn(d2[s], d3[s]);
-            uint2 pk;
-            pk.x = *reinterpret_cast<uint32_t*>(&lo2);
-            pk.y = *reinterpret_cast<uint32_t*>(&hi2);
-            *reinterpret_cast<uint2*>(dst + s * a.dst.pstride + cc) = pk;
-          }
-        }
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + lane + 32 * u;
+      float v = 0.f;
+      if (r < a.m && c < a.n) {
+        v = load_grad(g, a.dtype, (long long)r * a.n + c);
+        if (!isfinite(v)) bad = 1;
       }
+      tile[i * PREP_LD + lane + 32 * u] = v;
     }
-    for (int c = nv + lane; c < a.cols; c += 32) digits_store(a.dst, o + c, src[c], inv);
+  }
+  __syncthreads();
+  for (int i = warp; i < 128; i += 8) {
+    float v[4];
+    if (r0 + i < a.m) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = tile[i * PREP_LD + lane + 32 * u];
+      tc_store_row128(a.G, b, r0 + i, c0, a.n, v);
+    }
+    if (c0 + i < a.n) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = tile[(lane + 32 * u) * PREP_LD + i];
+      tc_store_row128(a.GT, b, c0 + i, r0, a.m, v);
+    }
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) {
+    a.stats[a.roots2[2 * b]].nonfinite = 1;
+    a.stats[a.roots2[2 * b + 1]].nonfinite = 1;
   }
 }
 
@@ -198,12 +114,13 @@ struct RootArgs {
   int d;
   float eps;
   IterCtl ctl;
-  double alpha0, beta0;      // first step polynomial T_0 = alpha0 I - beta0 M_0
+  double alpha0, beta0;      // first step polynomial T_0 = alpha0 I - beta0 M_0 (linear first step)
+  int write_x1;              // 1: the start also writes X_1 = T_0 (linear first step)
   // engine planes
-  Plane M0, X1;              // start outputs (fp32 form in the tcgen05 engine)
-  Plane X[2];                // finalize input (X buffer kfinal & 1)
-  Plane Xf;                  // finalize output in engine format (step), or unused
-  float* const* dst;         // finalize output to caller fp32 (inv_root), or null
+  Plane M0, X1;              // start outputs
+  Plane X[2];                // finish input (X buffer kfinal & 1)
+  Plane Xf;                  // finish output in engine format (step), or unused
+  float* const* dst;         // finish output to caller fp32 (inv_root), or null
 };
 
 __global__ void __launch_bounds__(256) root_stats_kernel(RootArgs a) {
@@ -326,77 +243,111 @@ __global__ void root_scalar_kernel(RootArgs a, int nb) {
   st->status = bad ? PRECOND_ENONFINITE : PRECOND_OK;
   st->sac = bad ? 0.f : (float)(0.5 / (t * c));
   st->seps = bad ? 0.f : (float)(eps / c);
+  st->sac_d = bad ? 0.0 : 0.5 / (t * c);
+  st->seps_d = bad ? 0.0 : eps / c;
   st->fin = bad ? 0.f : (float)pow(c, -1.0 / (double)a.ctl.p);
 }
 
-// M_0 = A_hat / c and X_1 = X_0 T_0 = T_0 = alpha0 I - beta0 M_0.  A block owns
-// 32-row strips of one root and walks their 32 x 32 tiles, so it holds the
-// strips' row maxima itself and stores them once (no atomics).
-template <int E>
-__global__ void __launch_bounds__(256) root_init_kernel(RootArgs a) {
+// ---------------------------------------------------------------------------
+// Start: M_0 = A_hat / c (exactly symmetric: (A + A^T)/2 / tr / c + eps / c I)
+// and, for a linear first step, X_1 = X_0 T_0 = T_0 = alpha0 I - beta0 M_0.
+// ---------------------------------------------------------------------------
+// fp64 engine: a block owns 32-row strips and walks their 32 x 32 tiles.
+__global__ void __launch_bounds__(256) root_init_f64_kernel(RootArgs a) {
   const int b = blockIdx.z;
   const RootStat* st = &a.stats[a.root_of[b]];
   if (st->done) return;                         // non-finite input or trace
-  const float s_ac = st->sac, s_eps = st->seps;
-  const float al = (float)a.alpha0, be = (float)a.beta0;
+  const double s_ac = st->sac_d, s_eps = st->seps_d;
+  const double al = a.alpha0, be = a.beta0;
   const float* A = a.src[b];
-  __shared__ float tt[2][32][33];
+  __shared__ float tt[32][33];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int T = (a.d + 31) / 32;
   for (int strip = blockIdx.x; strip < T; strip += gridDim.x) {
     const int r0 = strip * 32;
-    float mx[4] = {0.f, 0.f, 0.f, 0.f}, xx[4] = {0.f, 0.f, 0.f, 0.f};   // rows r0 + ty + 8 j
-    for (int c0 = 0; c0 < a.d; c0 += 64) {     // two 32-column tiles per pass, loads first
-      __syncthreads();                          // the previous pass's reads of tt are done
-      float av[2][4];
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int q = ty + 8 * j;
-          const int rm = c0 + 32 * t + q, cm = r0 + tx;             // mirrored tile (rows c0.., cols r0..)
-          tt[t][q][tx] = (rm < a.d && cm < a.d) ? A[(long long)rm * a.d + cm] : 0.f;
-          const int r = r0 + q, col = c0 + 32 * t + tx;             // this strip's own elements
-          av[t][j] = (r < a.d && col < a.d) ? A[(long long)r * a.d + col] : 0.f;
-        }
+    for (int c0 = 0; c0 < a.d; c0 += 32) {
       __syncthreads();
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int q = ty + 8 * j;
-          const int r = r0 + q, col = c0 + 32 * t + tx;
-          if (r < a.d && col < a.d) {
-            const bool dgl = (r == col);
-            // M_0 = ((A + A^T)/2 / tr + eps I) / c, exactly symmetric
-            const float m0 = fmaf(av[t][j] + tt[t][tx][q], s_ac, dgl ? s_eps : 0.f);
-            const float x1 = (dgl ? al : 0.f) - be * m0;
-            plane_store<E>(a.M0, b, r, col, m0);
-            plane_store<E>(a.X1, b, r, col, x1);
-            mx[j] = fmaxf(mx[j], fabsf(m0));
-            xx[j] = fmaxf(xx[j], fabsf(x1));
-          }
-        }
-    }
-    if (E == ENGINE_TC) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int r = r0 + ty + 8 * j;
-        const float m = warp_max(mx[j]), x = warp_max(xx[j]);
-        if (tx == 0 && r < a.d) {
-          a.M0.rowmax[(long long)b * a.d + r] = m;
-          a.X1.rowmax[(long long)b * a.d + r] = x;
+      for (int q = ty; q < 32; q += 8) {
+        const int rm = c0 + q, cm = r0 + tx;    // mirrored tile (rows c0.., cols r0..)
+        tt[q][tx] = (rm < a.d && cm < a.d) ? A[(long long)rm * a.d + cm] : 0.f;
+      }
+      __syncthreads();
+      for (int q = ty; q < 32; q += 8) {
+        const int r = r0 + q, col = c0 + tx;
+        if (r < a.d && col < a.d) {
+          const bool dgl = (r == col);
+          const double m0 = ((double)A[(long long)r * a.d + col] + (double)tt[tx][q]) * s_ac + (dgl ? s_eps : 0.0);
+          f64_store(a.M0, b, r, col, m0);
+          if (a.write_x1) f64_store(a.X1, b, r, col, (dgl ? al : 0.0) - be * m0);
         }
       }
     }
   }
 }
 
-// Result = sym(X_kfinal) * c^(-1/p): to the engine plane Xf (step) or caller fp32
-// (inv_root).  Blocks own 32-row strips, as in the start.
-template <int E>
-__global__ void __launch_bounds__(256) root_finish_kernel(RootArgs a) {
-  __shared__ float tile[2][32][33];
+// tcgen05 engine: block (column block J, 32-row strip, root); each warp owns 4
+// rows of the strip and the strip's transposed source block sits in shared memory.
+// M_0 is formed as an unevaluated fp32 pair hi + lo (exact sum of the two source
+// entries, product with the two-term scalar, fused error terms): its digits then
+// hold it to the 27 bits of the representation instead of fp32's 24, which is
+// what resolves eigenvalues at eps / c next to ones near 1.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+__global__ void __launch_bounds__(256) root_init_tc_kernel(RootArgs a) {
+  const int b = blockIdx.z;
+  const RootStat* st = &a.stats[a.root_of[b]];
+  if (st->done) return;
+  const float sh = (float)st->sac_d, sl = (float)(st->sac_d - (double)sh);
+  const float eh = (float)st->seps_d, el = (float)(st->seps_d - (double)eh);
+  const float al = (float)a.alpha0, be = (float)a.beta0;
+  const float* A = a.src[b];
+  __shared__ float tt[128][33];                 // A[c0 + i][r0 + j]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = blockIdx.x * 128, r0 = blockIdx.y * 32;
+  for (int i = warp; i < 128; i += 8) {
+    const int rm = c0 + i, cm = r0 + lane;
+    tt[i][lane] = (rm < a.d && cm < a.d) ? A[(long long)rm * a.d + cm] : 0.f;
+  }
+  __syncthreads();
+  for (int q = warp; q < 32; q += 8) {
+    const int r = r0 + q;
+    if (r >= a.d) break;
+    float mh[4], ml[4], x1[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int cl = lane + 32 * u, col = c0 + cl;
+      const bool dgl = (r == col);
+      const float av = (col < a.d) ? A[(long long)r * a.d + col] : 0.f;
+      float s, e;
+      two_sum(av, tt[cl][q], s, e);                 // A_rc + A_cr exactly
+      const float p = s * sh;
+      float lo = fmaf(s, sl, fmaf(e, sh, fmaf(s, sh, -p)));
+      float hi = p;
+      if (dgl) {
+        float s2, e2;
+        two_sum(p, eh, s2, e2);
+        hi = s2;
+        lo += e2 + el;
+      }
+      mh[u] = hi;
+      ml[u] = lo;
+      x1[u] = (dgl ? al : 0.f) - be * (hi + lo);
+    }
+    tc_store_row128_pair(a.M0, b, r, c0, a.d, mh, ml);
+    if (a.write_x1) tc_store_row128(a.X1, b, r, c0, a.d, x1);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Finish: result = sym(X_kfinal) c^(-1/p), to the engine plane Xf (step) or
+// the caller's fp32 (inv_root).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) root_finish_f64_kernel(RootArgs a) {
+  __shared__ float tile[32][33];
   const int b = blockIdx.z;
   const RootStat* st = &a.stats[a.root_of[b]];
   if (st->status == PRECOND_ENONFINITE || st->kfinal < 1) return;
@@ -406,48 +357,62 @@ __global__ void __launch_bounds__(256) root_finish_kernel(RootArgs a) {
   const int T = (a.d + 31) / 32;
   for (int strip = blockIdx.x; strip < T; strip += gridDim.x) {
     const int r0 = strip * 32;
-    float mx[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int c0 = 0; c0 < a.d; c0 += 64) {     // two 32-column tiles per pass, loads first
-      __syncthreads();                          // the previous pass's reads are done
-      float xv[2][4];
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int q = ty + 8 * j;
-          const int rm = c0 + 32 * t + q, cm = r0 + tx;             // transposed tile (rows c0.., cols r0..)
-          tile[t][q][tx] = (rm < a.d && cm < a.d) ? (float)plane_load<E>(X, b, rm, cm) : 0.f;
-          const int r = r0 + q, col = c0 + 32 * t + tx;
-          xv[t][j] = (r < a.d && col < a.d) ? (float)plane_load<E>(X, b, r, col) : 0.f;
-        }
+    for (int c0 = 0; c0 < a.d; c0 += 32) {
       __syncthreads();
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int q = ty + 8 * j;
-          const int r = r0 + q, col = c0 + 32 * t + tx;
-          if (r < a.d && col < a.d) {
-            const float v = 0.5f * (xv[t][j] + tile[t][tx][q]) * f;
-            if (a.dst) a.dst[b][(long long)r * a.d + col] = v;
-            else plane_store<E>(a.Xf, b, r, col, (double)v);
-            mx[j] = fmaxf(mx[j], fabsf(v));
-          }
+      for (int q = ty; q < 32; q += 8) {
+        const int rm = c0 + q, cm = r0 + tx;
+        tile[q][tx] = (rm < a.d && cm < a.d) ? (float)f64_load(X, b, rm, cm) : 0.f;
+      }
+      __syncthreads();
+      for (int q = ty; q < 32; q += 8) {
+        const int r = r0 + q, col = c0 + tx;
+        if (r < a.d && col < a.d) {
+          const float v = 0.5f * ((float)f64_load(X, b, r, col) + tile[tx][q]) * f;
+          if (a.dst) a.dst[b][(long long)r * a.d + col] = v;
+          else f64_store(a.Xf, b, r, col, (double)v);
         }
-    }
-    if (E == ENGINE_TC && !a.dst) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int r = r0 + ty + 8 * j;
-        const float m = warp_max(mx[j]);
-        if (tx == 0 && r < a.d) a.Xf.rowmax[(long long)b * a.d + r] = m;
       }
     }
   }
 }
 
-// X_1 = X_0 T_0 = alpha I + E_0 (X_0 = I) for quadratic steps, E_0 = T_0 - alpha I:
-// one warp per row, row maxima stored directly.  Converged or failed roots skip.
+__global__ void __launch_bounds__(256) root_finish_tc_kernel(RootArgs a) {
+  const int b = blockIdx.z;
+  const RootStat* st = &a.stats[a.root_of[b]];
+  if (st->status == PRECOND_ENONFINITE || st->kfinal < 1) return;
+  const Plane& X = a.X[st->kfinal & 1];
+  const float f = st->fin;
+  __shared__ float tt[128][33];                 // X[c0 + i][r0 + j]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = blockIdx.x * 128, r0 = blockIdx.y * 32;
+  for (int i = warp; i < 128; i += 8) {
+    const int rm = c0 + i, cm = r0 + lane;
+    tt[i][lane] = (rm < a.d && cm < a.d) ? tc_load(X, b, rm, cm) : 0.f;
+  }
+  __syncthreads();
+  for (int q = warp; q < 32; q += 8) {
+    const int r = r0 + q;
+    if (r >= a.d) break;
+    float x[4];
+    tc_load_row128(X, b, r, c0, a.d, x);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = 0.5f * (x[u] + tt[lane + 32 * u][q]) * f;
+    if (a.dst) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int col = c0 + lane + 32 * u;
+        if (col < a.d) a.dst[b][(long long)r * a.d + col] = x[u];
+      }
+    } else {
+      tc_store_row128(a.Xf, b, r, c0, a.d, x);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// X_1 = X_0 T_0 = alpha I + E_0 (X_0 = I) for quadratic steps, E_0 = T_0 - alpha I.
+// Converged or failed roots skip.
+// ---------------------------------------------------------------------------
 struct ShiftArgs {
   Plane src, dst;
   const int* root_of;
@@ -456,58 +421,71 @@ struct ShiftArgs {
   float alpha;
 };
 
-template <int E>
-__global__ void __launch_bounds__(256) shift_identity_kernel(ShiftArgs a) {
+__global__ void __launch_bounds__(256) shift_identity_f64_kernel(ShiftArgs a) {
   const int b = blockIdx.y;
   if (a.stats[a.root_of[b]].done) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = blockIdx.x * 8 + warp; r < a.d; r += gridDim.x * 8) {
-    float mx = 0.f;
-    int c0 = 0;
-    if (E == ENGINE_TC) {
-      // fp32 rows start 256 B aligned (ld is a multiple of 64): 16-byte vectors, two in flight
-      const float* src = a.src.f32 + (long long)b * a.src.bstride + (long long)r * a.src.ld;
-      float* dst = a.dst.f32 + (long long)b * a.dst.bstride + (long long)r * a.dst.ld;
-      const int nv = (a.d / 4) * 4;
-      for (int c = lane * 4; c < nv; c += 256) {
-        float4 v[2];
-        const bool two = c + 128 < nv;
-        v[0] = *reinterpret_cast<const float4*>(src + c);
-        if (two) v[1] = *reinterpret_cast<const float4*>(src + c + 128);
+  for (int r = blockIdx.x * 8 + warp; r < a.d; r += gridDim.x * 8)
+    for (int c = lane; c < a.d; c += 32)
+      f64_store(a.dst, b, r, c, f64_load(a.src, b, r, c) + (r == c ? (double)a.alpha : 0.0));
+}
+
+// tcgen05 engine: one warp per (row, 128-column block).  Blocks away from the
+// diagonal are the same matrix: digits and scale are copied bit for bit; the
+// diagonal block is rebuilt with alpha added and a fresh scale.
+__global__ void __launch_bounds__(256) shift_identity_tc_kernel(ShiftArgs a) {
+  const int b = blockIdx.z;
+  if (a.stats[a.root_of[b]].done) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = blockIdx.x * 128;
+  const int r = blockIdx.y * 8 + warp;
+  if (r >= a.d) return;
+  if (r >= c0 && r < c0 + 128) {
+    float v[4];
+    tc_load_row128(a.src, b, r, c0, a.d, v);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (h == 1 && !two) break;
-          const int cc = c + h * 128;
-          float4 w = v[h];
-          if (r >= cc && r < cc + 4) (&w.x)[r - cc] += a.alpha;
-          *reinterpret_cast<float4*>(dst + cc) = w;
-          mx = fmaxf(mx, fmaxf(fmaxf(fabsf(w.x), fabsf(w.y)), fmaxf(fabsf(w.z), fabsf(w.w))));
-        }
-      }
-      c0 = nv;
+    for (int u = 0; u < 4; ++u)
+      if (c0 + lane + 32 * u == r) v[u] += a.alpha;
+    tc_store_row128(a.dst, b, r, c0, a.d, v);
+  } else {
+    const long long so = (long long)b * a.src.bstride + (long long)r * a.src.ld;
+    const long long dof = (long long)b * a.dst.bstride + (long long)r * a.dst.ld;
+    const uint16_t* s = reinterpret_cast<const uint16_t*>(a.src.hi);
+    uint16_t* dd = reinterpret_cast<uint16_t*>(a.dst.hi);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + lane + 32 * u;
+      if (c < a.d)
+#pragma unroll
+        for (int p = 0; p < 3; ++p) dd[dof + p * a.dst.pstride + c] = s[so + p * a.src.pstride + c];
     }
-    for (int c = c0 + lane; c < a.d; c += 32) {
-      const float v = (float)plane_load<E>(a.src, b, r, c) + (r == c ? a.alpha : 0.f);
-      plane_store<E>(a.dst, b, r, c, (double)v);
-      mx = fmaxf(mx, fabsf(v));
-    }
-    if (E == ENGINE_TC) {
-      mx = warp_max(mx);
-      if (lane == 0) a.dst.rowmax[(long long)b * a.d + r] = mx;
-    }
+    if (lane == 0) *tc_scale_ptr(a.dst, b, c0 / DIG_BLK, r) = *tc_scale_ptr(a.src, b, c0 / DIG_BLK, r);
   }
 }
 
-// Caller fp32 -> engine plane (GEMM self-test inputs).
-template <int E>
-__global__ void f32_to_plane_kernel(const float* src, Plane p, int rows, int cols) {
+// ---------------------------------------------------------------------------
+// Conversions for the self-test and the read-backs
+// ---------------------------------------------------------------------------
+// Caller fp32 (rows x cols, dense) -> digits: one warp per (row, block).
+__global__ void __launch_bounds__(256) f32_to_tc_kernel(const float* src, Plane p, int rows, int cols) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = blockIdx.x * 128;
+  const int r = blockIdx.y * 8 + warp;
+  if (r >= rows) return;
+  float v[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int c = c0 + lane + 32 * u;
+    v[u] = c < cols ? src[(long long)r * cols + c] : 0.f;
+  }
+  tc_store_row128(p, 0, r, c0, cols, v);
+}
+
+__global__ void f32_to_f64_kernel(const float* src, Plane p, int rows, int cols) {
   const long long n = (long long)rows * cols;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    plane_store<E>(p, 0, i / cols, i % cols, (double)src[i]);
-    if (E == ENGINE_TC && p.rowmax) atomic_max_nonneg(&p.rowmax[i / cols], fabsf(src[i]));
-  }
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    f64_store(p, 0, i / cols, i % cols, (double)src[i]);
 }
-
 
 // Engine plane -> caller fp32 (debug / test read-back of a root).
 template <int E>
@@ -515,7 +493,7 @@ __global__ void plane_to_f32_kernel(Plane p, int b, int rows, int cols, float* d
   const long long n = (long long)rows * cols;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
     const long long r = i / cols, c = i % cols;
-    dst[i] = (float)plane_load<E>(p, b, r, c);
+    dst[i] = (E == ENGINE_F64) ? (float)f64_load(p, b, r, c) : tc_load(p, b, r, c);
   }
 }
 

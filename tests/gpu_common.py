@@ -14,14 +14,17 @@ def to_dev(a, dtype=None):
     return t.to(dtype) if dtype is not None else t
 
 
-def run_steps(shapes, grads_per_step, dtype, beta, eps, power, engine=0, small_dim=0, check_roots=True,
+def run_steps(shapes, grads_per_step, dtype, beta, eps, power, engine=0, small_dim=None, check_roots=True,
               extra_opts=None):
     """Run len(grads_per_step) steps on the GPU and in the oracle; return the
     worst relative Frobenius errors (U, X_L, X_R) and the last stats."""
     import torch
     import shampoo_roots_gb300 as sr
     tdt = torch.bfloat16 if dtype == synth.BF16 else torch.float32
-    pc = sr.Preconditioner(0, engine=engine, small_dim=small_dim, **(extra_opts or {}))
+    opts = dict(extra_opts or {})
+    if small_dim is not None:
+        opts["small_dim"] = small_dim
+    pc = sr.Preconditioner(0, engine=engine, **opts)
     L = [torch.zeros((m, m), device="cuda") for m, _ in shapes]
     R = [torch.zeros((n, n), device="cuda") for _, n in shapes]
     st = oracle.OracleState(shapes)

@@ -229,16 +229,22 @@ def test_tiny_and_degenerate_shapes(engine):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("engine", [1, 2])
+@pytest.mark.parametrize("engine", [0, 1])
 def test_tiny_and_degenerate_shapes_root_of_the_fp32_state(engine):
-    """The same tiny and rank-deficient shapes at the workloads' eps = 1e-6.
+    """The same tiny and rank-deficient shapes at the workloads' eps = 1e-6,
+    through the default engine choice (these sides are all <= 64, so the fp64
+    engine) and the fp64 engine forced.
 
     Here the oracle roots the GPU's own fp32 EMA state (read back after each
     step and upcast exactly), so the state's rounding, which the caller's fp32
     layout fixes, is not part of the comparison: what is compared is the root
     of the Gram the step actually held ("Sharding EMA-Gram eigensolves",
     Background: rescale, add eps to the eigenvalues, raise to the power,
-    reconstruct), element by element, and the update built from it."""
+    reconstruct), element by element, and the update built from it.  A rank-1
+    Gram of side 3 has eigenvalues 1e-6 below entries of order 1: its root needs
+    the start matrix to about 2^-30, which the fp64 engine (and its fp64 start)
+    gives and the tcgen05 engine's 27-bit digits do not; that engine is checked
+    on these shapes at eps = 1e-4 above."""
     import torch
     import shampoo_roots_gb300 as sr
     shapes = [(1, 5), (3, 1), (2, 2), (17, 33)]
