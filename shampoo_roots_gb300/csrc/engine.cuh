@@ -287,7 +287,8 @@ __device__ __forceinline__ void epi_m_finish(const Epi& e, int b, double part, i
   for (unsigned int i = lane; i < e.tiles_per_entry; i += 32) acc += *((volatile double*)&parts[i]);
   acc = warp_sum(acc);
   if (lane != 0) return;
-  const double r = sqrt(acc) / sqrt((double)d);
+  // the stop decision needs no fp64 root (slow, long code on this GPU): fp32 of the fp64 sum
+  const double r = (double)sqrtf((float)(acc / (double)d));
   const int kdone = e.k + 1;
   st->iters = kdone;
   st->kfinal = kdone;

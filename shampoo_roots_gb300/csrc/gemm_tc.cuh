@@ -27,11 +27,10 @@
 // terms) and writes it in its consumer's format: digits with the tile's
 // per-(row, block) scales for products that feed further products (and the
 // mirrored tile for symmetric products, so results are exactly symmetric), the
-// caller's fp32 state for the Gram EMA, or the caller's update.  Digit tiles go
-// in and out through one 32 KB shared staging tile, one digit plane at a time,
-// moved by TMA (128-byte swizzle): the element-wise input is loaded by TMA
-// (prefetched into L2 when the tile starts) and every output plane is stored by
-// TMA, so no warp issues row-scattered global accesses.
+// caller's fp32 state for the Gram EMA, or the caller's update.  Digit outputs
+// leave through a 16 KB shared staging area, one plane of half a tile per
+// round, stored by TMA (128-byte swizzle), so no warp issues row-scattered
+// global stores; the element-wise input is taken from the operand ring.
 //
 // Every mbarrier wait is bounded.  On a time-out the kernel records an error
 // word and raises a shared abort flag: every other wait then gives up at once,
@@ -67,17 +66,15 @@ struct TcGemmArgs {
 struct TcSmem {
   static constexpr int PLANE_BYTES = TC_BM * TC_BK * 2;                 // 8 KB (A and B tiles alike)
   static constexpr int STAGE_BYTES = 2 * DIGITS * PLANE_BYTES;          // 48 KB
-  static constexpr int STAGES = 3;
+  static constexpr int STAGES = 4;
   static constexpr int RING = STAGES * STAGE_BYTES;
-  static constexpr int OFF_STG = RING;                                  // staging: 3 planes x 2 boxes of 64 x 64 bf16
-  static constexpr int STG_BYTES = DIGITS * TC_BM * 64 * 2;             // 48 KB: half a tile, all planes
-  static constexpr int XP_LD = 17;                                      // transpose scratch row (floats)
-  static constexpr int XP_FLOATS = 32 * XP_LD;                          // per epilogue warp
-  static constexpr int OFF_XP = OFF_STG + STG_BYTES;
-  static constexpr int OFF_SB = OFF_XP + EPI_WARPS * XP_FLOATS * 4;     // per warp: B scales of 2 chunks
+  static constexpr int XS_LD = 17;                                      // per-warp scratch row (32-bit words)
+  static constexpr int OFF_XS = RING;                                   // per warp: 32 rows x 16 words
+  static constexpr int OFF_SB = OFF_XS + EPI_WARPS * 32 * XS_LD * 4;    // per warp: B scales of 2 chunks
   static constexpr int OFF_RMAX = OFF_SB + EPI_WARPS * 128 * 4;         // [2 halves][128 rows]
   static constexpr int OFF_CMAX = OFF_RMAX + 2 * TC_BM * 4;             // [4 quadrants][128 columns]
-  static constexpr int OFF_RED = OFF_CMAX + 4 * TC_BN * 4;              // [8] doubles
+  static constexpr int OFF_INV = OFF_CMAX + 4 * TC_BN * 4;              // [128] row and [128] column 1/sigma
+  static constexpr int OFF_RED = OFF_INV + (TC_BM + TC_BN) * 4;         // [8] doubles
   static constexpr int OFF_BAR = OFF_RED + EPI_WARPS * 8;
   static constexpr int BAR_BYTES = 256;
   static constexpr int BYTES = 1024 /*align*/ + OFF_BAR + BAR_BYTES;
@@ -141,26 +138,10 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
-// TMA store of a box from shared memory (bulk group), its commit and waits.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
-               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y), "r"(z) : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// Order this thread's generic shared-memory accesses before later async-proxy (TMA) ones.
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];"
-               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z) : "memory");
-}
-// Staging area of one epilogue round: digit plane p, box bx (two TMA boxes of
-// {64 columns, 64 rows} per plane, 8 KB each), row rr < 64 of the box; the
-// 16-byte chunks of a 128-byte row are XOR-swizzled by rr % 8 (the layout of a
-// TMA box with 128-byte swizzle).  Offset of the chunk holding column cc < 64.
-__device__ __forceinline__ uint32_t stg_chunk(int p, int bx, int rr, int cc) {
-  return (uint32_t)(p * 16384 + bx * 8192 + rr * 128 + (((cc >> 3) ^ (rr & 7)) << 4));
+// Byte offset of element (row, k), k < 32, of a ring operand tile (TMA box {32, 128},
+// 64-byte swizzle: the 16-byte chunk index XOR (row / 2) % 4).
+__device__ __forceinline__ uint32_t ring_off(int row, int k) {
+  return (uint32_t)(row * 64 + ((((k >> 3) ^ ((row >> 1) & 3)) << 4) | ((k & 7) << 1)));
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -234,6 +215,32 @@ __device__ __forceinline__ float opaque(float x) {
   asm volatile("mov.b32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Store 16 fp32 columns of this warp's 32 lanes into tensor memory.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])),
+        "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+        "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// acc[0..63] <- acc[16..63], acc[0..15]: the epilogue walks a thread's 64 columns in
+// four groups of 16 inside loops that are not unrolled (so their bodies exist once
+// in the instruction stream), always working on acc[0..15] and rotating after each
+// group; four rotations restore the order.  Register indices stay compile-time.
+__device__ __forceinline__ void rotate16(float (&a)[64]) {
+  float t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t[i] = a[i];
+#pragma unroll
+  for (int i = 0; i < 48; ++i) a[i] = a[i + 16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[48 + i] = t[i];
+}
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }   // the 8 epilogue warps
 // Barrier of the 8 epilogue warps that also returns the OR of `v` over them (a
 // decision every epilogue thread takes the same way).
@@ -252,14 +259,10 @@ __host__ __device__ constexpr int pair_a(int i) { return i == 0 ? 0 : i == 1 ? 0
 __host__ __device__ constexpr int pair_b(int i) { return i == 0 ? 0 : i == 1 ? 1 : i == 2 ? 0 : i == 3 ? 2 : i == 4 ? 1 : 0; }
 
 // ----------------------------------------------------------------- kernel
-// Tensor maps: digit plane s of A is a[s], of B is b[s] (boxes {32, 128}, 64-byte
-// swizzle); of the output c[s] and of the element-wise input in[s] (boxes
-// {64, 128}, 128-byte swizzle; zero when the epilogue has none).
+// Tensor maps: digit plane s of A is a[s], of B is b[s] (boxes {32, 128}, 64-byte swizzle).
 struct TcMaps {
   CUtensorMap a[DIGITS];
   CUtensorMap b[DIGITS];
-  CUtensorMap c[DIGITS];
-  CUtensorMap in[DIGITS];
 };
 
 // Tile order within one batch entry: groups of TC_GROUP tile-rows, and inside a
@@ -350,6 +353,13 @@ __device__ __forceinline__ void store_digits16(const Plane& p, long long o, cons
 }
 
 // Persistent: CTA c takes tiles c, c + gridDim.x, ... of every batch entry.
+//
+// Element-wise input.  Every product with one (EPI_AFF, EPI_M) is launched with
+// that input equal to its first operand A, so the input tile (rows tile_m..,
+// columns tile_n..) is A's K chunk tj, which passes through the operand ring
+// anyway: the drain warps read it from the ring stages of that chunk and add
+// it to their sums, and the producer refills those stages only after they have
+// (barrier in_done).
 __global__ void __launch_bounds__(TC_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
   using SM = TcSmem;
@@ -357,12 +367,12 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  uint8_t* stg = gbase + SM::OFF_STG;
-  const uint32_t stg_s = base + SM::OFF_STG;
-  float* xp_all = reinterpret_cast<float*>(gbase + SM::OFF_XP);
+  uint32_t* xs_all = reinterpret_cast<uint32_t*>(gbase + SM::OFF_XS);
   float* sb_all = reinterpret_cast<float*>(gbase + SM::OFF_SB);
   float* rmax = reinterpret_cast<float*>(gbase + SM::OFF_RMAX);     // [2][128]
   float* cmax = reinterpret_cast<float*>(gbase + SM::OFF_CMAX);     // [4][128]
+  float* invr = reinterpret_cast<float*>(gbase + SM::OFF_INV);      // [128] 1 / sigma of the output rows
+  float* invc = invr + TC_BM;                                       // [128] of the mirrored tile's rows
   double* red = reinterpret_cast<double*>(gbase + SM::OFF_RED);
   uint8_t* tail = gbase + SM::OFF_BAR;
   const uint32_t bars = smem_u32(tail);
@@ -371,7 +381,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
   auto chunk_full = [&](uint32_t b) { return bars + 8u * (2 * SM::STAGES + b); };
   auto chunk_empty = [&](uint32_t b) { return bars + 8u * (2 * SM::STAGES + 2 + b); };
   const uint32_t final_bar = bars + 8u * (2 * SM::STAGES + 4);
-  const uint32_t in_bar = bars + 8u * (2 * SM::STAGES + 5);
+  const uint32_t in_done = bars + 8u * (2 * SM::STAGES + 5);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + 8 * (2 * SM::STAGES + 6));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 8 * (2 * SM::STAGES + 6) + 8);
 
@@ -388,7 +398,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       mbar_init(chunk_empty(b), EPI_WARPS);
     }
     mbar_init(final_bar, 1);
-    mbar_init(in_bar, 1);
+    mbar_init(in_done, EPI_WARPS);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -412,7 +422,9 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      uint32_t q = 0;
+      uint32_t q = 0, nin = 0;
+      long long in_cur = -1, in_prev = -1;      // first ring K block of the input chunk of the
+      uint32_t par_cur = 0, par_prev = 0;        // current and the previous tile, and its in_done phase
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const int b = t / tiles_per_entry, tl = t % tiles_per_entry;
@@ -422,12 +434,12 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
         const int tile_m = ti * TC_BM, tile_n = tj * TC_BN;
         const int za = g.a_index ? g.a_index[b] : b;
         const int zb = g.b_index ? g.b_index[b] : b;
-        if (need_in) {            // the epilogue's input tile, into L2 while the products run
-#pragma unroll
-          for (int p = 0; p < DIGITS; ++p) {
-            tma_prefetch_3d(&maps.in[p], tile_n, tile_m, b);
-            tma_prefetch_3d(&maps.in[p], tile_n + 64, tile_m, b);
-          }
+        if (need_in) {
+          in_prev = in_cur;
+          par_prev = par_cur;
+          in_cur = (long long)q + (long long)TC_CHUNK_KB * tj;
+          par_cur = nin & 1;
+          ++nin;
         }
         for (int kb = 0; kb < nk; ++kb) {
           const int s = q % SM::STAGES;
@@ -435,6 +447,17 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
           if (q >= (uint32_t)SM::STAGES && !mbar_wait(empty_bar(s), (round - 1) & 1, g.err, abort_flag)) {
             ok = false;
             break;
+          }
+          if (need_in) {
+            // the stage held K block q - STAGES: if that was part of a tile's input chunk, the
+            // drain warps must have read it
+            const long long old = (long long)q - SM::STAGES;
+            const bool in_c = old >= in_cur && old < in_cur + TC_CHUNK_KB;
+            const bool in_p = in_prev >= 0 && old >= in_prev && old < in_prev + TC_CHUNK_KB;
+            if ((in_c || in_p) && !mbar_wait(in_done, in_c ? par_cur : par_prev, g.err, abort_flag)) {
+              ok = false;
+              break;
+            }
           }
           const uint32_t st = base + s * SM::STAGE_BYTES;
           mbar_expect_tx(full_bar(s), SM::STAGE_BYTES);
@@ -510,13 +533,15 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
     const int qd = warp & 3;                // TMEM lane quadrant (tile rows qd*32 ..)
     const int ew = warp - 2;                // epilogue warp index 0..7
     const int own = ew >> 2;                // column half
-    const int et = threadIdx.x - 64;        // epilogue thread 0..255
     const int r = qd * 32 + lane;           // tile row of this thread
-    float* xp = xp_all + ew * SM::XP_FLOATS;
     float* sbw = sb_all + ew * 128;
+    uint32_t* xs = xs_all + ew * 32 * SM::XS_LD;
     const uint32_t tlane = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(own * 64);
-    const float alpha16 = (float)((e.kind == EPI_AFF ? e.alpha : 1.0) * (1.0 / 65536.0));
-    uint32_t cq = 0, in_phase = 0;
+    const double alpha_eff = (e.kind == EPI_AFF) ? e.alpha : 1.0;
+    const float alpha16 = (float)(alpha_eff * (1.0 / 65536.0));
+    // input term in the sums' units: (beta / alpha) 2^16 sigma / 256 (P1 + P2 + P3)
+    const float in_unit = need_in ? (float)(e.beta_in / alpha_eff * 256.0) : 0.f;
+    uint32_t cq = 0, q = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const int b = t / tiles_per_entry, tl = t % tiles_per_entry;
       if (epi_skip(e, b)) continue;
@@ -555,6 +580,48 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
           sb_next0 = cv0 ? sb_ptr[o * g.b_srows] : 0.f;
           sb_next1 = cv1 ? sb_ptr[o * g.b_srows + 32] : 0.f;
         }
+        if (need_in && c == tj) {
+          // the input: this thread's 64 columns are the K blocks 4 tj + 2 own (+1) of A's
+          // chunk tj, row r, all three planes, resident in the ring; group gi = 16 columns
+          const float iu = in_unit * sa;
+          bool okr = true;
+#pragma unroll 1
+          for (int gi = 0; gi < 4; ++gi) {
+            const int kb = TC_CHUNK_KB * tj + 2 * own + (gi >> 1);
+            if (kb < nk) {
+              const uint32_t qq = q + (uint32_t)kb;
+              const int s = qq % SM::STAGES;
+              if (mbar_wait(full_bar(s), (qq / SM::STAGES) & 1, g.err, abort_flag)) {
+                if (rv) {
+                  const uint8_t* tp = gbase + s * SM::STAGE_BYTES;
+#pragma unroll
+                  for (int h8 = 0; h8 < 2; ++h8) {
+                    uint4 w[3];
+#pragma unroll
+                    for (int p = 0; p < DIGITS; ++p)
+                      w[p] = *reinterpret_cast<const uint4*>(tp + p * SM::PLANE_BYTES + ring_off(r, 16 * (gi & 1) + 8 * h8));
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                      float f[3];
+#pragma unroll
+                      for (int p = 0; p < DIGITS; ++p) {
+                        const uint32_t x = (&w[p].x)[i >> 1];
+                        f[p] = __uint_as_float((i & 1) ? (x & 0xFFFF0000u) : (x << 16));
+                      }
+                      acc[8 * h8 + i] = fmaf(iu, f[0] + (f[1] + f[2]), acc[8 * h8 + i]);
+                    }
+                  }
+                }
+              } else {
+                okr = false;
+              }
+            }
+            rotate16(acc);
+          }
+          if (!okr) ok = false;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(in_done);
+        }
         const bool okc = mbar_wait(chunk_full(buf), (cq >> 1) & 1, g.err, abort_flag);
         tc_fence_after();
         if (okc) {
@@ -569,289 +636,213 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
         } else {
           ok = false;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(chunk_empty(buf));
+        if (c + 1 < nchunks) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(chunk_empty(buf));
+        }
       }
-      // ---- element values: v = alpha acc 2^-16 + beta In (+ gamma on the diagonal)
+      q += (uint32_t)nk;
+      // The tile's sums go back into the last chunk's buffer (its S0 columns, this thread's row
+      // and half), which is released when the epilogue is done: every epilogue phase below is a
+      // loop over four 16-column groups loading from there, so its body exists once in the code
+      // (the epilogue runs once per tile; unrolled over 64 registers it would not stay in the
+      // instruction cache).
+      const uint32_t stash = tlane + ((cq - 1) & 1) * 256u;
 #pragma unroll
-      for (int j = 0; j < 64; ++j) acc[j] *= alpha16;
-      if (need_in) {
-        // the input tile through the staging area: round h loads its column half (all three
-        // planes) and the warps owning that half read it
-        const float sin = (rv && hv) ? *tc_scale_ptr(e.In, b, tj, gr) * 0.00390625f * (float)e.beta_in : 0.f;
+      for (int j = 0; j < 64; ++j) {
+        acc[j] *= alpha16;
+        if (e.kind == EPI_AFF && tile_n + own * 64 + j == gr) acc[j] += (float)e.gamma;
+      }
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = acc[16 * h + i];
+        tmem_st16(stash + 16 * h, v);
+      }
+      tmem_wait_st();
+      // ---- element values: v = alpha acc 2^-16 + beta In (+ gamma on the diagonal); then the
+      // maxima: the row over this half (elements the direct write keeps) and, for the transposed
+      // write, each column over this warp's 32 rows (elements it keeps)
+      float part = 0.f, mrow = 0.f;
+      const bool want_cmax = transposed && digits_out;
 #pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          if (et == 0) {
-            fence_async_smem();              // earlier reads of the staging area precede the load
-            mbar_expect_tx(in_bar, SM::STG_BYTES);
+      for (int gi = 0; gi < 4; ++gi) {
+        float m[16], v[16];
+        tmem_ld16(stash + 16 * gi, v);
 #pragma unroll
-            for (int p = 0; p < DIGITS; ++p)
-#pragma unroll
-              for (int bx = 0; bx < 2; ++bx)
-                tma_load_3d(stg_s + p * 16384 + bx * 8192, &maps.in[p], in_bar, tile_n + 64 * h, tile_m + 64 * bx, b);
-          }
-          const bool okl = mbar_wait(in_bar, in_phase & 1, g.err, abort_flag);
-          ++in_phase;
-          if (!okl) ok = false;
-          if (own == h && rv && hv && ok) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              uint4 w[3];
-#pragma unroll
-              for (int p = 0; p < DIGITS; ++p) w[p] = *reinterpret_cast<const uint4*>(stg + stg_chunk(p, r >> 6, r & 63, 8 * k));
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const int j = 8 * k + u;
-                float f[3];
-#pragma unroll
-                for (int p = 0; p < DIGITS; ++p) {
-                  const uint32_t x = (&w[p].x)[u >> 1];
-                  f[p] = __uint_as_float((u & 1) ? (x & 0xFFFF0000u) : (x << 16));
-                }
-                if (c0 + j < g.N) acc[j] = fmaf(sin, f[0] + (f[1] + f[2]), acc[j]);
-              }
-            }
-          }
-          epi_bar();                         // the half is read before the staging area is reused
-        }
-      }
-      if (e.kind == EPI_AFF && e.gamma != 0.0 && rv) {
-        const long long jd = gr - c0;
-        if (jd >= 0 && jd < 64) {
-#pragma unroll
-          for (int j = 0; j < 64; ++j)
-            if (j == jd) acc[j] += (float)e.gamma;
-        }
-      }
-      // ---- maxima: the row over this half (elements the direct write keeps) and, for the
-      // transposed write, each column over this warp's 32 rows (elements it keeps)
-      float part = 0.f;
-      {
-        float m = 0.f;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int cl = own * 64 + j;
-          const bool valid = rv && (c0 + j < g.N) && !(diag && cl < r);
-          if (valid) m = fmaxf(m, fabsf(acc[j]));
+        for (int i = 0; i < 16; ++i) {
+          const int j = 16 * gi + i, cl = own * 64 + j;
+          const bool vcol = rv && (c0 + j < g.N);
+          const bool valid = vcol && !(diag && cl < r);
+          if (valid) mrow = fmaxf(mrow, fabsf(v[i]));
           if (e.kind == EPI_M && valid) {
-            const float rd = acc[j] - ((tile_n + cl == gr) ? 1.0f : 0.0f);
+            const float rd = v[i] - ((tile_n + cl == gr) ? 1.0f : 0.0f);
             part += (mirror || (diag && cl > r)) ? 2.f * (rd * rd) : rd * rd;
           }
+          m[i] = (vcol && !(diag && cl <= r)) ? fabsf(v[i]) : 0.f;
         }
-        rmax[own * TC_BM + r] = m;
-      }
-      if (transposed && digits_out) {
+        if (want_cmax) {
+          // butterfly over the warp: after the exchanges lane L holds column L % 16 of the group
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
+          for (int w = 8; w >= 1; w >>= 1) {
+            const bool up = (lane & w) != 0;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int cl = own * 64 + h * 16 + i;
-            const bool valid = rv && (c0 + h * 16 + i < g.N) && !(diag && cl <= r);
-            xp[lane * SM::XP_LD + i] = valid ? fabsf(acc[h * 16 + i]) : 0.f;
+            for (int i = 0; i < w; ++i) {
+              const float send = up ? m[i] : m[i + w];
+              const float keep = up ? m[i + w] : m[i];
+              m[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, w));
+            }
           }
-          __syncwarp();
-          const int jj = lane & 15, rh = lane >> 4;
-          float m = 0.f;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) m = fmaxf(m, xp[(rh * 16 + i) * SM::XP_LD + jj]);
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-          if (lane < 16) cmax[qd * TC_BN + own * 64 + h * 16 + jj] = m;
-          __syncwarp();
+          m[0] = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], 16));
+          if (lane < 16) cmax[qd * TC_BN + own * 64 + 16 * gi + lane] = m[0];
         }
       }
+      rmax[own * TC_BM + r] = mrow;
       if (e.kind == EPI_M) {
         const double pd = warp_sum((double)part);
         if (lane == 0) red[ew] = pd;
       }
       epi_bar();                                       // maxima of the whole tile visible
       if (digits_out) {
-        // ---- digit planes of the output: staged one column half (all planes) per round, TMA stores
-        float inv_r = 1.f;
-        if (e.kind != EPI_VT) {
+        // output scales: rows of this tile (and, for a diagonal tile, its lower part
+        // mirrored in), and the rows of the mirrored tile / of V^T
+        if (own == 0) {
           float m = fmaxf(rmax[r], rmax[TC_BM + r]);
           if (diag) m = fmaxf(m, fmaxf(fmaxf(cmax[r], cmax[TC_BN + r]), fmaxf(cmax[2 * TC_BN + r], cmax[3 * TC_BN + r])));
           const float sigma = pow2_ceil_scale(m);
-          inv_r = 1.0f / sigma;
-          if (own == 0 && rv && ok) *tc_scale_ptr(e.C, b, tj, gr) = sigma;
+          invr[r] = 1.0f / sigma;
+          if (e.kind != EPI_VT && rv && ok) *tc_scale_ptr(e.C, b, tj, gr) = sigma;
+        } else if (mirror || e.kind == EPI_VT) {
+          const int cl = r;                            // one thread per tile column
+          const float m = fmaxf(fmaxf(cmax[cl], cmax[TC_BN + cl]), fmaxf(cmax[2 * TC_BN + cl], cmax[3 * TC_BN + cl]));
+          const float sigma = pow2_ceil_scale(m);
+          invc[cl] = 1.0f / sigma;
+          if (tile_n + cl < g.N && ok) *tc_scale_ptr(e.C, b, ti, tile_n + cl) = sigma;
         }
-        // direct (and diagonal) rounds: output columns tile_n + 64 h .., all 128 rows
-        if (e.kind != EPI_VT) {
+        epi_bar();
+        // ---- direct tile: digits of row r with its scale.  A warp writes its 32 rows x 16
+        // columns of one plane per step: each lane stores its row's 8 packed words into the
+        // warp's scratch, then the lanes store 4 rows x 8 words per instruction (32-byte runs)
+        const long long rbase = (long long)tile_m + qd * 32;
+        if (e.kind != EPI_VT && hv) {
+          const float ih = invr[r];
 #pragma unroll 1
-          for (int h = 0; h < 2; ++h) {
-            if (own == h && rv && hv) {
-              const float inv_h = opaque(inv_r);
+          for (int gi = 0; gi < 4; ++gi) {
+            float v[16];
+            tmem_ld16(stash + 16 * gi, v);
+            uint32_t wv[3][8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              float a[3], c[3];
+              digits3(v[2 * u], ih, a[0], a[1], a[2]);
+              digits3(v[2 * u + 1], ih, c[0], c[1], c[2]);
+#pragma unroll
+              for (int p = 0; p < DIGITS; ++p) wv[p][u] = pack_bf16x2(a[p], c[p]);
+            }
+#pragma unroll
+            for (int p = 0; p < DIGITS; ++p) {
+#pragma unroll
+              for (int u = 0; u < 8; ++u) xs[lane * SM::XS_LD + u] = wv[p][u];
+              __syncwarp();
+              uint32_t* plane = reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(e.C.hi) +
+                                                            (long long)b * e.C.bstride + p * e.C.pstride);
 #pragma unroll
               for (int k = 0; k < 8; ++k) {
-                uint32_t wv[3][4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  float a[3], c[3];
-                  digits3(acc[8 * k + 2 * u], inv_h, a[0], a[1], a[2]);
-                  digits3(acc[8 * k + 2 * u + 1], inv_h, c[0], c[1], c[2]);
-#pragma unroll
-                  for (int p = 0; p < DIGITS; ++p) wv[p][u] = pack_bf16x2(a[p], c[p]);
-                }
-#pragma unroll
-                for (int p = 0; p < DIGITS; ++p)
-                  *reinterpret_cast<uint4*>(stg + stg_chunk(p, r >> 6, r & 63, 8 * k)) =
-                      make_uint4(wv[p][0], wv[p][1], wv[p][2], wv[p][3]);
+                const int R = 4 * k + (lane >> 3), w = lane & 7;
+                if (rbase + R < g.M && ok)
+                  plane[((rbase + R) * e.C.ld + c0 + 16 * gi) / 2 + w] = xs[R * SM::XS_LD + w];
               }
+              __syncwarp();
             }
-            if (diag) {
-              // a diagonal tile's lower part comes from its upper part: element (lc, cl), lc < cl,
-              // of the tile becomes (cl, lc); lc lies in this round's half, so the writers are the
-              // warps of the quadrants 2h, 2h + 1
-              epi_bar();                             // the direct values of the half are in place
-              if ((qd >> 1) == h) {
-#pragma unroll
-                for (int hb = 0; hb < 4; ++hb) {
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) xp[lane * SM::XP_LD + i] = acc[hb * 16 + i];
-                  __syncwarp();
-                  const int jj = lane & 15, rh = lane >> 4;
-                  const int cl = own * 64 + hb * 16 + jj, lc0 = qd * 32 + rh * 16;
-                  float v16[16];
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) v16[i] = xp[(rh * 16 + i) * SM::XP_LD + jj];
-                  __syncwarp();
-                  float m = fmaxf(fmaxf(cmax[cl], cmax[TC_BN + cl]), fmaxf(cmax[2 * TC_BN + cl], cmax[3 * TC_BN + cl]));
-                  m = fmaxf(m, fmaxf(rmax[cl], rmax[TC_BM + cl]));
-                  const float inv = opaque(1.0f / pow2_ceil_scale(m));
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) {
-                    const int lc = lc0 + i;
-                    if (lc < cl) {
-                      float d[3];
-                      digits3(v16[i], inv, d[0], d[1], d[2]);
-                      const int cc = lc - 64 * h;
-#pragma unroll
-                      for (int p = 0; p < DIGITS; ++p)
-                        *reinterpret_cast<__nv_bfloat16*>(stg + stg_chunk(p, cl >> 6, cl & 63, cc) + ((cc & 7) << 1)) =
-                            __float2bfloat16_rn(d[p]);
-                    }
-                  }
-                }
-              }
-            }
-            fence_async_smem();
-            epi_bar();
-            if (et == 0) {
-#pragma unroll
-              for (int p = 0; p < DIGITS; ++p)
-#pragma unroll
-                for (int bx = 0; bx < 2; ++bx)
-                  tma_store_3d(&maps.c[p], stg_s + p * 16384 + bx * 8192, tile_n + 64 * h, tile_m + 64 * bx, b);
-              bulk_commit();
-              bulk_wait_read0();                       // the staging area may be rewritten
-            }
-            epi_bar();
           }
         }
-        // transposed rounds (mirrored tile, or V^T): tile column cl becomes output row tile_n + cl,
-        // round h takes the tile's columns 64 h .. (the warps of that half), all 128 tile rows
-        if (mirror || e.kind == EPI_VT) {
+        // ---- mirrored tile (and a diagonal tile's lower part, and V^T): element (r, cl) goes to
+        // output row tile_n + cl, column tile_m + r.  Lane pairs (rows r, r + 1) trade one value
+        // so that each lane stores a word of two adjacent output columns; for a fixed column the
+        // warp's stores form two 64-byte runs.
+        if (transposed) {
+          if (diag) epi_bar();                         // a diagonal tile's direct part is written
 #pragma unroll 1
-          for (int h = 0; h < 2; ++h) {
-            if (own == h) {
+          for (int gi = 0; gi < 4; ++gi) {
+            float v[16];
+            tmem_ld16(stash + 16 * gi, v);
 #pragma unroll
-              for (int hb = 0; hb < 4; ++hb) {
+            for (int u = 0; u < 8; ++u) {
+              const int j0 = 16 * gi + 2 * u;          // this pair of columns: j0, j0 + 1
+              const int cl0 = own * 64 + j0;
+              const float i0 = diag ? invr[cl0] : invc[cl0];
+              const float i1 = diag ? invr[cl0 + 1] : invc[cl0 + 1];
+              float a[3], c[3];
+              digits3(v[2 * u], i0, a[0], a[1], a[2]);
+              digits3(v[2 * u + 1], i1, c[0], c[1], c[2]);
+              const bool odd = lane & 1;
+              const long long orow = tile_n + cl0 + (odd ? 1 : 0);
+              const long long ocol = (long long)tile_m + (r & ~1);
+              // diagonal tile: only elements above the diagonal (cl > row) are mirrored
+              const bool lo_ok = !diag || (cl0 + (odd ? 1 : 0) > (r & ~1));
+              const bool hi_ok = !diag || (cl0 + (odd ? 1 : 0) > (r | 1));
+              const bool rowok = orow < g.N && ocol < g.M && ok;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) xp[lane * SM::XP_LD + i] = acc[hb * 16 + i];
-                __syncwarp();
-                const int jj = lane & 15, rh = lane >> 4;
-                const int ol = hb * 16 + jj;              // output row within the round (cl - 64 h)
-                const int cl = own * 64 + ol, lc0 = qd * 32 + rh * 16;
-                float v16[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v16[i] = xp[(rh * 16 + i) * SM::XP_LD + jj];
-                __syncwarp();
-                const float m = fmaxf(fmaxf(cmax[cl], cmax[TC_BN + cl]), fmaxf(cmax[2 * TC_BN + cl], cmax[3 * TC_BN + cl]));
-                const float sigma = pow2_ceil_scale(m);
-                const float inv = opaque(1.0f / sigma);
-                if (qd == 0 && rh == 0 && tile_n + cl < g.N && ok) *tc_scale_ptr(e.C, b, ti, tile_n + cl) = sigma;
-#pragma unroll
-                for (int half8 = 0; half8 < 2; ++half8) {
-                  uint32_t wv[3][4];
-#pragma unroll
-                  for (int u = 0; u < 4; ++u) {
-                    float a[3], c[3];
-                    digits3(v16[8 * half8 + 2 * u], inv, a[0], a[1], a[2]);
-                    digits3(v16[8 * half8 + 2 * u + 1], inv, c[0], c[1], c[2]);
-#pragma unroll
-                    for (int p = 0; p < DIGITS; ++p) wv[p][u] = pack_bf16x2(a[p], c[p]);
-                  }
-                  const int cc = (lc0 & 63) + 8 * half8;
-#pragma unroll
-                  for (int p = 0; p < DIGITS; ++p)
-                    *reinterpret_cast<uint4*>(stg + stg_chunk(p, lc0 >> 6, ol, cc)) =
-                        make_uint4(wv[p][0], wv[p][1], wv[p][2], wv[p][3]);
+              for (int p = 0; p < DIGITS; ++p) {
+                // even lane keeps (r, j0), sends (r, j0 + 1); odd lane keeps (r, j0 + 1), sends (r, j0)
+                const float mine = odd ? c[p] : a[p];
+                const float other = __shfl_xor_sync(0xffffffffu, odd ? a[p] : c[p], 1);
+                // the word's low half is the even row's element, its high half the odd row's
+                const float lo = odd ? other : mine, hi = odd ? mine : other;
+                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(e.C.hi) + (long long)b * e.C.bstride +
+                                     p * e.C.pstride + orow * e.C.ld + ocol;
+                if (rowok) {
+                  if (lo_ok && hi_ok) *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(lo, hi);
+                  else if (lo_ok) dst[0] = __float2bfloat16_rn(lo);
                 }
               }
             }
-            fence_async_smem();
-            epi_bar();
-            if (et == 0) {
+          }
+        }
+      } else if (hv) {
+        // ---- fp32 results: the caller's state (Gram EMA, and its mirrored tile), the update, or
+        // a plain store.  Row-major stores pass through the warp's scratch: lanes store 2 rows x
+        // 16 columns per instruction (64-byte runs); the mirrored Gram tile is stored directly
+        // (for a fixed column the warp's lanes are consecutive addresses).
+        const long long rbase = (long long)tile_m + qd * 32;
+#pragma unroll 1
+        for (int gi = 0; gi < 4; ++gi) {
+          float v[16];
+          tmem_ld16(stash + 16 * gi, v);
 #pragma unroll
-              for (int p = 0; p < DIGITS; ++p)
+          for (int i = 0; i < 16; ++i) xs[lane * SM::XS_LD + i] = __float_as_uint(v[i]);
+          __syncwarp();
 #pragma unroll
-                for (int bx = 0; bx < 2; ++bx)
-                  tma_store_3d(&maps.c[p], stg_s + p * 16384 + bx * 8192, tile_m + 64 * bx, tile_n + 64 * h, b);
-              bulk_commit();
-              bulk_wait_read0();
+          for (int k = 0; k < 16; ++k) {
+            const int R = 2 * k + (lane >> 4), w = lane & 15;
+            const long long row = rbase + R;
+            const int col = c0 + 16 * gi + w;
+            const int cl = own * 64 + 16 * gi + w;
+            if (row < g.M && col < g.N && ok) {
+              const float v = __uint_as_float(xs[R * SM::XS_LD + w]);
+              const long long o = row * (long long)e.cols + col;
+              if (e.kind == EPI_GRAM) {
+                if (!(diag && cl < qd * 32 + R)) e.state[b][o] = fmaf(e.beta, e.state[b][o], (1.0f - e.beta) * v);
+              } else if (e.kind == EPI_U) {
+                if (e.out_dtype == PRECOND_BF16) reinterpret_cast<__nv_bfloat16*>(e.out[b])[o] = __float2bfloat16_rn(v);
+                else reinterpret_cast<float*>(e.out[b])[o] = v;
+              } else if (e.kind == EPI_STORE) {
+                e.f32out[(long long)b * e.rows * e.cols + o] = v;
+              }
             }
-            epi_bar();
           }
-        }
-      } else if (rv && hv && ok) {
-        // ---- fp32 results: the caller's state (Gram EMA), update, or a plain store
-        if (e.kind == EPI_GRAM) {
-          float* srow = e.state[b] + gr * (long long)e.cols;
-#pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const int cl = own * 64 + j;
-            if (c0 + j < g.N && !(diag && cl < r)) srow[c0 + j] = fmaf(e.beta, srow[c0 + j], (1.0f - e.beta) * acc[j]);
-          }
-        } else if (e.kind == EPI_U) {
-          const long long o = gr * (long long)e.cols + c0;
-          if (e.out_dtype == PRECOND_BF16) {
-            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(e.out[b]) + o;
-#pragma unroll
-            for (int j = 0; j < 64; ++j)
-              if (c0 + j < g.N) dst[j] = __float2bfloat16_rn(acc[j]);
-          } else {
-            float* dst = reinterpret_cast<float*>(e.out[b]) + o;
-#pragma unroll
-            for (int j = 0; j < 64; ++j)
-              if (c0 + j < g.N) dst[j] = acc[j];
-          }
-        } else if (e.kind == EPI_STORE) {
-          float* dst = e.f32out + (long long)b * e.rows * e.cols + gr * (long long)e.cols + c0;
-#pragma unroll
-          for (int j = 0; j < 64; ++j)
-            if (c0 + j < g.N) dst[j] = acc[j];
-        }
-      }
-      if (e.kind == EPI_GRAM && transposed) {
-        // the state's mirrored tile: column cl of the tile is row tile_n + cl of the state
-        epi_bar();
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) xp[lane * SM::XP_LD + i] = acc[h * 16 + i];
           __syncwarp();
-          const int jj = lane & 15, rh = lane >> 4;
-          const int cl = own * 64 + h * 16 + jj, lc0 = qd * 32 + rh * 16;
-          const long long orow = tile_n + cl;
-          float v16[16];
+          if (e.kind == EPI_GRAM && transposed && rv && ok) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v16[i] = xp[(rh * 16 + i) * SM::XP_LD + jj];
-          __syncwarp();
-          if (orow < g.N && ok) {
-            float* srow = e.state[b] + orow * (long long)e.cols + tile_m + lc0;
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (tile_m + lc0 + i < g.M && !(diag && lc0 + i >= cl)) srow[i] = fmaf(e.beta, srow[i], (1.0f - e.beta) * v16[i]);
+            for (int i = 0; i < 16; ++i) {
+              const int j = 16 * gi + i, cl = own * 64 + j;
+              if (c0 + j < g.N && !(diag && cl <= r)) {
+                float* sp = e.state[b] + (long long)(c0 + j) * e.cols + gr;
+                *sp = fmaf(e.beta, *sp, (1.0f - e.beta) * v[i]);
+              }
+            }
           }
         }
       }
@@ -861,12 +852,12 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
         for (int w = 0; w < EPI_WARPS; ++w) sum += red[w];     // fixed order: deterministic
         if (ok) epi_m_finish(e, b, sum, g.M, tl);
       }
+      // the stash's buffer may take the next chunks
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(chunk_empty(((cq - 1) & 1)));
       // shared scratch free for the next tile; leave together once any role has aborted
       if (epi_bar_or(*abort_flag != 0)) break;
-    }
-    if (et == 0) {
-      bulk_wait0();                              // every output store has completed
-      if (in_phase > 0) mbar_wait_own(in_bar, (in_phase - 1) & 1, g.err);   // and the last input load
     }
   }
 

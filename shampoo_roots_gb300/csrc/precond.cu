@@ -673,16 +673,14 @@ int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int 
     e.tiles_per_entry = grid.x * grid.y;
     gemm_f64_kernel<<<grid, 256, 0, c.st>>>(g, e);
   } else {
+    // the epilogue takes its element-wise input from the operand ring: it must be A itself
+    if (Ins && (Ins->off != A.off || e.kind == EPI_AFF && e.alpha == 0.0)) return PRECOND_EINVAL;
     TcMaps maps;
     memset(&maps, 0, sizeof(maps));
     int rc;
     for (int q = 0; q < DIGITS; ++q) {
       if ((rc = encode_map(c.h, &maps.a[q], c.ws + A.off + (size_t)q * A.pstride * 2, A, TC_BM))) return rc;
       if ((rc = encode_map(c.h, &maps.b[q], c.ws + B.off + (size_t)q * B.pstride * 2, B, TC_BN))) return rc;
-      if (Cs && (rc = encode_map(c.h, &maps.c[q], c.ws + Cs->off + (size_t)q * Cs->pstride * 2, *Cs, TC_BM, true)))
-        return rc;
-      if (Ins && (rc = encode_map(c.h, &maps.in[q], c.ws + Ins->off + (size_t)q * Ins->pstride * 2, *Ins, TC_BM, true)))
-        return rc;
     }
     TcGemmArgs g;
     memset(&g, 0, sizeof(g));
