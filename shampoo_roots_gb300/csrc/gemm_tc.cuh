@@ -701,8 +701,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       }
       rmax[own * TC_BM + r] = mrow;
       if (e.kind == EPI_M) {
-        const double pd = warp_sum((double)part);
-        if (lane == 0) red[ew] = pd;
+        const float pd = warp_sum(part);
+        if (lane == 0) red[ew] = (double)pd;
       }
       epi_bar();                                       // maxima of the whole tile visible
       if (digits_out) {
@@ -722,10 +722,11 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
           if (tile_n + cl < g.N && ok) *tc_scale_ptr(e.C, b, ti, tile_n + cl) = sigma;
         }
         epi_bar();
-        // ---- direct tile: digits of row r with its scale.  A warp writes its 32 rows x 16
-        // columns of one plane per step: each lane stores its row's 8 packed words into the
-        // warp's scratch, then the lanes store 4 rows x 8 words per instruction (32-byte runs)
+        // ---- direct tile: digits of row r with its scale.  Per 16-column group and plane each
+        // lane puts its row's 32 bytes into the warp's scratch (rows 48 bytes apart), then the
+        // lanes store 16-byte pieces: two per lane, 32 rows x 32 bytes.
         const long long rbase = (long long)tile_m + qd * 32;
+        uint8_t* xb = reinterpret_cast<uint8_t*>(xs);
         if (e.kind != EPI_VT && hv) {
           const float ih = invr[r];
 #pragma unroll 1
@@ -743,61 +744,60 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
             }
 #pragma unroll
             for (int p = 0; p < DIGITS; ++p) {
-#pragma unroll
-              for (int u = 0; u < 8; ++u) xs[lane * SM::XS_LD + u] = wv[p][u];
+              *reinterpret_cast<uint4*>(xb + lane * 48) = make_uint4(wv[p][0], wv[p][1], wv[p][2], wv[p][3]);
+              *reinterpret_cast<uint4*>(xb + lane * 48 + 16) = make_uint4(wv[p][4], wv[p][5], wv[p][6], wv[p][7]);
               __syncwarp();
-              uint32_t* plane = reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(e.C.hi) +
-                                                            (long long)b * e.C.bstride + p * e.C.pstride);
+              __nv_bfloat16* plane = reinterpret_cast<__nv_bfloat16*>(e.C.hi) + (long long)b * e.C.bstride + p * e.C.pstride;
 #pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const int R = 4 * k + (lane >> 3), w = lane & 7;
+              for (int t = 0; t < 2; ++t) {
+                const int cidx = lane + 32 * t, R = cidx >> 1, hh = cidx & 1;
+                const uint4 w = *reinterpret_cast<const uint4*>(xb + R * 48 + hh * 16);
                 if (rbase + R < g.M && ok)
-                  plane[((rbase + R) * e.C.ld + c0 + 16 * gi) / 2 + w] = xs[R * SM::XS_LD + w];
+                  *reinterpret_cast<uint4*>(plane + (rbase + R) * e.C.ld + c0 + 16 * gi + 8 * hh) = w;
               }
               __syncwarp();
             }
           }
         }
         // ---- mirrored tile (and a diagonal tile's lower part, and V^T): element (r, cl) goes to
-        // output row tile_n + cl, column tile_m + r.  Lane pairs (rows r, r + 1) trade one value
-        // so that each lane stores a word of two adjacent output columns; for a fixed column the
-        // warp's stores form two 64-byte runs.
+        // output row tile_n + cl, column tile_m + r.  Per group and plane each lane writes its 16
+        // values into the scratch column-major (16 output rows x 32 output columns), then the lanes
+        // store 16-byte pieces of 8 output columns: two per lane.
         if (transposed) {
           if (diag) epi_bar();                         // a diagonal tile's direct part is written
+          __nv_bfloat16* xh = reinterpret_cast<__nv_bfloat16*>(xs);
 #pragma unroll 1
           for (int gi = 0; gi < 4; ++gi) {
-            float v[16];
+            float v[16], inv[16];
             tmem_ld16(stash + 16 * gi, v);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int j0 = 16 * gi + 2 * u;          // this pair of columns: j0, j0 + 1
-              const int cl0 = own * 64 + j0;
-              const float i0 = diag ? invr[cl0] : invc[cl0];
-              const float i1 = diag ? invr[cl0 + 1] : invc[cl0 + 1];
-              float a[3], c[3];
-              digits3(v[2 * u], i0, a[0], a[1], a[2]);
-              digits3(v[2 * u + 1], i1, c[0], c[1], c[2]);
-              const bool odd = lane & 1;
-              const long long orow = tile_n + cl0 + (odd ? 1 : 0);
-              const long long ocol = (long long)tile_m + (r & ~1);
-              // diagonal tile: only elements above the diagonal (cl > row) are mirrored
-              const bool lo_ok = !diag || (cl0 + (odd ? 1 : 0) > (r & ~1));
-              const bool hi_ok = !diag || (cl0 + (odd ? 1 : 0) > (r | 1));
-              const bool rowok = orow < g.N && ocol < g.M && ok;
+            for (int i = 0; i < 16; ++i) {
+              const int cl = own * 64 + 16 * gi + i;
+              inv[i] = diag ? invr[cl] : invc[cl];
+            }
 #pragma unroll
-              for (int p = 0; p < DIGITS; ++p) {
-                // even lane keeps (r, j0), sends (r, j0 + 1); odd lane keeps (r, j0 + 1), sends (r, j0)
-                const float mine = odd ? c[p] : a[p];
-                const float other = __shfl_xor_sync(0xffffffffu, odd ? a[p] : c[p], 1);
-                // the word's low half is the even row's element, its high half the odd row's
-                const float lo = odd ? other : mine, hi = odd ? mine : other;
-                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(e.C.hi) + (long long)b * e.C.bstride +
-                                     p * e.C.pstride + orow * e.C.ld + ocol;
-                if (rowok) {
-                  if (lo_ok && hi_ok) *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(lo, hi);
-                  else if (lo_ok) dst[0] = __float2bfloat16_rn(lo);
+            for (int p = 0; p < DIGITS; ++p) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) xh[i * 32 + lane] = __float2bfloat16_rn(digit_p(v[i], inv[i], p));
+              __syncwarp();
+              __nv_bfloat16* plane = reinterpret_cast<__nv_bfloat16*>(e.C.hi) + (long long)b * e.C.bstride + p * e.C.pstride;
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                const int cidx = lane + 32 * t, jj = cidx >> 2, k = cidx & 3;
+                const int cl = own * 64 + 16 * gi + jj;      // tile column = output row offset
+                const int lc = qd * 32 + 8 * k;             // first tile row = output column offset
+                const long long orow = tile_n + cl, ocol = (long long)tile_m + lc;
+                if (orow < g.N && ocol < g.M && ok) {
+                  __nv_bfloat16* dst = plane + orow * e.C.ld + ocol;
+                  if (!diag || lc + 7 < cl) {
+                    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(xh + jj * 32 + 8 * k);
+                  } else if (lc < cl) {
+                    // a diagonal tile's piece crossing the diagonal: only rows above it
+                    for (int i = 0; i < cl - lc; ++i) dst[i] = xh[jj * 32 + 8 * k + i];
+                  }
                 }
               }
+              __syncwarp();
             }
           }
         }
