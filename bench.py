@@ -208,12 +208,15 @@ def oracle_sample_spd(w, power, n=2):
     return dt / n * w.count, f"{n} of the {w.count} SPD {w.dims[0]}^2 matrices ({dt:.1f} s), extrapolated", os.cpu_count()
 
 
-# The arithmetic of the path: fp32 values, every product on bf16 tensor cores as
-# exact products of per-row-scaled bf16 digits (4 digits of 7 bits, the leading
-# product levels accumulated exactly), fp32 storage between products.
-DTYPE = "fp32 (bf16x4 exact digit products)"
-DTYPE_NOTE = ("fp32 matrices; products as exact bf16 digit products on tensor cores (4 digits of 7 bits, "
-              "leading levels accumulated exactly in fp32), about 2^-28 relative to the row scales")
+# The arithmetic of the path: fp32 values; every product on bf16 tensor cores as
+# exact products of three 9-bit bf16 digits under a power-of-two scale per (row,
+# 128-column block), six digit products per K step accumulated in tensor memory
+# over one 128-wide K block and summed across blocks in fp32 registers; fp32
+# storage between products.
+DTYPE = "fp32 (exact bf16x3 digit products)"
+DTYPE_NOTE = ("fp32 matrices; products as exact bf16 digit products on tensor cores (3 digits of 9 bits "
+              "per (row, 128-column block) scale, six digit products per K step, per-block sums in fp32), "
+              "about 2^-26 relative to the block scales")
 SM_COUNT = 152
 BF16_FLOPS_PER_CLK_SM = 8192.0     # dense bf16 tensor-core rate per SM and clock (2 x 4096 FMA)
 
@@ -356,7 +359,7 @@ def main():
                     help="0 single 256x128, 1 stack p=-1/4 (default), 2 stack p=-1/2, 3 SPD 64x2048^2, 4 wide 6144")
     ap.add_argument("--power", type=float, default=None, help="override the workload's power")
     ap.add_argument("--opt", action="append", default=[], metavar="KEY=VALUE",
-                    help="handle option (PRECOND_OPT_KEY, lower case), e.g. digits3_from=0.04")
+                    help="handle option (PRECOND_OPT_KEY, lower case), e.g. tol=1e-5")
     ap.add_argument("--profile-dim", type=int, default=2048, help="profiling case: matrix side")
     ap.add_argument("--profile-count", type=int, default=4, help="profiling case: number of matrices")
     ap.add_argument("--profile-small", action="store_true",
@@ -506,13 +509,13 @@ def main():
     # dominant kernel: the tcgen05 GEMM of the iteration stage (timed inside a long step -> sustained peak)
     achieved = (root_flops / (gemm_ms / 1e3) / 1e12) if gemm_ms > 0 else None
     peak = peaks["bf16_tflops_sustained"]
-    # issued: tiles actually run (upper triangles of symmetric products) x 10 bf16 digit products
+    # issued: tiles actually run (upper triangles of symmetric products) x 6 bf16 digit products
     issued = (issued_flops / (gemm_ms / 1e3) / 1e12) if gemm_ms > 0 else None
     traffic, traffic_alg = captured_traffic(w.index)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": (achieved / peak) if achieved else None, "traffic": traffic,
                 "traffic_algorithmic": traffic_alg,
-                "kernel": "gemm_tc_kernel<4> (iteration-stage products)",
+                "kernel": "gemm_tc_kernel (iteration-stage products)",
                 "peak_kind": f"bf16 dense, sustained ({peaks['source']})",
                 "issued_tflops": issued, "issued_frac": (issued / peak) if issued else None,
                 "avg_launch_ms": gemm_ms / gemm_n if gemm_n else None}
