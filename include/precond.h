@@ -176,6 +176,16 @@ int precond_get_timing(precond_t h, double ms[4], int64_t* ns_gemm_launches, dou
  */
 int precond_get_gemm_timing(precond_t h, double* ms_total, int64_t* launches, double* issued_flops);
 
+/*
+ * Workspace bytes.  *planned: the plan of the last precond_step /
+ * precond_inv_root call on this handle that passed validation, also on a
+ * host-only handle (where that call returns PRECOND_ENODEV after planning);
+ * 0 before any such call.  *allocated: the device workspace the handle holds
+ * now (0 on a host-only handle).  Either pointer may be NULL.  The EMA state,
+ * gradients and outputs are the caller's and are not counted.
+ */
+int precond_get_workspace(precond_t h, int64_t* planned, int64_t* allocated);
+
 /* Kernel launches this handle has issued since creation (every library kernel). */
 int64_t precond_launch_count(precond_t h);
 

@@ -50,6 +50,7 @@ def load():
     L.precond_get_timing.argtypes = [vp, ctypes.POINTER(f64), ctypes.POINTER(i64), ctypes.POINTER(f64)]
     L.precond_launch_count.argtypes = [vp]
     L.precond_get_gemm_timing.argtypes = [vp, ctypes.POINTER(f64), ctypes.POINTER(i64), ctypes.POINTER(f64)]
+    L.precond_get_workspace.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     L.precond_launch_count.restype = i64
     L.precond_get_root.argtypes = [vp, i32, vp, vp]
     L.precond_debug_plane.argtypes = [vp, i32, i32, vp, vp]
@@ -61,7 +62,7 @@ def load():
     L.precond_error_string.restype = ctypes.c_char_p
     for name in ("precond_create", "precond_destroy", "precond_step", "precond_inv_root", "precond_get_stats",
                  "precond_set_option", "precond_get_timing", "precond_get_root", "precond_gemm_selftest",
-                 "precond_debug_plane", "precond_get_gemm_timing",
+                 "precond_debug_plane", "precond_get_gemm_timing", "precond_get_workspace",
                  "precond_inv_root_noalloc", "precond_step_schedule"):
         getattr(L, name).restype = i32
     _lib = L
@@ -200,6 +201,13 @@ def precond_get_gemm_timing(h):
     _check(load().precond_get_gemm_timing(h, ctypes.byref(ms), ctypes.byref(n), ctypes.byref(fl)),
            "precond_get_gemm_timing")
     return ms.value, n.value, fl.value
+
+
+def precond_get_workspace(h):
+    """(planned bytes of the last validated call, device bytes held now)."""
+    planned, held = ctypes.c_int64(), ctypes.c_int64()
+    _check(load().precond_get_workspace(h, ctypes.byref(planned), ctypes.byref(held)), "precond_get_workspace")
+    return planned.value, held.value
 
 
 def precond_launch_count(h) -> int:

@@ -104,6 +104,7 @@ struct precond_ctx {
   double ws_max = 0;
   void* ws = nullptr;
   size_t ws_cap = 0;
+  size_t planned_bytes = 0;   // workspace bytes of the last validated plan
   void* pinned = nullptr;
   size_t pinned_cap = 0;
   cudaEvent_t upload_done = nullptr;
@@ -1316,6 +1317,7 @@ int precond_step(precond_t h, int count, void* const grads[], int grad_dtype, co
   Plan P;
   int rc = build_plan(h, P, true, count, shapes, grad_dtype, eps, p, grads, L, R, out_f32, nullptr, nullptr);
   if (rc) return rc;
+  h->planned_bytes = P.total;
   if (h->ws_max > 0 && (double)P.total > h->ws_max) return PRECOND_ENOMEM;
   if (h->device < 0) return PRECOND_ENODEV;
   if ((rc = prepare_device(h))) return rc;
@@ -1340,6 +1342,7 @@ int precond_inv_root(precond_t h, int count, const float* const A[], const int64
   Plan P;
   int rc = build_plan(h, P, false, count, dims, PRECOND_F32, eps, p, nullptr, nullptr, nullptr, nullptr, A, X);
   if (rc) return rc;
+  h->planned_bytes = P.total;
   if (h->ws_max > 0 && (double)P.total > h->ws_max) return PRECOND_ENOMEM;
   if (h->device < 0) return PRECOND_ENODEV;
   if ((rc = prepare_device(h))) return rc;
@@ -1408,6 +1411,13 @@ int precond_get_timing(precond_t h, double ms[4], int64_t* ns_gemm_launches, dou
 }
 
 int64_t precond_launch_count(precond_t h) { return h ? h->launches : -1; }
+
+int precond_get_workspace(precond_t h, int64_t* planned, int64_t* allocated) {
+  if (!h) return PRECOND_EINVAL;
+  if (planned) *planned = (int64_t)h->planned_bytes;
+  if (allocated) *allocated = (int64_t)h->ws_cap;
+  return PRECOND_OK;
+}
 
 int precond_get_gemm_timing(precond_t h, double* ms_total, int64_t* launches, double* issued_flops) {
   if (!h) return PRECOND_EINVAL;

@@ -173,3 +173,18 @@ def test_bench_traffic_is_dropped_when_the_kernel_changes(monkeypatch):
     monkeypatch.setitem(bench.TRAFFIC_CAPTURES, 1, cap)
     assert bench.captured_traffic(1) == (None, None)
     assert bench.captured_traffic(0) == (None, None)
+
+
+def test_workspace_is_planned_on_a_host_only_handle(host):
+    assert sr.precond_get_workspace(host.h) == (0, 0)
+    assert host.step([(256, 128)]) == sr.ENODEV
+    one, held = sr.precond_get_workspace(host.h)
+    assert one > 0 and held == 0
+    # the digit planes of both roots dominate: 3 bf16 digits per element of X (2), M (2), D and F
+    assert one >= 6 * 6 * (256 * 256 + 128 * 128)
+    assert host.step([(256, 128)] * 4) == sr.ENODEV
+    four, _ = sr.precond_get_workspace(host.h)
+    assert 3 * one < four <= 4 * one
+    assert host.step([(8, 4)], eps=0.0) == sr.EINVAL          # a rejected call leaves the figure alone
+    assert sr.precond_get_workspace(host.h)[0] == four
+    assert host.lib.precond_get_workspace(None, None, None) == sr.EINVAL
