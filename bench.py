@@ -55,33 +55,68 @@ def rank_step_seed(rank: int, step: int) -> int:
     return 1000 * rank + step
 
 
-# DRAM traffic of the dominant kernel from one ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum of one iteration's products of both root classes of the
-# d = 1024 stack), per launch over a step's
-# launch mix: per class 34 computed products (7 iterations) and 15 launches whose
-# roots have all converged (no tiles, no traffic).  Valid only for the kernel
-# sources it was taken on: their SHA-1s (the gemm_tc.cuh one after a comment-only
-# edit of its header).
+# DRAM traffic of the dominant kernel, from ncu captures (dram__bytes_read.sum +
+# dram__bytes_write.sum) of one whole iteration (E, X', D, F, M') of a small
+# case per root class: 2 roots of 6144^2 and 8 roots of 3072^2, each about 2400
+# tiles of 128 x 128 (as many tiles in flight per SM as at full size).  Bytes
+# per output element and product, averaged over the iteration; the bench scales
+# them by the elements each root class computed in the step.  The algorithmic
+# bytes are 6 B of digits per element for each distinct operand read and 6 B
+# written (the element-wise input is the A operand: no extra read), 14.4 B on
+# average over an iteration.  Valid only for the kernel sources the captures
+# were taken on (their SHA-1s), the default options and the quadratic p = 4
+# steps (4 products in the first iteration, 5 after).
 TRAFFIC_CAPTURES = {
-    1: {"bytes_per_launch": 10.71e9, "algorithmic_bytes_per_launch": 7.04e9,
-        "sources": {"gemm_tc.cuh": "38c0b49c103fc7d7dec1f31db160d9196aaabf8d",
-                    "engine.cuh": "4ed3254d617f51583c8c6d6ebfef32cc43e157e2",
-                    "common.cuh": "983868160199120ad308ddf0b9fbbdd1021863c0"}},
+    4: {"bytes_per_element": {6144: 35.30, 3072: 18.50}, "algorithmic_bytes_per_element": 14.4,
+        "power": -0.25,
+        "sources": {"gemm_tc.cuh": "7ec34887fbbcafd05412ba8425b1f21b49e529a3",
+                    "engine.cuh": "9f93f9fd23cc0f6ceaa695703a91b7623e3d287b",
+                    "common.cuh": "bde15094817cdd9be373c93fc049db220e42550e"}},
 }
 
 
-def captured_traffic(workload: int):
-    """(traffic, algorithmic bytes) per launch of the dominant kernel, or
-    (None, None) when no capture exists or the kernel changed since."""
+def captured_traffic(workload: int, power: float, opts, root_dims, root_iters, launches: float):
+    """(traffic, algorithmic bytes) per launch of the dominant kernel over the
+    step's launch mix, or (None, None) when no capture covers this run or the
+    kernel changed since."""
     import hashlib
     cap = TRAFFIC_CAPTURES.get(workload)
-    if cap is None:
+    if cap is None or opts or power != cap["power"] or not launches:
         return None, None
     for name, digest in cap["sources"].items():
         with open(os.path.join(ROOT, "shampoo_roots_gb300", "csrc", name), "rb") as f:
             if hashlib.sha1(f.read()).hexdigest() != digest:
                 return None, None
-    return cap["bytes_per_launch"], cap["algorithmic_bytes_per_launch"]
+    measured = 0.0
+    for d, k in zip(root_dims, root_iters):
+        if d not in cap["bytes_per_element"] or k < 1:
+            return None, None
+        products = 4 + 5 * (k - 1)
+        measured += products * d * d * cap["bytes_per_element"][d]
+    algorithmic = iteration_bytes(power, opts, root_dims, root_iters)
+    return measured / launches, algorithmic / launches
+
+
+def iteration_bytes(power: float, opts, root_dims, root_iters):
+    """Algorithmic DRAM bytes of the step's iteration-stage products with the
+    default options: 6 B of digits per element for each distinct operand read
+    and 6 B written.  p = 4 takes quadratic steps (4 products in the first
+    iteration: 3 with one operand and M' with two, 13.5 B per element on
+    average; 5 after, 14.4 B); p = 2 takes linear steps (D = M M and M', then X'
+    too: 30 B, then 48 B per element and iteration).  None for other options."""
+    if opts:
+        return None
+    total = 0.0
+    for d, k in zip(root_dims, root_iters):
+        if k < 1:
+            continue
+        if power == -0.25:
+            total += (54.0 + 72.0 * (k - 1)) * d * d
+        elif power == -0.5:
+            total += (30.0 + 48.0 * (k - 1)) * d * d
+        else:
+            return None
+    return total
 
 
 def load_peaks():
@@ -423,6 +458,7 @@ def main():
     ns_ms, ns_flops, gemm_ms, gemm_n, root_flops, issued_flops = 0.0, 0.0, 0.0, 0, 0.0, 0.0
     stage_ms = [0.0, 0.0, 0.0, 0.0]
     iters_seen = []
+    last_iters = []
     # workloads whose data fit in L2 (the single 256x128 matrix) get an L2 flush
     # (a 256 MB write) between timed steps, outside the steps' events
     flush = torch.empty((64 << 20,), device=dev) if w.index == 0 else None
@@ -445,6 +481,7 @@ def main():
             gemm_n += gn
             it, _, _, _ = sr.precond_get_stats(pc.h, nroots)
             iters_seen.append(statistics.mean(it))
+            last_iters = list(it)
         barrier()
     elapsed = sum(a.elapsed_time(b) for a, b in evs) / 1e3
     gpu_launches = sr.precond_launch_count(pc.h) - launches0
@@ -511,7 +548,9 @@ def main():
     peak = peaks["bf16_tflops_sustained"]
     # issued: tiles actually run (upper triangles of symmetric products) x 6 bf16 digit products
     issued = (issued_flops / (gemm_ms / 1e3) / 1e12) if gemm_ms > 0 else None
-    traffic, traffic_alg = captured_traffic(w.index)
+    root_dims = [d for m, n in shapes for d in (m, n)] if w.kind == "step" else list(w.dims)
+    traffic, traffic_alg = captured_traffic(w.index, power, opts, root_dims, last_iters,
+                                            gemm_n / args.steps if args.steps else 0)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": (achieved / peak) if achieved else None, "traffic": traffic,
                 "traffic_algorithmic": traffic_alg,
@@ -519,6 +558,13 @@ def main():
                 "peak_kind": f"bf16 dense, sustained ({peaks['source']})",
                 "issued_tflops": issued, "issued_frac": (issued / peak) if issued else None,
                 "avg_launch_ms": gemm_ms / gemm_n if gemm_n else None}
+    # the same products seen from HBM: algorithmic bytes over the GEMMs' event time (the
+    # latency-bound small workloads are far from both roofs)
+    alg_bytes = iteration_bytes(power, opts, root_dims, last_iters)
+    if alg_bytes is not None and gemm_ms > 0:
+        gbs = alg_bytes / (gemm_ms / args.steps / 1e3) / 1e9
+        roofline["hbm_view"] = {"achieved_algorithmic_gbs": gbs, "peak_gbs": peaks["hbm_gbs"],
+                                "frac": gbs / peaks["hbm_gbs"], "bytes_per_step": alg_bytes}
     clk_summary = clk.summary()
     if clk_summary.get("sm_mhz") and achieved:
         # secondary view: against the tensor cores' nominal dense bf16 rate at the

@@ -18,19 +18,22 @@
 // sums in registers while the MMAs of the next chunk run.
 //
 // Pipeline: TMA (3-D tensor maps {K, rows, batch}, 64-byte swizzle, K block 32)
-// into a 3-stage shared-memory ring; one elected thread issues tcgen05.mma
+// into a 4-stage shared-memory ring (48 KB per stage: three planes of A and B); one elected thread issues tcgen05.mma
 // (kind::f16, bf16, M = N = 128, K = 16).  Warp roles (320 threads): warp 0 TMA
 // producer, warp 1 TMEM owner and MMA issuer, warps 2..9 drain and epilogue (two
 // per tensor-memory lane quadrant, 64 columns each).
 //
 // The epilogue forms the output element (the product plus the element-wise
-// terms) and writes it in its consumer's format: digits with the tile's
-// per-(row, block) scales for products that feed further products (and the
-// mirrored tile for symmetric products, so results are exactly symmetric), the
-// caller's fp32 state for the Gram EMA, or the caller's update.  Digit outputs
-// leave through a 16 KB shared staging area, one plane of half a tile per
-// round, stored by TMA (128-byte swizzle), so no warp issues row-scattered
-// global stores; the element-wise input is taken from the operand ring.
+// terms; that input is the A operand itself for every product of the
+// iteration, so it is read from the operand ring as the K loop passes the
+// tile's diagonal columns) and writes it in its consumer's format: digits with
+// the tile's per-(row, block) scales for products that feed further products
+// (and the mirrored tile for symmetric products, so results are exactly
+// symmetric), the caller's fp32 state for the Gram EMA, or the caller's
+// update.  The drain warps park the finished sums in tensor memory, take the
+// row maxima (direct scales) and column maxima (mirrored scales), then write
+// the digit planes in 16-byte vectors staged through a per-warp shared
+// scratch, so every global store is a full 16-byte piece of a row.
 //
 // Every mbarrier wait is bounded.  On a time-out the kernel records an error
 // word and raises a shared abort flag: every other wait then gives up at once,

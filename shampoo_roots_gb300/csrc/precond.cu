@@ -633,15 +633,14 @@ Epi base_epi(const Ctx& c, int kind, int rows, int cols) {
 }
 
 // Tensor map of one digit plane of a slab: operand boxes {K block 32, 128 rows}
-// with 64-byte swizzle (the MMA operand layout), or epilogue boxes {64, 64}
-// with 128-byte swizzle (the staging area of the epilogue's input and output).
-int encode_map(precond_ctx* h, CUtensorMap* map, void* base, const Slab& s, int box_rows, bool epilogue = false) {
+// with 64-byte swizzle (the MMA operand layout).
+int encode_map(precond_ctx* h, CUtensorMap* map, void* base, const Slab& s, int box_rows) {
   cuuint64_t dims[3] = {(cuuint64_t)s.cols, (cuuint64_t)s.rows, (cuuint64_t)s.batch};
   cuuint64_t strides[2] = {(cuuint64_t)s.ld * 2, (cuuint64_t)s.ld * 2 * s.rows};
-  cuuint32_t box[3] = {(cuuint32_t)(epilogue ? 64 : TC_BK), (cuuint32_t)(epilogue ? 64 : box_rows), 1};
+  cuuint32_t box[3] = {(cuuint32_t)TC_BK, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, epilogue ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     fprintf(stderr, "libprecond: cuTensorMapEncodeTiled failed (%d)\n", (int)r);
@@ -651,11 +650,10 @@ int encode_map(precond_ctx* h, CUtensorMap* map, void* base, const Slab& s, int 
 }
 
 // Batched product C_b = A_b B_b^T in the engine of the operands.
-// Cs / Ins: the slabs of a digit output (EPI_AFF, EPI_M, EPI_VT) and of the
-// element-wise input (EPI_AFF, EPI_M) of the tcgen05 engine, for their tensor maps.
+// Ins: the slab of the element-wise input (EPI_AFF, EPI_M) of the tcgen05
+// engine, which must be A itself (the epilogue reads it from the operand ring).
 int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int K, const int* aidx,
-         const int* bidx, const Epi& e0, int batch, bool sym = false, const Slab* Cs = nullptr,
-         const Slab* Ins = nullptr) {
+         const int* bidx, const Epi& e0, int batch, bool sym = false, const Slab* Ins = nullptr) {
   Epi e = e0;
   if (eng == ENGINE_F64) {
     GemmF64Args g;
@@ -864,7 +862,7 @@ int launch_iterations(const Ctx& c) {
         ea.beta_in = beta_in;
         ea.gamma = 0.0;
         int rc2;
-        if ((rc2 = gemm(cc, eng, A, B, d, d, d, nullptr, nullptr, ea, nb, true, &C, &In))) return rc2;
+        if ((rc2 = gemm(cc, eng, A, B, d, d, d, nullptr, nullptr, ea, nb, true, &In))) return rc2;
         ++n;
         return PRECOND_OK;
       };
@@ -937,7 +935,7 @@ int launch_iterations(const Ctx& c) {
       // which also removes the antisymmetric mode the iteration would amplify
       // M' = M P (P = D or F, a polynomial in M: it commits with M), so that the element-wise
       // input M is the product's first operand
-      if ((rcode = gemm(cm, eng, r.M[cur], *Pk, d, d, d, nullptr, nullptr, em, nb, true, &r.M[nxt], &r.M[cur])))
+      if ((rcode = gemm(cm, eng, r.M[cur], *Pk, d, d, d, nullptr, nullptr, em, nb, true, &r.M[cur])))
         return rcode;
       ++n;
       if (br) {
@@ -1037,7 +1035,7 @@ int run_step(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream_t 
     const Slab& G = tc ? s.Gq : s.Gd;
     const Slab& VT = tc ? s.VTq : s.VTd;
     ev.C = c.plane(VT);
-    if ((rc = gemm(c, s.eng, G, r.Xf, s.m, s.n, s.n, nullptr, rsl, ev, nb, false, &VT))) return rc;
+    if ((rc = gemm(c, s.eng, G, r.Xf, s.m, s.n, s.n, nullptr, rsl, ev, nb, false))) return rc;
     if ((rc = gemm(c, s.eng, l.Xf, VT, s.m, s.n, s.m, lsl, nullptr, eu, nb))) return rc;
   }
   if ((rc = record(h, 4, st))) return rc;
