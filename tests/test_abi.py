@@ -166,13 +166,20 @@ def test_option_keys_match_header():
 
 def test_bench_traffic_is_dropped_when_the_kernel_changes(monkeypatch):
     """bench.py reports the captured DRAM traffic only for the kernel sources it
-    was captured on."""
+    was captured on, with the default options and the captured power."""
     import bench
-    cap = dict(bench.TRAFFIC_CAPTURES[1])
+    dims, iters = [6144] * 48 + [3072] * 16, [6] * 64
+    t, a = bench.captured_traffic(4, -0.25, {}, dims, iters, 92)
+    assert t is not None and t > a > 0
+    # 48 x 6144^2 + 16 x 3072^2 elements, 29 products each at 6 iterations, over 92 launches
+    assert a == pytest.approx((54 + 72 * 5) * (48 * 6144 ** 2 + 16 * 3072 ** 2) / 92)
+    assert bench.captured_traffic(4, -0.5, {}, dims, iters, 92) == (None, None)
+    assert bench.captured_traffic(4, -0.25, {"tol": 1e-5}, dims, iters, 92) == (None, None)
+    assert bench.captured_traffic(0, -0.25, {}, [256, 128], [6, 6], 96) == (None, None)
+    cap = dict(bench.TRAFFIC_CAPTURES[4])
     cap["sources"] = dict(cap["sources"], **{"gemm_tc.cuh": "0" * 40})
-    monkeypatch.setitem(bench.TRAFFIC_CAPTURES, 1, cap)
-    assert bench.captured_traffic(1) == (None, None)
-    assert bench.captured_traffic(0) == (None, None)
+    monkeypatch.setitem(bench.TRAFFIC_CAPTURES, 4, cap)
+    assert bench.captured_traffic(4, -0.25, {}, dims, iters, 92) == (None, None)
 
 
 def test_workspace_is_planned_on_a_host_only_handle(host):
