@@ -48,8 +48,9 @@ namespace precond {
 constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 32;
 constexpr int TC_CHUNK_KB = DIG_BLK / TC_BK;       // K blocks per chunk (4)
 constexpr int TC_PAIRS = 6;                        // digit products per K step
-constexpr int EPI_WARPS = 8;                       // two per tensor-memory lane quadrant
-constexpr int TC_THREADS = 64 + 32 * EPI_WARPS;    // producer warp, MMA warp, epilogue warps
+constexpr int EPI_WARPS = 8;                       // drain warps: two per tensor-memory lane quadrant
+constexpr int OUT_WARPS = 8;                       // output warps: 32 tile rows x 64 columns each
+constexpr int TC_THREADS = 64 + 32 * (EPI_WARPS + OUT_WARPS);   // producer, MMA, drain, output warps
 constexpr unsigned long long TC_WAIT_CYCLES = 4000000000ull;   // ~2 s at 2 GHz
 
 struct TcGemmArgs {
@@ -64,6 +65,7 @@ struct TcGemmArgs {
   const float* b_scale; long long b_sbstride; int b_srows;
   unsigned int* err;     // error word (bit 0: a wait timed out)
   unsigned long long* issued;   // may be null: += (K blocks x digit pairs) of every tile computed
+  float* scratch;        // per CTA two 128 x 128 fp32 slots: finished tiles from the drain to the output warps
 };
 
 struct TcSmem {
@@ -72,13 +74,13 @@ struct TcSmem {
   static constexpr int STAGES = 4;
   static constexpr int RING = STAGES * STAGE_BYTES;
   static constexpr int XS_LD = 17;                                      // per-warp scratch row (32-bit words)
-  static constexpr int OFF_XS = RING;                                   // per warp: 32 rows x 16 words
-  static constexpr int OFF_SB = OFF_XS + EPI_WARPS * 32 * XS_LD * 4;    // per warp: B scales of 2 chunks
-  static constexpr int OFF_RMAX = OFF_SB + EPI_WARPS * 128 * 4;         // [2 halves][128 rows]
-  static constexpr int OFF_CMAX = OFF_RMAX + 2 * TC_BM * 4;             // [4 quadrants][128 columns]
+  static constexpr int OFF_XS = RING;                                   // per output warp: 32 rows x 17 words
+  static constexpr int OFF_SB = OFF_XS + OUT_WARPS * 32 * XS_LD * 4;    // per drain warp: B scales of 2 chunks
+  static constexpr int OFF_RMAX = OFF_SB + EPI_WARPS * 128 * 4;         // [2 column halves][128 rows]
+  static constexpr int OFF_CMAX = OFF_RMAX + 2 * TC_BM * 4;             // [4 row quarters][128 columns]
   static constexpr int OFF_INV = OFF_CMAX + 4 * TC_BN * 4;              // [128] row and [128] column 1/sigma
   static constexpr int OFF_RED = OFF_INV + (TC_BM + TC_BN) * 4;         // [8] doubles
-  static constexpr int OFF_BAR = OFF_RED + EPI_WARPS * 8;
+  static constexpr int OFF_BAR = OFF_RED + OUT_WARPS * 8;
   static constexpr int BAR_BYTES = 256;
   static constexpr int BYTES = 1024 /*align*/ + OFF_BAR + BAR_BYTES;
   static constexpr int TMEM_COLS = 512;                                 // 2 chunk buffers x (S0, S1) x 128
@@ -182,20 +184,16 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// 8 consecutive fp32 columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32"
-      " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 // 16 consecutive fp32 columns of this warp's 32 lanes.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
@@ -210,31 +208,11 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
-// The value of x, opaque to the compiler: keeps per-round work inside its round
-// (otherwise the digits of all 64 values of a thread are hoisted out of the
-// round loop and held at once, far beyond the register budget).
-__device__ __forceinline__ float opaque(float x) {
-  float y;
-  asm volatile("mov.b32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-// Store 16 fp32 columns of this warp's 32 lanes into tensor memory.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-      ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])),
-        "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
-        "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15]))
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// acc[0..63] <- acc[16..63], acc[0..15]: the epilogue walks a thread's 64 columns in
-// four groups of 16 inside loops that are not unrolled (so their bodies exist once
-// in the instruction stream), always working on acc[0..15] and rotating after each
-// group; four rotations restore the order.  Register indices stay compile-time.
+// acc[0..63] <- acc[16..63], acc[0..15]: the drain reads the element-wise input for a
+// thread's 64 columns in four groups of 16 inside a loop that is not unrolled (so its
+// body exists once in the instruction stream), always adding to acc[0..15] and
+// rotating after each group; four rotations restore the order.  Register indices
+// stay compile-time.
 __device__ __forceinline__ void rotate16(float (&a)[64]) {
   float t[16];
 #pragma unroll
@@ -244,16 +222,28 @@ __device__ __forceinline__ void rotate16(float (&a)[64]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) a[48 + i] = t[i];
 }
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }   // the 8 epilogue warps
-// Barrier of the 8 epilogue warps that also returns the OR of `v` over them (a
-// decision every epilogue thread takes the same way).
-__device__ __forceinline__ bool epi_bar_or(bool v) {
+__device__ __forceinline__ void out_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }   // the 8 output warps
+// Barrier of the 8 output warps that also returns the OR of `v` over them (a
+// decision every output thread takes the same way).
+__device__ __forceinline__ bool out_bar_or(bool v) {
   uint32_t r;
   asm volatile(
       "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n"
       " bar.red.or.pred p, 1, 256, q;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(r) : "r"((uint32_t)v) : "memory");
   return r != 0;
+}
+// Columns 16 gi .. 16 gi + 15 of tile row r from a scratch slot laid out as
+// [32 column quads][128 rows][4] (L2 only: the slot is rewritten by other warps).
+__device__ __forceinline__ void load_row16(const float4* sp, int gi, int r, float (&v)[16]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float4 x = __ldcg(sp + (4 * gi + k) * TC_BM + r);
+    v[4 * k] = x.x;
+    v[4 * k + 1] = x.y;
+    v[4 * k + 2] = x.z;
+    v[4 * k + 3] = x.w;
+  }
 }
 
 // Digit-pair schedule (0-based digit indices): pair 0 is level 0 (accumulator
@@ -316,45 +306,6 @@ __device__ __forceinline__ float digit_p(float v, float inv, int p) {
   return p == 0 ? d1 : (p == 1 ? d2 : d3);
 }
 
-// 16 bf16 words (8 x uint32) -> 16 floats.
-__device__ __forceinline__ void unpack16(const uint4 (&w)[2], float (&f)[16]) {
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const uint32_t x = (u < 4) ? (&w[0].x)[u] : (&w[1].x)[u - 4];
-    f[2 * u] = __uint_as_float(x << 16);
-    f[2 * u + 1] = __uint_as_float(x & 0xFFFF0000u);
-  }
-}
-
-// Write 16 consecutive values of one output row as digits (scale `inv` = 1/sigma):
-// full 32-byte pieces per plane, or element by element where `mask` excludes some.
-__device__ __forceinline__ void store_digits16(const Plane& p, long long o, const float (&v)[16], float inv,
-                                               uint32_t mask) {
-  float d[3][16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) digits3(v[i], inv, d[0][i], d[1][i], d[2][i]);
-  __nv_bfloat16* base = reinterpret_cast<__nv_bfloat16*>(p.hi) + o;
-  if (mask == 0xFFFFu) {
-#pragma unroll
-    for (int s = 0; s < 3; ++s) {
-      uint4 w0, w1;
-      w0.x = pack_bf16x2(d[s][0], d[s][1]);   w0.y = pack_bf16x2(d[s][2], d[s][3]);
-      w0.z = pack_bf16x2(d[s][4], d[s][5]);   w0.w = pack_bf16x2(d[s][6], d[s][7]);
-      w1.x = pack_bf16x2(d[s][8], d[s][9]);   w1.y = pack_bf16x2(d[s][10], d[s][11]);
-      w1.z = pack_bf16x2(d[s][12], d[s][13]); w1.w = pack_bf16x2(d[s][14], d[s][15]);
-      uint4* q = reinterpret_cast<uint4*>(base + s * p.pstride);   // 32-byte aligned: o is a multiple of 16
-      q[0] = w0;
-      q[1] = w1;
-    }
-  } else if (mask) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (mask & (1u << i))
-#pragma unroll
-        for (int s = 0; s < 3; ++s) base[s * p.pstride + i] = __float2bfloat16_rn(d[s][i]);
-  }
-}
-
 // Persistent: CTA c takes tiles c, c + gridDim.x, ... of every batch entry.
 //
 // Element-wise input.  Every product with one (EPI_AFF, EPI_M) is launched with
@@ -385,8 +336,10 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
   auto chunk_empty = [&](uint32_t b) { return bars + 8u * (2 * SM::STAGES + 2 + b); };
   const uint32_t final_bar = bars + 8u * (2 * SM::STAGES + 4);
   const uint32_t in_done = bars + 8u * (2 * SM::STAGES + 5);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + 8 * (2 * SM::STAGES + 6));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 8 * (2 * SM::STAGES + 6) + 8);
+  auto slot_full = [&](uint32_t b) { return bars + 8u * (2 * SM::STAGES + 6 + b); };
+  auto slot_empty = [&](uint32_t b) { return bars + 8u * (2 * SM::STAGES + 8 + b); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + 8 * (2 * SM::STAGES + 10));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 8 * (2 * SM::STAGES + 10) + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool need_in = (e.kind == EPI_AFF || e.kind == EPI_M);
@@ -402,6 +355,10 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
     }
     mbar_init(final_bar, 1);
     mbar_init(in_done, EPI_WARPS);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(slot_full(b), EPI_WARPS);
+      mbar_init(slot_empty(b), OUT_WARPS);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -529,37 +486,34 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       tc_commit(final_bar);
       mbar_wait_own(final_bar, 0, g.err);
     }
-  } else {
-    // ------------------------------------------------ drain + epilogue (warps 2..9)
+  } else if (warp < 2 + EPI_WARPS) {
+    // ------------------------------------------------ drain (warps 2..9)
     // Warps w and w + 4 share a tensor-memory lane quadrant: the first owns the
-    // tile's columns 0..63, the second 64..127, of the quadrant's 32 rows.
+    // tile's columns 0..63, the second 64..127, of the quadrant's 32 rows.  After
+    // a tile's last chunk they hand its sums to the output warps through this
+    // CTA's scratch slot and go on with the next tile at once.
     const int qd = warp & 3;                // TMEM lane quadrant (tile rows qd*32 ..)
-    const int ew = warp - 2;                // epilogue warp index 0..7
+    const int ew = warp - 2;                // drain warp index 0..7
     const int own = ew >> 2;                // column half
     const int r = qd * 32 + lane;           // tile row of this thread
     float* sbw = sb_all + ew * 128;
-    uint32_t* xs = xs_all + ew * 32 * SM::XS_LD;
     const uint32_t tlane = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(own * 64);
     const double alpha_eff = (e.kind == EPI_AFF) ? e.alpha : 1.0;
     const float alpha16 = (float)(alpha_eff * (1.0 / 65536.0));
     // input term in the sums' units: (beta / alpha) 2^16 sigma / 256 (P1 + P2 + P3)
     const float in_unit = need_in ? (float)(e.beta_in / alpha_eff * 256.0) : 0.f;
-    uint32_t cq = 0, q = 0;
+    uint32_t cq = 0, q = 0, lt = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const int b = t / tiles_per_entry, tl = t % tiles_per_entry;
       if (epi_skip(e, b)) continue;
       int ti, tj;
       tile_coords(tl, tiles_m, tiles_n, g.sym, ti, tj);
       const int tile_m = ti * TC_BM, tile_n = tj * TC_BN;
-      const bool mirror = g.sym && ti != tj;
-      const bool diag = g.sym && ti == tj;
-      const bool transposed = mirror || diag || e.kind == EPI_VT;
       const int za = g.a_index ? g.a_index[b] : b;
       const int zb = g.b_index ? g.b_index[b] : b;
       const long long gr = tile_m + r;
       const bool rv = gr < g.M;
       const int c0 = tile_n + own * 64;      // first global column of this thread's half
-      const bool hv = c0 < g.N;              // the half holds at least one column of the output
       const float* sa_ptr = g.a_scale + (long long)za * g.a_sbstride + gr;
       const float* sb_ptr = g.b_scale + (long long)zb * g.b_sbstride + c0 + lane;
       const bool cv0 = c0 + lane < g.N, cv1 = c0 + 32 + lane < g.N;
@@ -629,55 +583,84 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
         tc_fence_after();
         if (okc) {
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            float v0[16], v1[16];
-            tmem_ld16(tlane + buf * 256u + h * 16, v0);
-            tmem_ld16(tlane + buf * 256u + 128u + h * 16, v1);
+          for (int h = 0; h < 8; ++h) {
+            float v0[8], v1[8];
+            tmem_ld8(tlane + buf * 256u + h * 8, v0);
+            tmem_ld8(tlane + buf * 256u + 128u + h * 8, v1);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[h * 16 + j] = fmaf((v0[j] + v1[j]) * sbc[h * 16 + j], sa, acc[h * 16 + j]);
+            for (int j = 0; j < 8; ++j) acc[h * 8 + j] = fmaf((v0[j] + v1[j]) * sbc[h * 8 + j], sa, acc[h * 8 + j]);
           }
         } else {
           ok = false;
         }
-        if (c + 1 < nchunks) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(chunk_empty(buf));
-        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(chunk_empty(buf));
       }
       q += (uint32_t)nk;
-      // The tile's sums go back into the last chunk's buffer (its S0 columns, this thread's row
-      // and half), which is released when the epilogue is done: every epilogue phase below is a
-      // loop over four 16-column groups loading from there, so its body exists once in the code
-      // (the epilogue runs once per tile; unrolled over 64 registers it would not stay in the
-      // instruction cache).
-      const uint32_t stash = tlane + ((cq - 1) & 1) * 256u;
+      if (!ok) break;                        // a role gave up: leave (every other wait does too)
+      // the tile's sums, in the output's units, to the scratch slot: [32 column quads][128 rows][4]
 #pragma unroll
       for (int j = 0; j < 64; ++j) {
         acc[j] *= alpha16;
-        if (e.kind == EPI_AFF && tile_n + own * 64 + j == gr) acc[j] += (float)e.gamma;
+        if (e.kind == EPI_AFF && c0 + j == gr) acc[j] += (float)e.gamma;
       }
+      const uint32_t slot = lt & 1;
+      if (lt >= 2 && !mbar_wait(slot_empty(slot), ((lt >> 1) - 1) & 1, g.err, abort_flag)) break;
+      float4* sp = reinterpret_cast<float4*>(g.scratch + ((size_t)blockIdx.x * 2 + slot) * (TC_BM * TC_BN));
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        float v[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = acc[16 * h + i];
-        tmem_st16(stash + 16 * h, v);
-      }
-      tmem_wait_st();
-      // ---- element values: v = alpha acc 2^-16 + beta In (+ gamma on the diagonal); then the
-      // maxima: the row over this half (elements the direct write keeps) and, for the transposed
-      // write, each column over this warp's 32 rows (elements it keeps)
+      for (int k4 = 0; k4 < 16; ++k4)
+        __stcg(sp + (own * 16 + k4) * TC_BM + r,
+               make_float4(acc[4 * k4], acc[4 * k4 + 1], acc[4 * k4 + 2], acc[4 * k4 + 3]));
+      __threadfence_block();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(slot_full(slot));
+      ++lt;
+    }
+  } else {
+    // ------------------------------------------------ output warps (10..17)
+    // Warp ow owns tile rows oq*32 .. +31 (one row per lane) and columns
+    // oh*64 .. +63 of the tiles the drain hands over, in the same order.  Pass 1
+    // takes the row maxima (the direct write's scales), the column maxima (the
+    // mirrored write's) and the residual; pass 2 writes the digits of both, or
+    // the fp32 results.
+    const int ow = warp - 2 - EPI_WARPS;
+    const int oq = ow & 3, oh = ow >> 2;    // row quarter, column half
+    const int r = oq * 32 + lane;           // tile row of this thread
+    const int cb = oh * 64;                 // first tile column of this thread
+    uint32_t* xs = xs_all + ow * 32 * SM::XS_LD;
+    uint8_t* xb = reinterpret_cast<uint8_t*>(xs);
+    uint32_t lt = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const int b = t / tiles_per_entry, tl = t % tiles_per_entry;
+      if (epi_skip(e, b)) continue;
+      int ti, tj;
+      tile_coords(tl, tiles_m, tiles_n, g.sym, ti, tj);
+      const int tile_m = ti * TC_BM, tile_n = tj * TC_BN;
+      const bool mirror = g.sym && ti != tj;
+      const bool diag = g.sym && ti == tj;
+      const bool transposed = mirror || diag || e.kind == EPI_VT;
+      const long long gr = tile_m + r;
+      const bool rv = gr < g.M;
+      const uint32_t slot = lt & 1;
+      const bool got = mbar_wait(slot_full(slot), (lt >> 1) & 1, g.err, abort_flag);
+      if (out_bar_or(!got || *abort_flag != 0)) break;
+      const float4* sp = reinterpret_cast<const float4*>(g.scratch + ((size_t)blockIdx.x * 2 + slot) * (TC_BM * TC_BN));
+      // ---- pass 1: maxima (and the residual of an M product); fp32 results need neither
       float part = 0.f, mrow = 0.f;
       const bool want_cmax = transposed && digits_out;
+      float vn[16];
+      if (digits_out) load_row16(sp, 4 * oh, r, vn);
 #pragma unroll 1
-      for (int gi = 0; gi < 4; ++gi) {
-        float m[16], v[16];
-        tmem_ld16(stash + 16 * gi, v);
+      for (int gi = 0; gi < (digits_out ? 4 : 0); ++gi) {
+        float v[16], m[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = vn[i];
+        if (gi + 1 < 4) load_row16(sp, 4 * oh + gi + 1, r, vn);     // next group in flight
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int j = 16 * gi + i, cl = own * 64 + j;
-          const bool vcol = rv && (c0 + j < g.N);
+          const int cl = cb + 16 * gi + i;
+          const bool vcol = rv && (tile_n + cl < g.N);
           const bool valid = vcol && !(diag && cl < r);
           if (valid) mrow = fmaxf(mrow, fabsf(v[i]));
           if (e.kind == EPI_M && valid) {
@@ -699,43 +682,46 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
             }
           }
           m[0] = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], 16));
-          if (lane < 16) cmax[qd * TC_BN + own * 64 + 16 * gi + lane] = m[0];
+          if (lane < 16) cmax[oq * TC_BN + cb + 16 * gi + lane] = m[0];
         }
       }
-      rmax[own * TC_BM + r] = mrow;
+      rmax[oh * TC_BM + r] = mrow;
       if (e.kind == EPI_M) {
         const float pd = warp_sum(part);
-        if (lane == 0) red[ew] = (double)pd;
+        if (lane == 0) red[ow] = (double)pd;
       }
-      epi_bar();                                       // maxima of the whole tile visible
+      out_bar();                                       // column maxima and residual parts visible
       if (digits_out) {
-        // output scales: rows of this tile (and, for a diagonal tile, its lower part
-        // mirrored in), and the rows of the mirrored tile / of V^T
-        if (own == 0) {
+        // output scales: the first column half's threads take row r of this tile (and, for a
+        // diagonal tile, its lower part mirrored in), the second half's row r of the mirrored
+        // tile / of V^T (tile column r)
+        if (oh == 0) {
           float m = fmaxf(rmax[r], rmax[TC_BM + r]);
           if (diag) m = fmaxf(m, fmaxf(fmaxf(cmax[r], cmax[TC_BN + r]), fmaxf(cmax[2 * TC_BN + r], cmax[3 * TC_BN + r])));
           const float sigma = pow2_ceil_scale(m);
           invr[r] = 1.0f / sigma;
-          if (e.kind != EPI_VT && rv && ok) *tc_scale_ptr(e.C, b, tj, gr) = sigma;
+          if (e.kind != EPI_VT && rv) *tc_scale_ptr(e.C, b, tj, gr) = sigma;
         } else if (mirror || e.kind == EPI_VT) {
-          const int cl = r;                            // one thread per tile column
-          const float m = fmaxf(fmaxf(cmax[cl], cmax[TC_BN + cl]), fmaxf(cmax[2 * TC_BN + cl], cmax[3 * TC_BN + cl]));
+          const float m = fmaxf(fmaxf(cmax[r], cmax[TC_BN + r]), fmaxf(cmax[2 * TC_BN + r], cmax[3 * TC_BN + r]));
           const float sigma = pow2_ceil_scale(m);
-          invc[cl] = 1.0f / sigma;
-          if (tile_n + cl < g.N && ok) *tc_scale_ptr(e.C, b, ti, tile_n + cl) = sigma;
+          invc[r] = 1.0f / sigma;
+          if (tile_n + r < g.N) *tc_scale_ptr(e.C, b, ti, tile_n + r) = sigma;
         }
-        epi_bar();
-        // ---- direct tile: digits of row r with its scale.  Per 16-column group and plane each
-        // lane puts its row's 32 bytes into the warp's scratch (rows 48 bytes apart), then the
-        // lanes store 16-byte pieces: two per lane, 32 rows x 32 bytes.
-        const long long rbase = (long long)tile_m + qd * 32;
-        uint8_t* xb = reinterpret_cast<uint8_t*>(xs);
-        if (e.kind != EPI_VT && hv) {
-          const float ih = invr[r];
+        out_bar();
+        const float ih = invr[r];
+        const long long rbase = (long long)tile_m + oq * 32;
+        load_row16(sp, 4 * oh, r, vn);
 #pragma unroll 1
-          for (int gi = 0; gi < 4; ++gi) {
-            float v[16];
-            tmem_ld16(stash + 16 * gi, v);
+        for (int gi = 0; gi < 4; ++gi) {
+          if (tile_n + cb + 16 * gi >= g.N) break;     // this and later groups lie beyond the output
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = vn[i];
+          if (gi + 1 < 4) load_row16(sp, 4 * oh + gi + 1, r, vn);
+          // ---- direct tile: digits of row r with its scale.  Per plane each lane puts its row's
+          // 32 bytes into the warp's scratch (rows 48 bytes apart), then the lanes store 16-byte
+          // pieces: two per lane, 32 rows x 32 bytes.  A diagonal tile keeps columns >= row only.
+          if (e.kind != EPI_VT) {
             uint32_t wv[3][8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
@@ -752,32 +738,32 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
               __syncwarp();
               __nv_bfloat16* plane = reinterpret_cast<__nv_bfloat16*>(e.C.hi) + (long long)b * e.C.bstride + p * e.C.pstride;
 #pragma unroll
-              for (int t = 0; t < 2; ++t) {
-                const int cidx = lane + 32 * t, R = cidx >> 1, hh = cidx & 1;
-                const uint4 w = *reinterpret_cast<const uint4*>(xb + R * 48 + hh * 16);
-                if (rbase + R < g.M && ok)
-                  *reinterpret_cast<uint4*>(plane + (rbase + R) * e.C.ld + c0 + 16 * gi + 8 * hh) = w;
+              for (int tt = 0; tt < 2; ++tt) {
+                const int cidx = lane + 32 * tt, R = cidx >> 1, hh = cidx & 1;
+                const int lc = cb + 16 * gi + 8 * hh;     // first tile column of the piece
+                const int lr = oq * 32 + R;               // its tile row
+                if (rbase + R < g.M) {
+                  __nv_bfloat16* dst = plane + (rbase + R) * e.C.ld + tile_n + lc;
+                  if (!diag || lc >= lr) {
+                    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(xb + R * 48 + hh * 16);
+                  } else if (lc + 7 >= lr) {
+                    const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(xb + R * 48 + hh * 16);
+                    for (int i = lr - lc; i < 8; ++i) dst[i] = src[i];
+                  }
+                }
               }
               __syncwarp();
             }
           }
-        }
-        // ---- mirrored tile (and a diagonal tile's lower part, and V^T): element (r, cl) goes to
-        // output row tile_n + cl, column tile_m + r.  Per group and plane each lane writes its 16
-        // values into the scratch column-major (16 output rows x 32 output columns), then the lanes
-        // store 16-byte pieces of 8 output columns: two per lane.
-        if (transposed) {
-          if (diag) epi_bar();                         // a diagonal tile's direct part is written
-          __nv_bfloat16* xh = reinterpret_cast<__nv_bfloat16*>(xs);
-#pragma unroll 1
-          for (int gi = 0; gi < 4; ++gi) {
-            float v[16], inv[16];
-            tmem_ld16(stash + 16 * gi, v);
+          // ---- mirrored tile (a diagonal tile's strict lower part, and V^T): element (r, cl) goes
+          // to output row tile_n + cl, column tile_m + r.  Per plane each lane writes its 16 values
+          // into the scratch column-major (16 output rows x 32 output columns), then the lanes
+          // store 16-byte pieces of 8 output columns: two per lane.
+          if (transposed) {
+            __nv_bfloat16* xh = reinterpret_cast<__nv_bfloat16*>(xs);
+            float inv[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int cl = own * 64 + 16 * gi + i;
-              inv[i] = diag ? invr[cl] : invc[cl];
-            }
+            for (int i = 0; i < 16; ++i) inv[i] = diag ? invr[cb + 16 * gi + i] : invc[cb + 16 * gi + i];
 #pragma unroll
             for (int p = 0; p < DIGITS; ++p) {
 #pragma unroll
@@ -785,12 +771,12 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
               __syncwarp();
               __nv_bfloat16* plane = reinterpret_cast<__nv_bfloat16*>(e.C.hi) + (long long)b * e.C.bstride + p * e.C.pstride;
 #pragma unroll
-              for (int t = 0; t < 2; ++t) {
-                const int cidx = lane + 32 * t, jj = cidx >> 2, k = cidx & 3;
-                const int cl = own * 64 + 16 * gi + jj;      // tile column = output row offset
-                const int lc = qd * 32 + 8 * k;             // first tile row = output column offset
+              for (int tt = 0; tt < 2; ++tt) {
+                const int cidx = lane + 32 * tt, jj = cidx >> 2, k = cidx & 3;
+                const int cl = cb + 16 * gi + jj;           // tile column = output row offset
+                const int lc = oq * 32 + 8 * k;             // first tile row = output column offset
                 const long long orow = tile_n + cl, ocol = (long long)tile_m + lc;
-                if (orow < g.N && ocol < g.M && ok) {
+                if (orow < g.N && ocol < g.M) {
                   __nv_bfloat16* dst = plane + orow * e.C.ld + ocol;
                   if (!diag || lc + 7 < cl) {
                     *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(xh + jj * 32 + 8 * k);
@@ -804,16 +790,17 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
             }
           }
         }
-      } else if (hv) {
+      } else {
         // ---- fp32 results: the caller's state (Gram EMA, and its mirrored tile), the update, or
         // a plain store.  Row-major stores pass through the warp's scratch: lanes store 2 rows x
         // 16 columns per instruction (64-byte runs); the mirrored Gram tile is stored directly
         // (for a fixed column the warp's lanes are consecutive addresses).
-        const long long rbase = (long long)tile_m + qd * 32;
+        const long long rbase = (long long)tile_m + oq * 32;
 #pragma unroll 1
         for (int gi = 0; gi < 4; ++gi) {
+          if (tile_n + cb + 16 * gi >= g.N) break;
           float v[16];
-          tmem_ld16(stash + 16 * gi, v);
+          load_row16(sp, 4 * oh + gi, r, v);
 #pragma unroll
           for (int i = 0; i < 16; ++i) xs[lane * SM::XS_LD + i] = __float_as_uint(v[i]);
           __syncwarp();
@@ -821,46 +808,45 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
           for (int k = 0; k < 16; ++k) {
             const int R = 2 * k + (lane >> 4), w = lane & 15;
             const long long row = rbase + R;
-            const int col = c0 + 16 * gi + w;
-            const int cl = own * 64 + 16 * gi + w;
-            if (row < g.M && col < g.N && ok) {
-              const float v = __uint_as_float(xs[R * SM::XS_LD + w]);
+            const int cl = cb + 16 * gi + w;
+            const int col = tile_n + cl;
+            if (row < g.M && col < g.N) {
+              const float x = __uint_as_float(xs[R * SM::XS_LD + w]);
               const long long o = row * (long long)e.cols + col;
               if (e.kind == EPI_GRAM) {
-                if (!(diag && cl < qd * 32 + R)) e.state[b][o] = fmaf(e.beta, e.state[b][o], (1.0f - e.beta) * v);
+                if (!(diag && cl < oq * 32 + R)) e.state[b][o] = fmaf(e.beta, e.state[b][o], (1.0f - e.beta) * x);
               } else if (e.kind == EPI_U) {
-                if (e.out_dtype == PRECOND_BF16) reinterpret_cast<__nv_bfloat16*>(e.out[b])[o] = __float2bfloat16_rn(v);
-                else reinterpret_cast<float*>(e.out[b])[o] = v;
+                if (e.out_dtype == PRECOND_BF16) reinterpret_cast<__nv_bfloat16*>(e.out[b])[o] = __float2bfloat16_rn(x);
+                else reinterpret_cast<float*>(e.out[b])[o] = x;
               } else if (e.kind == EPI_STORE) {
-                e.f32out[(long long)b * e.rows * e.cols + o] = v;
+                e.f32out[(long long)b * e.rows * e.cols + o] = x;
               }
             }
           }
           __syncwarp();
-          if (e.kind == EPI_GRAM && transposed && rv && ok) {
+          if (e.kind == EPI_GRAM && transposed && rv) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const int j = 16 * gi + i, cl = own * 64 + j;
-              if (c0 + j < g.N && !(diag && cl <= r)) {
-                float* sp = e.state[b] + (long long)(c0 + j) * e.cols + gr;
-                *sp = fmaf(e.beta, *sp, (1.0f - e.beta) * v[i]);
+              const int cl = cb + 16 * gi + i;
+              if (tile_n + cl < g.N && !(diag && cl <= r)) {
+                float* stp = e.state[b] + (long long)(tile_n + cl) * e.cols + gr;
+                *stp = fmaf(e.beta, *stp, (1.0f - e.beta) * v[i]);
               }
             }
           }
         }
       }
-      if (e.kind == EPI_M && ew == 0) {
+      if (e.kind == EPI_M && ow == 0) {
         double sum = 0.0;
 #pragma unroll
-        for (int w = 0; w < EPI_WARPS; ++w) sum += red[w];     // fixed order: deterministic
-        if (ok) epi_m_finish(e, b, sum, g.M, tl);
+        for (int w = 0; w < OUT_WARPS; ++w) sum += red[w];     // fixed order: deterministic
+        epi_m_finish(e, b, sum, g.M, tl);
       }
-      // the stash's buffer may take the next chunks
-      tc_fence_before();
+      // the slot may take the next tile; leave together once any role has aborted
       __syncwarp();
-      if (lane == 0) mbar_arrive(chunk_empty(((cq - 1) & 1)));
-      // shared scratch free for the next tile; leave together once any role has aborted
-      if (epi_bar_or(*abort_flag != 0)) break;
+      if (lane == 0) mbar_arrive(slot_empty(slot));
+      ++lt;
+      if (out_bar_or(*abort_flag != 0)) break;
     }
   }
 

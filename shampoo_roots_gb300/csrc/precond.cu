@@ -67,6 +67,7 @@ struct RootClass {
   long long tiles = 0;
   size_t t_root = 0, t_src = 0, t_dst = 0;   // device tables (offsets)
   int kmax = 0;
+  int tc_ord = -1;                     // ordinal among the tcgen05 root classes (scratch regions)
   StepPoly steps;                      // per-iteration step polynomial coefficients
 };
 
@@ -87,6 +88,9 @@ struct Plan {
   std::vector<ShapeClass> sc;
   std::vector<RootClass> rc;
   size_t stats = 0, err = 0, partials = 0, meta = 0, meta_bytes = 0, total = 0;
+  size_t scratch = 0, scratch_slot_bytes = 0;   // tcgen05 GEMM tile hand-over slots, one region per stream
+  int scratch_slots = 0;
+  long long scratch_ctas = 0;                    // CTAs a region serves (the largest tcgen05 grid)
   long long max_tiles = 0;
   std::vector<uint8_t> meta_host;
 };
@@ -513,6 +517,28 @@ int build_plan(precond_ctx* h, Plan& P, bool step, int count, const int64_t* dim
       c.VTq = make_slab(L, ENGINE_TC, nb, c.n, c.m);
     }
   }
+  // hand-over slots of the tcgen05 GEMM: two 128 x 128 fp32 tiles per CTA (at most one CTA per
+  // SM), one region for the call's stream and one for each side stream the iteration stage may fork
+  {
+    auto tiles = [](long long rows, long long cols) { return ((rows + TC_BM - 1) / TC_BM) * ((cols + TC_BN - 1) / TC_BN); };
+    int tc_classes = 0;
+    long long most = 0;
+    for (auto& r : P.rc)
+      if (r.eng == ENGINE_TC) {
+        r.tc_ord = tc_classes++;
+        most = std::max(most, tiles(r.d, r.d) * (long long)r.roots.size());
+      }
+    for (const auto& c : P.sc)
+      if (c.eng == ENGINE_TC)
+        most = std::max(most, std::max(tiles(c.m, c.m), std::max(tiles(c.n, c.n), tiles(c.m, c.n))) *
+                                  (long long)c.mats.size());
+    if (most > 0) {
+      P.scratch_ctas = std::min<long long>(most, h->num_sms);
+      P.scratch_slots = 1 + 2 * tc_classes;
+      P.scratch_slot_bytes = (size_t)P.scratch_ctas * 2 * TC_BM * TC_BN * sizeof(float);
+      P.scratch = L.take(P.scratch_slot_bytes * P.scratch_slots);
+    }
+  }
   // meta tables
   P.meta = L.top;
   MetaWriter W(P.meta_host, P.meta);
@@ -614,6 +640,7 @@ struct Ctx {
   const Plan& P;
   char* ws;
   cudaStream_t st;
+  int sslot = 0;         // scratch region of the stream (0: the call's stream, 1 + i: side stream i)
   template <typename T>
   T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
   RootStat* stats() const { return at<RootStat>(P.stats); }
@@ -683,6 +710,7 @@ int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int 
     }
     TcGemmArgs g;
     memset(&g, 0, sizeof(g));
+    g.scratch = c.at<float>(c.P.scratch + (size_t)c.sslot * c.P.scratch_slot_bytes);
     g.M = M;
     g.N = N;
     g.K = K;
@@ -701,6 +729,8 @@ int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int 
     const long long tiles = g.sym ? tn * (tn + 1) / 2 : tn * ((M + TC_BM - 1) / TC_BM);
     e.tiles_per_entry = (unsigned int)tiles;
     dim3 grid((unsigned int)std::min<long long>(tiles * batch, (long long)c.h->num_sms), 1, 1);
+    // every CTA needs its two hand-over slots in the stream's scratch region
+    if (c.sslot >= c.P.scratch_slots || (long long)grid.x > c.P.scratch_ctas) return PRECOND_EINVAL;
     const bool timed = c.h->timing && c.h->events && c.h->in_ns;
     // iteration-stage products count the MMA work they issue (converged roots' tiles are skipped on the device)
     g.issued = c.h->in_ns ? reinterpret_cast<unsigned long long*>(c.err() + 2) : nullptr;
@@ -831,8 +861,9 @@ int launch_iterations(const Ctx& c) {
     for (size_t ri = 0; ri < ncls; ++ri) {
       const RootClass& r = c.P.rc[ri];
       if (k >= r.kmax) continue;
-      const Ctx cm{c.h, c.P, c.ws, br ? c.h->side[2 * ri] : c.st};       // M chain
-      const Ctx cx{c.h, c.P, c.ws, br ? c.h->side[2 * ri + 1] : c.st};   // X chain
+      const int so = (br && r.tc_ord >= 0) ? 1 + 2 * r.tc_ord : 0;       // scratch regions of the side streams
+      const Ctx cm{c.h, c.P, c.ws, br ? c.h->side[2 * ri] : c.st, so};           // M chain
+      const Ctx cx{c.h, c.P, c.ws, br ? c.h->side[2 * ri + 1] : c.st, so ? so + 1 : 0};   // X chain
       const int nb = (int)r.roots.size(), d = r.d, eng = r.eng;
       const int* root_of = c.at<const int>(r.t_root);
       const int cur = k & 1, nxt = (k + 1) & 1;
@@ -1190,7 +1221,10 @@ int precond_create(precond_t* out, int cuda_device) {
       delete h;
       return PRECOND_ECUDA;
     }
-    if (cudaSetDevice(cuda_device) != cudaSuccess || cudaEventCreateWithFlags(&h->upload_done, cudaEventDisableTiming) != cudaSuccess) {
+    // the SM count sizes the plans' persistent grids and their scratch regions from the first call on
+    if (cudaSetDevice(cuda_device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, cuda_device) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->upload_done, cudaEventDisableTiming) != cudaSuccess) {
       cudaGetLastError();
       delete h;
       return PRECOND_ECUDA;
@@ -1519,6 +1553,12 @@ int precond_gemm_selftest(precond_t h, int engine, int M, int N, int K, const fl
   P.stats = L.take(sizeof(RootStat));
   P.err = L.take(64);
   Slab sa = make_slab(L, eng, 1, M, K), sb = make_slab(L, eng, 1, N, K);
+  if (eng == ENGINE_TC) {
+    P.scratch_slots = 1;
+    P.scratch_ctas = std::min<long long>((long long)((M + TC_BM - 1) / TC_BM) * ((N + TC_BN - 1) / TC_BN), h->num_sms);
+    P.scratch_slot_bytes = (size_t)P.scratch_ctas * 2 * TC_BM * TC_BN * sizeof(float);
+    P.scratch = L.take(P.scratch_slot_bytes);
+  }
   if ((rc = ensure_workspace(h, L.top))) return rc;
   cudaStream_t st = (cudaStream_t)stream;
   Ctx c{h, P, (char*)h->ws, st};

@@ -165,20 +165,28 @@ def test_option_keys_match_header():
 
 
 def test_bench_traffic_is_dropped_when_the_kernel_changes(monkeypatch):
-    """bench.py reports the captured DRAM traffic only for the kernel sources it
-    was captured on, with the default options and the captured power."""
+    """bench.py scales the captured DRAM traffic by the elements each root class
+    computed, and reports it only for the kernel sources it was captured on,
+    with the default options and the captured power."""
+    import hashlib
     import bench
+    cap = dict(bench.TRAFFIC_CAPTURES[4])
+    current = {}
+    for name in cap["sources"]:
+        with open(os.path.join(ROOT, "shampoo_roots_gb300", "csrc", name), "rb") as f:
+            current[name] = hashlib.sha1(f.read()).hexdigest()
+    monkeypatch.setitem(bench.TRAFFIC_CAPTURES, 4, dict(cap, sources=current))
     dims, iters = [6144] * 48 + [3072] * 16, [6] * 64
     t, a = bench.captured_traffic(4, -0.25, {}, dims, iters, 92)
     assert t is not None and t > a > 0
     # 48 x 6144^2 + 16 x 3072^2 elements, 29 products each at 6 iterations, over 92 launches
     assert a == pytest.approx((54 + 72 * 5) * (48 * 6144 ** 2 + 16 * 3072 ** 2) / 92)
+    b = cap["bytes_per_element"]
+    assert t == pytest.approx(29 * (48 * 6144 ** 2 * b[6144] + 16 * 3072 ** 2 * b[3072]) / 92)
     assert bench.captured_traffic(4, -0.5, {}, dims, iters, 92) == (None, None)
     assert bench.captured_traffic(4, -0.25, {"tol": 1e-5}, dims, iters, 92) == (None, None)
     assert bench.captured_traffic(0, -0.25, {}, [256, 128], [6, 6], 96) == (None, None)
-    cap = dict(bench.TRAFFIC_CAPTURES[4])
-    cap["sources"] = dict(cap["sources"], **{"gemm_tc.cuh": "0" * 40})
-    monkeypatch.setitem(bench.TRAFFIC_CAPTURES, 4, cap)
+    monkeypatch.setitem(bench.TRAFFIC_CAPTURES, 4, dict(cap, sources=dict(current, **{"gemm_tc.cuh": "0" * 40})))
     assert bench.captured_traffic(4, -0.25, {}, dims, iters, 92) == (None, None)
 
 
