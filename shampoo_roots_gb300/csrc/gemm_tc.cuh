@@ -842,7 +842,14 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
         for (int w = 0; w < OUT_WARPS; ++w) sum += red[w];     // fixed order: deterministic
         epi_m_finish(e, b, sum, g.M, tl);
       }
-      // the slot may take the next tile; leave together once any role has aborted
+      // the slot's data is dead: drop its L2 lines without writing them back (the slot is
+      // rewritten two tiles later), then hand it back; leave together once any role has aborted
+      out_bar();
+      {
+        const char* lines = reinterpret_cast<const char*>(sp) + (size_t)(threadIdx.x - 32 * (2 + EPI_WARPS)) * 256;
+        asm volatile("discard.global.L2 [%0], 128;" ::"l"(lines) : "memory");
+        asm volatile("discard.global.L2 [%0], 128;" ::"l"(lines + 128) : "memory");
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(slot_empty(slot));
       ++lt;
