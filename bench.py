@@ -62,14 +62,15 @@ def rank_step_seed(rank: int, step: int) -> int:
 # per output element and product, averaged over the iteration; the bench scales
 # them by the elements each root class computed in the step.  The algorithmic
 # bytes are 6 B of digits per element for each distinct operand read and 6 B
-# written (the element-wise input is the A operand: no extra read), 14.4 B on
-# average over an iteration.  Valid only for the kernel sources the captures
-# were taken on (their SHA-1s), the default options and the quadratic p = 4
-# steps (4 products in the first iteration, 5 after).
+# written (the element-wise input is the A operand, taken from the operand
+# ring: no extra read), 14.4 B on average over an iteration.  Valid only for
+# the kernel sources the captures were taken on (their SHA-1s), the default
+# options and the quadratic p = 4 steps (4 products in the first iteration,
+# 5 after).
 TRAFFIC_CAPTURES = {
-    4: {"bytes_per_element": {6144: 35.30, 3072: 18.50}, "algorithmic_bytes_per_element": 14.4,
+    4: {"bytes_per_element": {6144: 35.71, 3072: 19.09}, "algorithmic_bytes_per_element": 14.4,
         "power": -0.25,
-        "sources": {"gemm_tc.cuh": "7ec34887fbbcafd05412ba8425b1f21b49e529a3",
+        "sources": {"gemm_tc.cuh": "62fb3e6a30f2bd1a72c176c5dd805bb12ccb467f",
                     "engine.cuh": "9f93f9fd23cc0f6ceaa695703a91b7623e3d287b",
                     "common.cuh": "bde15094817cdd9be373c93fc049db220e42550e"}},
 }
