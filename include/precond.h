@@ -96,6 +96,13 @@ typedef struct precond_ctx* precond_t;
                                          iterations from l_0 = 1e-6) or 1 (T = a I - b M, 4 products, about
                                          10 iterations).  p = 2 always takes linear steps (both degrees
                                          need 36 products there). */
+#define PRECOND_OPT_PACKED_STATE  13  /* 1 = the EMA state L[i], R[i] of precond_step is the upper triangle
+                                         only, packed row by row: d(d+1)/2 floats, element (r, c) with
+                                         r <= c at offset r d - r (r - 1) / 2 + (c - r) (half the state
+                                         memory of the full layout; "Online KL Shampoo", Appendix F).
+                                         0 = full d x d row-major state (default).  The full state is
+                                         kept exactly symmetric, so both layouts give identical roots
+                                         and updates. */
 
 /*
  * Create a handle bound to `cuda_device` (>= 0).  cuda_device = -1 creates a
@@ -116,7 +123,9 @@ int precond_destroy(precond_t h);
  *                  bf16 grads).
  *   shapes       : 2*count int64: m_0, n_0, m_1, n_1, ...  (each >= 1)
  *   L[i], R[i]   : fp32 EMA state, m_i x m_i and n_i x n_i, read and updated
- *                  in place (start from zeros for the first step).  L[i] and
+ *                  in place (start from zeros for the first step); with
+ *                  PRECOND_OPT_PACKED_STATE, their packed upper triangles
+ *                  (m_i (m_i + 1) / 2 and n_i (n_i + 1) / 2 floats).  L[i] and
  *                  R[i] must not alias each other or any other state.
  *   beta         : EMA coefficient in [0, 1)
  *   eps          : regulariser added to the eigenvalues of the unit-trace

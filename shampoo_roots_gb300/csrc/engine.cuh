@@ -181,6 +181,12 @@ enum EpiKind {
   EPI_AFF   = 5,  // C_b = alpha acc + beta In_b + gamma I
 };
 
+// Offset of element (i, j), i <= j, of a d x d symmetric matrix stored as its
+// upper triangle packed row by row.
+__host__ __device__ __forceinline__ long long packed_offset(long long i, long long j, long long d) {
+  return i * d - i * (i - 1) / 2 + (j - i);
+}
+
 struct Epi {
   int kind;
   int rows, cols;            // output extent (M x N of the GEMM)
@@ -197,6 +203,7 @@ struct Epi {
   long long partials_stride;
   // EPI_GRAM
   float* const* state;       // per batch entry: caller's fp32 state matrix (rows x cols)
+  int state_packed;          // 1: the state is the upper triangle packed row by row (rows == cols)
   float beta;
   // EPI_U
   void* const* out;          // per batch entry: destination (rows x cols)
@@ -224,8 +231,9 @@ __device__ __forceinline__ double epi_apply_f64(const Epi& e, int b, long long i
       return r * r;
     }
     case EPI_GRAM: {
+      if (e.state_packed && i > j) return 0.0;   // the lower triangle is not stored
       float* s = e.state[b];
-      const long long o = i * e.cols + j;
+      const long long o = e.state_packed ? packed_offset(i, j, e.cols) : i * e.cols + j;
       s[o] = (float)((double)e.beta * (double)s[o] + (1.0 - (double)e.beta) * acc);
       return 0.0;
     }

@@ -814,7 +814,10 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
               const float x = __uint_as_float(xs[R * SM::XS_LD + w]);
               const long long o = row * (long long)e.cols + col;
               if (e.kind == EPI_GRAM) {
-                if (!(diag && cl < oq * 32 + R)) e.state[b][o] = fmaf(e.beta, e.state[b][o], (1.0f - e.beta) * x);
+                // the direct tile is upper (diagonal tiles: from the diagonal on); a packed
+                // state stores exactly that part
+                const long long os = e.state_packed ? packed_offset(row, col, e.cols) : o;
+                if (!(diag && cl < oq * 32 + R)) e.state[b][os] = fmaf(e.beta, e.state[b][os], (1.0f - e.beta) * x);
               } else if (e.kind == EPI_U) {
                 if (e.out_dtype == PRECOND_BF16) reinterpret_cast<__nv_bfloat16*>(e.out[b])[o] = __float2bfloat16_rn(x);
                 else reinterpret_cast<float*>(e.out[b])[o] = x;
@@ -824,7 +827,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
             }
           }
           __syncwarp();
-          if (e.kind == EPI_GRAM && transposed && rv) {
+          if (e.kind == EPI_GRAM && transposed && rv && !e.state_packed) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int cl = cb + 16 * gi + i;

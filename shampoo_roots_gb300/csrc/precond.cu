@@ -105,6 +105,7 @@ struct precond_ctx {
   double fold = 0.3;                   // minimax step: T(1) >= fold * T(l)
   std::map<std::string, StepPoly> schedules;   // step schedules already computed (keyed by l0, p, fold, degree)
   int step_degree = 2;                 // 2: quadratic step polynomials at p = 4; 1: linear
+  int packed = 0;                      // 1: precond_step's EMA state is the packed upper triangle
   double ws_max = 0;
   void* ws = nullptr;
   size_t ws_cap = 0;
@@ -781,6 +782,7 @@ RootArgs root_args(const Ctx& c, const RootClass& r, float eps) {
   a.X[1] = c.plane(r.X[1]);
   a.Xf = c.plane(r.Xf);
   a.dst = c.P.step ? nullptr : c.at<float* const>(r.t_dst);
+  a.packed = c.P.step ? c.h->packed : 0;
   return a;
 }
 
@@ -1038,6 +1040,7 @@ int run_step(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream_t 
       const int dim = side == 0 ? s.m : s.n, K = side == 0 ? s.n : s.m;
       Epi e = base_epi(c, EPI_GRAM, dim, dim);
       e.state = c.at<float* const>(side == 0 ? s.t_L : s.t_R);
+      e.state_packed = h->packed;
       e.beta = beta;
       e.nonfinite_of = c.at<const int>(s.t_roots2);
       const Slab& G = tc ? (side == 0 ? s.Gq : s.GTq) : (side == 0 ? s.Gd : s.GTd);
@@ -1124,7 +1127,7 @@ std::string plan_key(const precond_ctx* h, const Plan& P, float beta, float eps)
   std::ostringstream k;
   k << P.step << ' ' << P.count << ' ' << P.nroots << ' ' << P.p << ' ' << P.dtype << ' ' << P.out_f32 << ' '
     << P.total << ' ' << P.meta << ' ' << P.meta_bytes << ' ' << P.max_tiles << ' ' << beta << ' ' << eps << ' '
-    << h->tol << ' ' << h->min_iter << ' ' << h->timing << ' ' << h->branches << ' ' << h->step_degree << ' ' << h->ws;
+    << h->tol << ' ' << h->min_iter << ' ' << h->timing << ' ' << h->branches << ' ' << h->step_degree << ' ' << h->packed << ' ' << h->ws;
   for (const auto& r : P.rc) {
     k << " r" << r.d << ',' << r.eng << ',' << r.roots.size() << ',' << r.kmax;
     for (size_t i = 0; i < r.steps.alpha.size(); ++i)
@@ -1313,6 +1316,10 @@ int precond_set_option(precond_t h, int key, double v) {
     case PRECOND_OPT_USE_GRAPH:
       if (v != 0 && v != 1) return PRECOND_EINVAL;
       h->use_graph = (int)v;
+      return PRECOND_OK;
+    case PRECOND_OPT_PACKED_STATE:
+      if (v != 0 && v != 1) return PRECOND_EINVAL;
+      h->packed = (int)v;
       return PRECOND_OK;
     case PRECOND_OPT_STEP_DEGREE:
       if (v != 1 && v != 2) return PRECOND_EINVAL;

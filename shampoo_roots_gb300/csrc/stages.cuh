@@ -121,7 +121,14 @@ struct RootArgs {
   Plane X[2];                // finish input (X buffer kfinal & 1)
   Plane Xf;                  // finish output in engine format (step), or unused
   float* const* dst;         // finish output to caller fp32 (inv_root), or null
+  int packed;                // 1: src is the upper triangle packed row by row
 };
+
+// Element (r, c) of a root's source matrix: full row-major, or packed upper triangle.
+__device__ __forceinline__ float src_at(const float* A, long long r, long long c, int d, int packed) {
+  if (!packed) return A[r * d + c];
+  return r <= c ? A[packed_offset(r, c, d)] : A[packed_offset(c, r, d)];
+}
 
 __global__ void __launch_bounds__(256) root_stats_kernel(RootArgs a) {
   const int b = blockIdx.y;
@@ -134,7 +141,7 @@ __global__ void __launch_bounds__(256) root_stats_kernel(RootArgs a) {
     // fixed order in fp64: the sums feed bounds used with a 1.01 margin
     float p1 = 0.f, p2 = 0.f;
     for (int c = lane; c < a.d; c += 32) {
-      const float v = A[(long long)r * a.d + c];
+      const float v = src_at(A, r, c, a.d, a.packed);
       if (!isfinite(v)) bad = 1;
       p1 += fabsf(v);
       p2 = fmaf(v, v, p2);
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(256) root_stats_kernel(RootArgs a) {
       const long long o = (long long)b * a.d + r;
       a.rowabs[o] = s1;
       a.rowsq[o] = s2;
-      a.diag[o] = A[(long long)r * a.d + r];
+      a.diag[o] = src_at(A, r, r, a.d, a.packed);
     }
   }
   bad = __any_sync(0xffffffffu, bad);
@@ -203,11 +210,10 @@ __global__ void __launch_bounds__(256) root_bound_kernel(RootArgs a) {
   const float* rs = in_smem ? rsh : rv;
   float best = 0.f;
   for (int r = blockIdx.x * 8 + warp; r < a.d; r += gridDim.x * 8) {
-    const float* row = A + (long long)r * a.d;
     float y = 0.f;
-    for (int c = lane; c < a.d; c += 32) y = fmaf(fabsf(row[c]), rs[c], y);
+    for (int c = lane; c < a.d; c += 32) y = fmaf(fabsf(src_at(A, r, c, a.d, a.packed)), rs[c], y);
     y = warp_sum(y);
-    const float arr = row[r];
+    const float arr = src_at(A, r, r, a.d, a.packed);
     y = y * it - fabsf(arr) * it * rs[r] + fabsf(arr * it + eps) * rs[r];   // the diagonal carries + eps
     best = fmaxf(best, y / rs[r]);
   }
@@ -269,14 +275,14 @@ __global__ void __launch_bounds__(256) root_init_f64_kernel(RootArgs a) {
       __syncthreads();
       for (int q = ty; q < 32; q += 8) {
         const int rm = c0 + q, cm = r0 + tx;    // mirrored tile (rows c0.., cols r0..)
-        tt[q][tx] = (rm < a.d && cm < a.d) ? A[(long long)rm * a.d + cm] : 0.f;
+        tt[q][tx] = (rm < a.d && cm < a.d) ? src_at(A, rm, cm, a.d, a.packed) : 0.f;
       }
       __syncthreads();
       for (int q = ty; q < 32; q += 8) {
         const int r = r0 + q, col = c0 + tx;
         if (r < a.d && col < a.d) {
           const bool dgl = (r == col);
-          const double m0 = ((double)A[(long long)r * a.d + col] + (double)tt[tx][q]) * s_ac + (dgl ? s_eps : 0.0);
+          const double m0 = ((double)src_at(A, r, col, a.d, a.packed) + (double)tt[tx][q]) * s_ac + (dgl ? s_eps : 0.0);
           f64_store(a.M0, b, r, col, m0);
           if (a.write_x1) f64_store(a.X1, b, r, col, (dgl ? al : 0.0) - be * m0);
         }
@@ -310,7 +316,7 @@ __global__ void __launch_bounds__(256) root_init_tc_kernel(RootArgs a) {
   const int c0 = blockIdx.x * 128, r0 = blockIdx.y * 32;
   for (int i = warp; i < 128; i += 8) {
     const int rm = c0 + i, cm = r0 + lane;
-    tt[i][lane] = (rm < a.d && cm < a.d) ? A[(long long)rm * a.d + cm] : 0.f;
+    tt[i][lane] = (rm < a.d && cm < a.d) ? src_at(A, rm, cm, a.d, a.packed) : 0.f;
   }
   __syncthreads();
   for (int q = warp; q < 32; q += 8) {
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(256) root_init_tc_kernel(RootArgs a) {
     for (int u = 0; u < 4; ++u) {
       const int cl = lane + 32 * u, col = c0 + cl;
       const bool dgl = (r == col);
-      const float av = (col < a.d) ? A[(long long)r * a.d + col] : 0.f;
+      const float av = (col < a.d) ? src_at(A, r, col, a.d, a.packed) : 0.f;
       float s, e;
       two_sum(av, tt[cl][q], s, e);                 // A_rc + A_cr exactly
       const float p = s * sh;

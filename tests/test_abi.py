@@ -203,3 +203,9 @@ def test_workspace_is_planned_on_a_host_only_handle(host):
     assert host.step([(8, 4)], eps=0.0) == sr.EINVAL          # a rejected call leaves the figure alone
     assert sr.precond_get_workspace(host.h)[0] == four
     assert host.lib.precond_get_workspace(None, None, None) == sr.EINVAL
+
+
+def test_packed_state_option(host):
+    assert sr.precond_set_option(host.h, sr.OPT_PACKED_STATE, 1) is None
+    assert host.lib.precond_set_option(host.h, sr.OPT_PACKED_STATE, ctypes.c_double(2.0)) == sr.EINVAL
+    assert host.step([(256, 128)]) == sr.ENODEV          # plans and validates with packed state

@@ -346,3 +346,65 @@ def test_many_small_matrices_in_one_call():
     worst, (it, res, status, _) = run_steps(shapes, steps, synth.F32, 0.9, 1e-4, -0.25, check_roots=False)
     assert all(s == 0 for s in status), status
     assert worst["U"] <= TOL, worst
+
+
+def _pack_upper(a):
+    """Row-by-row packing of the upper triangle of a square array (the library's layout)."""
+    d = a.shape[0]
+    return np.concatenate([a[r, r:] for r in range(d)])
+
+
+@pytest.mark.parametrize("engine", [1, 2])
+def test_packed_state_matches_full_state_bit_for_bit(engine):
+    """PRECOND_OPT_PACKED_STATE ("Online KL Shampoo", Appendix F, packed
+    symmetric state): the EMA state is the upper triangle packed row by row.
+    The full state is kept exactly symmetric, so three steps with either layout
+    give identical updates and roots, the packed state equals the full state's
+    upper triangle, and both meet the oracle."""
+    import torch
+    import shampoo_roots_gb300 as sr
+    shapes = [(40, 24), (17, 33)] if engine == 1 else [(300, 130), (130, 300), (257, 257), (96, 64)]
+    steps = [[synth.gradient(m, n, -0.7, synth.rng_for(23, s, i), synth.F32) for i, (m, n) in enumerate(shapes)]
+             for s in range(3)]
+
+    def run(packed):
+        pc = sr.Preconditioner(0, engine=engine, packed_state=packed)
+        if packed:
+            L = [torch.zeros(m * (m + 1) // 2, device="cuda") for m, _ in shapes]
+            R = [torch.zeros(n * (n + 1) // 2, device="cuda") for _, n in shapes]
+        else:
+            L = [torch.zeros((m, m), device="cuda") for m, _ in shapes]
+            R = [torch.zeros((n, n), device="cuda") for _, n in shapes]
+        outs, roots = [], []
+        for G in steps:
+            out = [torch.empty((m, n), device="cuda") for m, n in shapes]
+            sr.precond_step(pc.h, [to_dev(g) for g in G], L, R, 0.95, 1e-6, -0.25, out=out)
+            outs.append([o.cpu().numpy() for o in out])
+            rr = []
+            for i, (m, n) in enumerate(shapes):
+                xl, xr = torch.empty((m, m), device="cuda"), torch.empty((n, n), device="cuda")
+                sr.precond_get_root(pc.h, 2 * i, xl)
+                sr.precond_get_root(pc.h, 2 * i + 1, xr)
+                rr.append((xl.cpu().numpy(), xr.cpu().numpy()))
+            roots.append(rr)
+        _, _, status, _ = sr.precond_get_stats(pc.h, 2 * len(shapes))
+        state = ([x.cpu().numpy() for x in L], [x.cpu().numpy() for x in R])
+        pc.close()
+        return outs, roots, state, status
+
+    fo, fr, (fL, fR), fs = run(0)
+    po, pr, (pL, pR), ps = run(1)
+    assert all(s == 0 for s in fs) and all(s == 0 for s in ps), (fs, ps)
+    for a, b in zip(fL + fR, pL + pR):
+        assert np.array_equal(a, a.T)                  # the full state is exactly symmetric
+        assert np.array_equal(_pack_upper(a), b)
+    for s in range(len(steps)):
+        for i in range(len(shapes)):
+            assert np.array_equal(fo[s][i], po[s][i]), (s, i)
+            assert np.array_equal(fr[s][i][0], pr[s][i][0]) and np.array_equal(fr[s][i][1], pr[s][i][1])
+    st = oracle.OracleState(shapes)
+    for s, G in enumerate(steps):
+        Uo, XLo, XRo = oracle.precond_step(st, [g.astype(np.float64) for g in G], 0.95, 1e-6, -0.25)
+        for i in range(len(shapes)):
+            assert oracle.rel_fro(po[s][i], Uo[i]) <= TOL
+            assert oracle.rel_fro(pr[s][i][0], XLo[i]) <= TOL and oracle.rel_fro(pr[s][i][1], XRo[i]) <= TOL
