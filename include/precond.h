@@ -76,7 +76,11 @@ typedef struct precond_ctx* precond_t;
                                          27-bit digits resolve (larger Grams spread that error over
                                          many directions and meet 1e-3) */
 #define PRECOND_OPT_WORKSPACE_MAX  6  /* workspace limit in bytes; 0 = unlimited (default) */
-#define PRECOND_OPT_TIMING         7  /* 1 = record per-stage CUDA events (read by precond_get_timing) */
+#define PRECOND_OPT_TIMING         7  /* 1 = record per-stage CUDA events (read by precond_get_timing) and
+                                         events around every iteration-stage GEMM (precond_get_gemm_timing);
+                                         2 = per-stage events only (a CUDA graph then holds no event node
+                                         between the GEMMs, which costs small steps a third of their time);
+                                         0 = none (default) */
 #define PRECOND_OPT_USE_GRAPH      8  /* 1 = capture each distinct plan (shapes, options, workspace) once as a
                                          CUDA graph on a handle-owned stream and replay it, ordered after
                                          and before the caller's stream by events; the 4 most recently
@@ -178,10 +182,11 @@ int precond_get_timing(precond_t h, double ms[4], int64_t* ns_gemm_launches, dou
 /*
  * With PRECOND_OPT_TIMING on: total milliseconds of the tcgen05 GEMM launches
  * of the last call's iteration stage (CUDA events around each launch on the
- * call's stream; synchronises), their number, and the bf16 MMA FLOPs they
- * issued, counted on the device: for every tile actually computed (tiles of
- * converged roots are skipped), 2 x 128 x 128 x 32 per K block and digit
- * product.  Any output pointer may be NULL.
+ * call's stream; synchronises; -1 in timing mode 2, which records no such
+ * events), their number, and the bf16 MMA FLOPs they issued, counted on the
+ * device: for every tile actually computed (tiles of converged roots are
+ * skipped), 2 x 128 x 128 x 32 per K block and digit product.  Any output
+ * pointer may be NULL.
  */
 int precond_get_gemm_timing(precond_t h, double* ms_total, int64_t* launches, double* issued_flops);
 

@@ -732,7 +732,7 @@ int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int 
     dim3 grid((unsigned int)std::min<long long>(tiles * batch, (long long)c.h->num_sms), 1, 1);
     // every CTA needs its two hand-over slots in the stream's scratch region
     if (c.sslot >= c.P.scratch_slots || (long long)grid.x > c.P.scratch_ctas) return PRECOND_EINVAL;
-    const bool timed = c.h->timing && c.h->events && c.h->in_ns;
+    const bool timed = c.h->timing == 1 && c.h->events && c.h->in_ns;   // per-launch events: mode 1 only
     // iteration-stage products count the MMA work they issue (converged roots' tiles are skipped on the device)
     g.issued = c.h->in_ns ? reinterpret_cast<unsigned long long*>(c.err() + 2) : nullptr;
     if (timed) {
@@ -1297,8 +1297,8 @@ int precond_set_option(precond_t h, int key, double v) {
       h->ws_max = v;
       return PRECOND_OK;
     case PRECOND_OPT_TIMING:
-      if (v != 0 && v != 1) return PRECOND_EINVAL;
-      if (v == 1 && h->device >= 0 && !h->events) {
+      if (v != 0 && v != 1 && v != 2) return PRECOND_EINVAL;
+      if (v != 0 && h->device >= 0 && !h->events) {
         for (auto& e : h->ev)
           if (cudaEventCreate(&e) != cudaSuccess) return PRECOND_ECUDA;
         h->events = true;
@@ -1463,14 +1463,17 @@ int precond_get_gemm_timing(precond_t h, double* ms_total, int64_t* launches, do
   if (h->device < 0) return PRECOND_ENODEV;
   if (!h->have_last || !h->timing || !h->events) return PRECOND_EINVAL;
   CK(cudaEventSynchronize(h->ev[4]));
-  double t = 0.0;
-  for (size_t i = 0; i + 1 < h->gemm_ev_used; i += 2) {
-    float x = 0.f;
-    CK(cudaEventElapsedTime(&x, h->gemm_ev[i], h->gemm_ev[i + 1]));
-    t += x;
+  double t = -1.0;                  // mode 2: no per-launch events
+  if (h->timing == 1) {
+    t = 0.0;
+    for (size_t i = 0; i + 1 < h->gemm_ev_used; i += 2) {
+      float x = 0.f;
+      CK(cudaEventElapsedTime(&x, h->gemm_ev[i], h->gemm_ev[i + 1]));
+      t += x;
+    }
   }
   if (ms_total) *ms_total = t;
-  if (launches) *launches = (int64_t)(h->gemm_ev_used / 2);
+  if (launches) *launches = h->timing == 1 ? (int64_t)(h->gemm_ev_used / 2) : (int64_t)h->ns_launches;
   if (issued_flops) {
     unsigned long long n = 0;   // (K blocks x digit pairs) of the computed tiles, counted on the device
     CK(cudaMemcpy(&n, (char*)h->ws + h->last_plan.err + 8, sizeof(n), cudaMemcpyDeviceToHost));
