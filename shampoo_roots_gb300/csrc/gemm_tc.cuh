@@ -18,22 +18,24 @@
 // sums in registers while the MMAs of the next chunk run.
 //
 // Pipeline: TMA (3-D tensor maps {K, rows, batch}, 64-byte swizzle, K block 32)
-// into a 4-stage shared-memory ring (48 KB per stage: three planes of A and B); one elected thread issues tcgen05.mma
-// (kind::f16, bf16, M = N = 128, K = 16).  Warp roles (320 threads): warp 0 TMA
-// producer, warp 1 TMEM owner and MMA issuer, warps 2..9 drain and epilogue (two
-// per tensor-memory lane quadrant, 64 columns each).
+// into a 4-stage shared-memory ring (48 KB per stage: three planes of A and B);
+// one elected thread issues tcgen05.mma (kind::f16, bf16, M = N = 128, K = 16).
+// Warp roles (576 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
+// issuer, warps 2..9 drain (two per tensor-memory lane quadrant, 64 columns
+// each), warps 10..17 output (32 rows x 64 columns each).
 //
-// The epilogue forms the output element (the product plus the element-wise
-// terms; that input is the A operand itself for every product of the
-// iteration, so it is read from the operand ring as the K loop passes the
-// tile's diagonal columns) and writes it in its consumer's format: digits with
-// the tile's per-(row, block) scales for products that feed further products
-// (and the mirrored tile for symmetric products, so results are exactly
-// symmetric), the caller's fp32 state for the Gram EMA, or the caller's
-// update.  The drain warps park the finished sums in tensor memory, take the
-// row maxima (direct scales) and column maxima (mirrored scales), then write
-// the digit planes in 16-byte vectors staged through a per-warp shared
-// scratch, so every global store is a full 16-byte piece of a row.
+// After a tile's last chunk the drain warps hand its sums to the output warps
+// through one of the CTA's two hand-over slots in L2 and go on with the next
+// tile.  The output warps form the output element (the product plus the
+// element-wise terms; that input is the A operand itself for every product of
+// the iteration, so the drain warps add it from the operand ring as the K loop
+// passes the tile's diagonal columns) and write it in its consumer's format:
+// digits with the tile's per-(row, block) scales for products that feed
+// further products (and the mirrored tile for symmetric products, so results
+// are exactly symmetric), the caller's fp32 state for the Gram EMA, or the
+// caller's update.  A first pass over the slot takes the row maxima (direct
+// scales) and column maxima (mirrored scales); a second writes the digit
+// planes in 16-byte vectors staged through a per-warp shared scratch.
 //
 // Every mbarrier wait is bounded.  On a time-out the kernel records an error
 // word and raises a shared abort flag: every other wait then gives up at once,
