@@ -68,8 +68,8 @@ typedef struct precond_ctx* precond_t;
 #define PRECOND_OPT_TOL            1  /* stop when ||M - I||_F <= tol*sqrt(d); default 1e-4 */
 #define PRECOND_OPT_MAX_ITER       2  /* iteration cap; 0 = derived from the scalar model (default) */
 #define PRECOND_OPT_MIN_ITER       3  /* stagnation test only after this many iterations; default 4 */
-#define PRECOND_OPT_ENGINE         4  /* 0 auto (default), 1 fp64 SIMT engine, 2 tcgen05 engine */
-#define PRECOND_OPT_SMALL_DIM      5  /* auto engine: max(m,n) <= this -> fp64 SIMT engine; default 64.
+#define PRECOND_OPT_ENGINE         4  /* 0 auto (default), 1 fp64 engine, 2 tcgen05 engine */
+#define PRECOND_OPT_SMALL_DIM      5  /* auto engine: max(m,n) <= this -> fp64 engine; default 64.
                                          Tiny Grams go there: with eps = 1e-6 on a unit-trace Gram of a
                                          few rows, a rank-deficient Gram's root is set by eigenvalues
                                          1e-6 below entries of order 1, finer than the tcgen05 engine's
@@ -215,7 +215,7 @@ int precond_get_root(precond_t h, int r, float* dst, void* stream);
 /*
  * Self-test of the GEMM core (no counterpart in the method: it checks the
  * library's building block).  C = A . B^T with A (M x K), B (N x K), C (M x N)
- * fp32 device buffers, through engine 1 (fp64 SIMT) or 2 (tcgen05: operands as
+ * fp32 device buffers, through engine 1 (fp64 planes, double-float products) or 2 (tcgen05: operands as
  * three bf16 digits with a scale per row and 128-column block, exact digit
  * products); `passes` = digits per operand, 3 for engine 2 (ignored by
  * engine 1).  Synchronises `stream`.
@@ -241,7 +241,7 @@ int precond_debug_plane(precond_t h, int r, int which, float* dst, void* stream)
  * because it would synchronise the device or break a fixed memory budget.
  *
  *   X = (A / tr(A) + eps I)^power,  A and X fp32 d x d device buffers owned by
- *   the caller (X may not alias A), power -0.25f or -0.5f, fp64 SIMT engine.
+ *   the caller (X may not alias A), power -0.25f or -0.5f, fp64 engine.
  *
  * All scratch lives in one fixed file-scope device array of 4 MiB that every
  * GPU which loads this library holds until the process exits; no cudaMalloc,

@@ -6,7 +6,7 @@
 //  * root classes: roots (left / right Grams, or given SPD matrices) of the
 //    same side d and engine, batched in the bound, start, iteration and finish
 //    launches.
-// Matrices with max(m, n) <= small_dim use the fp64 SIMT engine, the others
+// Matrices with max(m, n) <= small_dim use the fp64 engine, the others
 // the tcgen05 engine (three bf16 digit planes per matrix with per-(row,
 // 128-column block) scales, exact digit products on the tensor cores).
 // Everything is enqueued on the caller's stream; the only host <-> device
@@ -501,7 +501,7 @@ int build_plan(precond_ctx* h, Plan& P, bool step, int count, const int64_t* dim
       r.steps.lo.push_back(1.0);
     }
     const long long t = r.eng == ENGINE_F64
-        ? (long long)((r.d + F64_BM - 1) / F64_BM) * ((r.d + F64_BN - 1) / F64_BN)
+        ? (long long)((r.d + DF_BM - 1) / DF_BM) * ((r.d + DF_BN - 1) / DF_BN)
         : (long long)((r.d + TC_BM - 1) / TC_BM) * ((r.d + TC_BN - 1) / TC_BN);
     P.max_tiles = std::max(P.max_tiles, t);
   }
@@ -696,7 +696,7 @@ int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int 
     g.M = M;
     g.N = N;
     g.K = K;
-    dim3 grid((N + F64_BN - 1) / F64_BN, (M + F64_BM - 1) / F64_BM, batch);
+    dim3 grid((N + DF_BN - 1) / DF_BN, (M + DF_BM - 1) / DF_BM, batch);
     e.tiles_per_entry = grid.x * grid.y;
     gemm_f64_kernel<<<grid, 256, 0, c.st>>>(g, e);
   } else {
@@ -1665,7 +1665,7 @@ extern "C" int precond_inv_root_noalloc(const float* A, int64_t d, float eps, fl
   }
   precond_ctx h;          // options only; its workspace points at the scratch
   h.device = dev;
-  h.engine = 1;           // fp64 SIMT engine
+  h.engine = 1;           // fp64 engine
   h.branches = false;     // no streams or events of its own: everything on the call's stream
   Plan P;
   const int64_t dims[1] = {d};
