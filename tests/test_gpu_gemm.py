@@ -1,8 +1,9 @@
 """GPU check of the GEMM core through the C ABI self-test entry point: the
 tcgen05 digit GEMM (three bf16 digits per operand with a power-of-two scale per
 row and 128-column block, exact digit products, 128-wide K chunks summed in
-fp32) and the fp64 SIMT GEMM against float64 numpy, on ragged shapes that span
-several tiles and chunks and on rows whose magnitudes differ by many orders."""
+fp32) and the fp64 engine's GEMM (double-float products on the fp32 pipes)
+against float64 numpy, on ragged shapes that span several tiles and chunks and
+on rows whose magnitudes differ by many orders."""
 import numpy as np
 import pytest
 
