@@ -57,8 +57,9 @@ def rank_step_seed(rank: int, step: int) -> int:
 
 # DRAM traffic of the dominant kernel, from ncu captures (dram__bytes_read.sum +
 # dram__bytes_write.sum) of one whole iteration (E, X', D, F, M') of a small
-# case per root class: 2 roots of 6144^2 and 8 roots of 3072^2, each about 2400
-# tiles of 128 x 128 (as many tiles in flight per SM as at full size).  Bytes
+# case per root class: 2 roots of 6144^2 and 8 of 3072^2 (the wide stack), 5 of
+# 4096^2 and 64 of 1024^2 (the 24-layer stack), each 2300-2600 tiles of
+# 128 x 128 (as many tiles in flight per SM as at full size).  Bytes
 # per output element and product, averaged over the iteration; the bench scales
 # them by the elements each root class computed in the step.  The algorithmic
 # bytes are 6 B of digits per element for each distinct operand read and 6 B
@@ -68,6 +69,11 @@ def rank_step_seed(rank: int, step: int) -> int:
 # after a comment-only edit of its header), the default options and the
 # quadratic p = 4 steps (4 products in the first iteration, 5 after).
 TRAFFIC_CAPTURES = {
+    1: {"bytes_per_element": {4096: 26.16, 1024: 14.99}, "algorithmic_bytes_per_element": 14.4,
+        "power": -0.25,
+        "sources": {"gemm_tc.cuh": "7647db54b391bf0a752eecaedcb702b7b85a9c39",
+                    "engine.cuh": "23828dc074daf405d0bc22da5e5d8ffca1abbfdb",
+                    "common.cuh": "bde15094817cdd9be373c93fc049db220e42550e"}},
     4: {"bytes_per_element": {6144: 35.89, 3072: 19.22}, "algorithmic_bytes_per_element": 14.4,
         "power": -0.25,
         "sources": {"gemm_tc.cuh": "7647db54b391bf0a752eecaedcb702b7b85a9c39",
