@@ -301,11 +301,47 @@ __host__ __device__ __forceinline__ void tile_coords(int tl, int tiles_m, int ti
   }
 }
 
-// Digit p (0, 1, 2) of v with 1 / sigma = inv (engine.cuh digits3), selected without indexing.
-__device__ __forceinline__ float digit_p(float v, float inv, int p) {
-  float d1, d2, d3;
-  digits3(v, inv, d1, d2, d3);
-  return p == 0 ? d1 : (p == 1 ? d2 : d3);
+// The three digits of two values at once (engine.cuh digits3) with packed fp32
+// pair arithmetic: half the instructions.  rint(y) for |y| <= 2^22 is
+// (y + 1.5 2^23) - 1.5 2^23 in round-to-nearest-even, the rounding rintf uses;
+// here |y| <= 256.  Every other step is exact, as in digits3.
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ void digits3x2(float va, float vb, float ia, float ib, float (&da)[3], float (&db)[3]) {
+  const unsigned long long magic = f2_pack(12582912.0f, 12582912.0f);        // 1.5 2^23
+  const unsigned long long s512 = f2_pack(512.0f, 512.0f);
+  unsigned long long y = f2_mul(f2_pack(va, vb), f2_pack(ia * 256.0f, ib * 256.0f));
+  const unsigned long long d1 = f2_sub(f2_add(y, magic), magic);
+  y = f2_mul(f2_sub(y, d1), s512);
+  const unsigned long long d2 = f2_sub(f2_add(y, magic), magic);
+  y = f2_mul(f2_sub(y, d2), s512);
+  const unsigned long long d3 = f2_sub(f2_add(y, magic), magic);
+  const unsigned long long p2 = f2_mul(d2, f2_pack(0.001953125f, 0.001953125f));          // 2^-9
+  const unsigned long long p3 = f2_mul(d3, f2_pack(3.814697265625e-06f, 3.814697265625e-06f));   // 2^-18
+  f2_unpack(d1, da[0], db[0]);
+  f2_unpack(p2, da[1], db[1]);
+  f2_unpack(p3, da[2], db[2]);
 }
 
 // Persistent: CTA c takes tiles c, c + gridDim.x, ... of every batch entry.
@@ -712,14 +748,11 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
         out_bar();
         const float ih = invr[r];
         const long long rbase = (long long)tile_m + oq * 32;
-        load_row16(sp, 4 * oh, r, vn);
 #pragma unroll 1
         for (int gi = 0; gi < 4; ++gi) {
           if (tile_n + cb + 16 * gi >= g.N) break;     // this and later groups lie beyond the output
           float v[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = vn[i];
-          if (gi + 1 < 4) load_row16(sp, 4 * oh + gi + 1, r, vn);
+          load_row16(sp, 4 * oh + gi, r, v);
           // ---- direct tile: digits of row r with its scale.  Per plane each lane puts its row's
           // 32 bytes into the warp's scratch (rows 48 bytes apart), then the lanes store 16-byte
           // pieces: two per lane, 32 rows x 32 bytes.  A diagonal tile keeps columns >= row only.
@@ -728,8 +761,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
               float a[3], c[3];
-              digits3(v[2 * u], ih, a[0], a[1], a[2]);
-              digits3(v[2 * u + 1], ih, c[0], c[1], c[2]);
+              digits3x2(v[2 * u], v[2 * u + 1], ih, ih, a, c);
 #pragma unroll
               for (int p = 0; p < DIGITS; ++p) wv[p][u] = pack_bf16x2(a[p], c[p]);
             }
@@ -769,7 +801,12 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
 #pragma unroll
             for (int p = 0; p < DIGITS; ++p) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) xh[i * 32 + lane] = __float2bfloat16_rn(digit_p(v[i], inv[i], p));
+              for (int i = 0; i < 16; i += 2) {
+                float da[3], db[3];
+                digits3x2(v[i], v[i + 1], inv[i], inv[i + 1], da, db);
+                xh[i * 32 + lane] = __float2bfloat16_rn(p == 0 ? da[0] : (p == 1 ? da[1] : da[2]));
+                xh[(i + 1) * 32 + lane] = __float2bfloat16_rn(p == 0 ? db[0] : (p == 1 ? db[1] : db[2]));
+              }
               __syncwarp();
               __nv_bfloat16* plane = reinterpret_cast<__nv_bfloat16*>(e.C.hi) + (long long)b * e.C.bstride + p * e.C.pstride;
 #pragma unroll
