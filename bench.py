@@ -65,18 +65,18 @@ def rank_step_seed(rank: int, step: int) -> int:
 # bytes are 6 B of digits per element for each distinct operand read and 6 B
 # written (the element-wise input is the A operand, taken from the operand
 # ring: no extra read), 14.4 B on average over an iteration.  Valid only for
-# the kernel sources the captures were taken on (their SHA-1s; gemm_tc.cuh's
-# after a comment-only edit of its header), the default options and the
-# quadratic p = 4 steps (4 products in the first iteration, 5 after).
+# the kernel sources the captures were taken on (their SHA-1s), the default
+# options and the quadratic p = 4 steps (4 products in the first iteration, 5
+# after).
 TRAFFIC_CAPTURES = {
-    1: {"bytes_per_element": {4096: 26.16, 1024: 14.99}, "algorithmic_bytes_per_element": 14.4,
+    1: {"bytes_per_element": {4096: 25.97, 1024: 14.67}, "algorithmic_bytes_per_element": 14.4,
         "power": -0.25,
-        "sources": {"gemm_tc.cuh": "7647db54b391bf0a752eecaedcb702b7b85a9c39",
+        "sources": {"gemm_tc.cuh": "9275b89b9e7f364be267f3fcb1554c6818cdf01f",
                     "engine.cuh": "23828dc074daf405d0bc22da5e5d8ffca1abbfdb",
                     "common.cuh": "bde15094817cdd9be373c93fc049db220e42550e"}},
-    4: {"bytes_per_element": {6144: 35.89, 3072: 19.22}, "algorithmic_bytes_per_element": 14.4,
+    4: {"bytes_per_element": {6144: 35.61, 3072: 18.85}, "algorithmic_bytes_per_element": 14.4,
         "power": -0.25,
-        "sources": {"gemm_tc.cuh": "7647db54b391bf0a752eecaedcb702b7b85a9c39",
+        "sources": {"gemm_tc.cuh": "9275b89b9e7f364be267f3fcb1554c6818cdf01f",
                     "engine.cuh": "23828dc074daf405d0bc22da5e5d8ffca1abbfdb",
                     "common.cuh": "bde15094817cdd9be373c93fc049db220e42550e"}},
 }
