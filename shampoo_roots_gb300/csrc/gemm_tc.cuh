@@ -210,20 +210,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
-// acc[0..63] <- acc[16..63], acc[0..15]: the drain reads the element-wise input for a
-// thread's 64 columns in four groups of 16 inside a loop that is not unrolled (so its
-// body exists once in the instruction stream), always adding to acc[0..15] and
-// rotating after each group; four rotations restore the order.  Register indices
-// stay compile-time.
-__device__ __forceinline__ void rotate16(float (&a)[64]) {
-  float t[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) t[i] = a[i];
-#pragma unroll
-  for (int i = 0; i < 48; ++i) a[i] = a[i + 16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) a[48 + i] = t[i];
-}
 __device__ __forceinline__ void out_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }   // the 8 output warps
 // Barrier of the 8 output warps that also returns the OR of `v` over them (a
 // decision every output thread takes the same way).
@@ -580,7 +566,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
           // chunk tj, row r, all three planes, resident in the ring; group gi = 16 columns
           const float iu = in_unit * sa;
           bool okr = true;
-#pragma unroll 1
+#pragma unroll
           for (int gi = 0; gi < 4; ++gi) {
             const int kb = TC_CHUNK_KB * tj + 2 * own + (gi >> 1);
             if (kb < nk) {
@@ -603,7 +589,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
                         const uint32_t x = (&w[p].x)[i >> 1];
                         f[p] = __uint_as_float((i & 1) ? (x & 0xFFFF0000u) : (x << 16));
                       }
-                      acc[8 * h8 + i] = fmaf(iu, f[0] + (f[1] + f[2]), acc[8 * h8 + i]);
+                      acc[16 * gi + 8 * h8 + i] = fmaf(iu, f[0] + (f[1] + f[2]), acc[16 * gi + 8 * h8 + i]);
                     }
                   }
                 }
@@ -611,7 +597,6 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
                 okr = false;
               }
             }
-            rotate16(acc);
           }
           if (!okr) ok = false;
           __syncwarp();
