@@ -359,11 +359,12 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
   auto chunk_full = [&](uint32_t b) { return bars + 8u * (2 * SM::STAGES + b); };
   auto chunk_empty = [&](uint32_t b) { return bars + 8u * (2 * SM::STAGES + 2 + b); };
   const uint32_t final_bar = bars + 8u * (2 * SM::STAGES + 4);
-  const uint32_t in_done = bars + 8u * (2 * SM::STAGES + 5);
   auto slot_full = [&](uint32_t b) { return bars + 8u * (2 * SM::STAGES + 6 + b); };
   auto slot_empty = [&](uint32_t b) { return bars + 8u * (2 * SM::STAGES + 8 + b); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + 8 * (2 * SM::STAGES + 10));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 8 * (2 * SM::STAGES + 10) + 8);
+  // K block k of a tile's input chunk has been read by the four drain warps of its column half
+  auto in_done = [&](uint32_t k) { return bars + 8u * (2 * SM::STAGES + 10 + k); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + 8 * (2 * SM::STAGES + 14));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 8 * (2 * SM::STAGES + 14) + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool need_in = (e.kind == EPI_AFF || e.kind == EPI_M);
@@ -378,7 +379,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       mbar_init(chunk_empty(b), EPI_WARPS);
     }
     mbar_init(final_bar, 1);
-    mbar_init(in_done, EPI_WARPS);
+    for (int k = 0; k < TC_CHUNK_KB; ++k) mbar_init(in_done(k), EPI_WARPS / 2);
     for (int b = 0; b < 2; ++b) {
       mbar_init(slot_full(b), EPI_WARPS);
       mbar_init(slot_empty(b), OUT_WARPS);
@@ -438,7 +439,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
             const long long old = (long long)q - SM::STAGES;
             const bool in_c = old >= in_cur && old < in_cur + TC_CHUNK_KB;
             const bool in_p = in_prev >= 0 && old >= in_prev && old < in_prev + TC_CHUNK_KB;
-            if ((in_c || in_p) && !mbar_wait(in_done, in_c ? par_cur : par_prev, g.err, abort_flag)) {
+            if ((in_c || in_p) && !mbar_wait(in_done((uint32_t)(old - (in_c ? in_cur : in_prev))),
+                                             in_c ? par_cur : par_prev, g.err, abort_flag)) {
               ok = false;
               break;
             }
@@ -597,10 +599,12 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
                 okr = false;
               }
             }
+            if (gi & 1) {                         // both groups of this K block read: it may be refilled
+              __syncwarp();
+              if (lane == 0) mbar_arrive(in_done(2 * own + (gi >> 1)));
+            }
           }
           if (!okr) ok = false;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(in_done);
         }
         const bool okc = mbar_wait(chunk_full(buf), (cq >> 1) & 1, g.err, abort_flag);
         tc_fence_after();
