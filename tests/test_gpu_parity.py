@@ -408,3 +408,31 @@ def test_packed_state_matches_full_state_bit_for_bit(engine):
         for i in range(len(shapes)):
             assert oracle.rel_fro(po[s][i], Uo[i]) <= TOL
             assert oracle.rel_fro(pr[s][i][0], XLo[i]) <= TOL and oracle.rel_fro(pr[s][i][1], XRo[i]) <= TOL
+
+
+def test_timing_modes_give_identical_results():
+    """PRECOND_OPT_TIMING = 1 (an event around every iteration-stage GEMM) and
+    2 (per-stage events only) give the same update bit for bit; mode 2 reports
+    no per-launch time but the same launches and issued work."""
+    import torch
+    import shampoo_roots_gb300 as sr
+    shapes = [(256, 128), (300, 130)]
+    G = [synth.gradient(m, n, -0.7, synth.rng_for(29, 0, i), synth.F32) for i, (m, n) in enumerate(shapes)]
+    res = {}
+    for mode in (1, 2):
+        pc = sr.Preconditioner(0, timing=mode)
+        L = [torch.zeros((m, m), device="cuda") for m, _ in shapes]
+        R = [torch.zeros((n, n), device="cuda") for _, n in shapes]
+        out = [torch.empty((m, n), device="cuda") for m, n in shapes]
+        sr.precond_step(pc.h, [to_dev(g) for g in G], L, R, 0.95, 1e-6, -0.25, out=out)
+        ms, launches, flops = sr.precond_get_timing(pc.h)
+        gms, gn, gis = sr.precond_get_gemm_timing(pc.h)
+        res[mode] = ([o.cpu() for o in out], ms, launches, flops, gms, gn, gis)
+        pc.close()
+    for a, b in zip(res[1][0], res[2][0]):
+        assert torch.equal(a, b)
+    for mode in (1, 2):
+        assert all(x > 0 for x in res[mode][1]), res[mode][1]
+    assert res[1][4] > 0 and res[2][4] == -1.0
+    assert res[1][5] == res[2][5] == res[1][2] > 0
+    assert res[1][6] == res[2][6] > 0 and res[1][3] == res[2][3] > 0
