@@ -69,14 +69,14 @@ def rank_step_seed(rank: int, step: int) -> int:
 # options and the quadratic p = 4 steps (4 products in the first iteration, 5
 # after).
 TRAFFIC_CAPTURES = {
-    1: {"bytes_per_element": {4096: 25.97, 1024: 14.67}, "algorithmic_bytes_per_element": 14.4,
+    1: {"bytes_per_element": {4096: 26.38, 1024: 15.06}, "algorithmic_bytes_per_element": 14.4,
         "power": -0.25,
-        "sources": {"gemm_tc.cuh": "9275b89b9e7f364be267f3fcb1554c6818cdf01f",
+        "sources": {"gemm_tc.cuh": "02b32699b597b6a9a831391f9458019225f1f6c7",
                     "engine.cuh": "23828dc074daf405d0bc22da5e5d8ffca1abbfdb",
                     "common.cuh": "bde15094817cdd9be373c93fc049db220e42550e"}},
-    4: {"bytes_per_element": {6144: 35.61, 3072: 18.85}, "algorithmic_bytes_per_element": 14.4,
+    4: {"bytes_per_element": {6144: 35.88, 3072: 19.21}, "algorithmic_bytes_per_element": 14.4,
         "power": -0.25,
-        "sources": {"gemm_tc.cuh": "9275b89b9e7f364be267f3fcb1554c6818cdf01f",
+        "sources": {"gemm_tc.cuh": "02b32699b597b6a9a831391f9458019225f1f6c7",
                     "engine.cuh": "23828dc074daf405d0bc22da5e5d8ffca1abbfdb",
                     "common.cuh": "bde15094817cdd9be373c93fc049db220e42550e"}},
 }
