@@ -556,7 +556,8 @@ def main():
     # so the per-launch time is an upper bound and the rates lower bounds.
     achieved = (root_flops / (gemm_ms / 1e3) / 1e12) if gemm_ms > 0 else None
     peak = peaks["bf16_tflops_sustained"]
-    # issued: tiles actually run (upper triangles of symmetric products) x 6 bf16 digit products
+    # issued: tiles actually run (upper triangles of symmetric products) x 6 bf16 digit products,
+    # counted once per CTA that computed them (a launch of few tiles repeats each on up to 4 CTAs)
     issued = (issued_flops / (gemm_ms / 1e3) / 1e12) if gemm_ms > 0 else None
     root_dims = [d for m, n in shapes for d in (m, n)] if w.kind == "step" else list(w.dims)
     traffic, traffic_alg = captured_traffic(w.index, power, opts, root_dims, last_iters,

@@ -107,6 +107,11 @@ typedef struct precond_ctx* precond_t;
                                          0 = full d x d row-major state (default).  The full state is
                                          kept exactly symmetric, so both layouts give identical roots
                                          and updates. */
+#define PRECOND_OPT_TILE_SPLIT    14  /* most CTAs that share one 128 x 128 tile of a tcgen05 product: 1, 2
+                                         or 4 (default 4).  A product with fewer tiles than SMs gives
+                                         each tile to the largest of 4, 2, 1 (at most this) CTAs that
+                                         still fit one per SM; each computes the whole tile and writes a
+                                         share of its outputs.  Results are identical for every value. */
 
 /*
  * Create a handle bound to `cuda_device` (>= 0).  cuda_device = -1 creates a

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(HERE, "libprecond.so")
 OK, EINVAL, ENOMEM, ECUDA, ENODEV, ENOTCONV, ENONFINITE = 0, -1, -2, -3, -4, -5, -6
 F32, BF16 = 0, 1
 OPT_TOL, OPT_MAX_ITER, OPT_MIN_ITER, OPT_ENGINE, OPT_SMALL_DIM, OPT_WORKSPACE_MAX, OPT_TIMING, OPT_USE_GRAPH, \
-    OPT_CLASSICAL, OPT_FOLD, OPT_BRANCHES, OPT_STEP_DEGREE, OPT_PACKED_STATE = range(1, 14)
+    OPT_CLASSICAL, OPT_FOLD, OPT_BRANCHES, OPT_STEP_DEGREE, OPT_PACKED_STATE, OPT_TILE_SPLIT = range(1, 15)
 
 _lib = None
 

@@ -58,6 +58,9 @@ constexpr unsigned long long TC_WAIT_CYCLES = 4000000000ull;   // ~2 s at 2 GHz
 struct TcGemmArgs {
   int M, N, K;
   int batch;             // batch entries (z extent of the tile space)
+  int split;             // CTAs per tile (1, 2 or 4; launches with few tiles): each computes the
+                         //    whole tile and writes 4 / split of every output warp's four
+                         //    16-column groups, part 0 also the scales and the residual
   int sym;               // 1: the product is symmetric (M == N): compute tiles with row block <=
                          //    column block only and write each off-diagonal tile mirrored too
   const int* a_index;    // batch entry -> z coordinate of A (null: b)
@@ -330,7 +333,10 @@ __device__ __forceinline__ void digits3x2(float va, float vb, float ia, float ib
   f2_unpack(p3, da[2], db[2]);
 }
 
-// Persistent: CTA c takes tiles c, c + gridDim.x, ... of every batch entry.
+// Persistent: CTA c takes tiles c, c + gridDim.x, ... of every batch entry.  A
+// launch with few tiles gives each tile to `split` adjacent CTAs instead: all of
+// them compute it (the MMAs are cheap at that size), and each writes a share of
+// its outputs, which cuts the output pass that bounds a lone tile's latency.
 //
 // Element-wise input.  Every product with one (EPI_AFF, EPI_M) is launched with
 // that input equal to its first operand A, so the input tile (rows tile_m..,
@@ -401,6 +407,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
   const int tiles_m = (g.M + TC_BM - 1) / TC_BM, tiles_n = (g.N + TC_BN - 1) / TC_BN;
   const int tiles_per_entry = g.sym ? tiles_n * (tiles_n + 1) / 2 : tiles_m * tiles_n;
   const int total = tiles_per_entry * g.batch;
+  const int items = total * g.split;          // (tile, part) pairs, the parts of a tile adjacent
   const int nk = (g.K + TC_BK - 1) / TC_BK;
   const int nchunks = (nk + TC_CHUNK_KB - 1) / TC_CHUNK_KB;
 
@@ -411,7 +418,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       long long in_cur = -1, in_prev = -1;      // first ring K block of the input chunk of the
       uint32_t par_cur = 0, par_prev = 0;        // current and the previous tile, and its in_done phase
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
+        const int t = u / g.split;
         const int b = t / tiles_per_entry, tl = t % tiles_per_entry;
         if (epi_skip(e, b)) continue;
         int ti, tj;
@@ -466,7 +474,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       constexpr uint32_t idesc = tc_idesc();
       uint32_t q = 0, cq = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
+        const int t = u / g.split;
         const int b = t / tiles_per_entry;
         if (epi_skip(e, b)) continue;
         for (int kb = 0; kb < nk; ++kb) {
@@ -529,7 +538,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
     // input term in the sums' units: (beta / alpha) 2^16 sigma / 256 (P1 + P2 + P3)
     const float in_unit = need_in ? (float)(e.beta_in / alpha_eff * 256.0) : 0.f;
     uint32_t cq = 0, q = 0, lt = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int u = blockIdx.x; u < items; u += gridDim.x) {
+      const int t = u / g.split;
       const int b = t / tiles_per_entry, tl = t % tiles_per_entry;
       if (epi_skip(e, b)) continue;
       int ti, tj;
@@ -658,12 +668,16 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
     uint32_t* xs = xs_all + ow * 32 * SM::XS_LD;
     uint8_t* xb = reinterpret_cast<uint8_t*>(xs);
     uint32_t lt = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int u = blockIdx.x; u < items; u += gridDim.x) {
+      const int t = u / g.split;
       const int b = t / tiles_per_entry, tl = t % tiles_per_entry;
       if (epi_skip(e, b)) continue;
       int ti, tj;
       tile_coords(tl, tiles_m, tiles_n, g.sym, ti, tj);
       const int tile_m = ti * TC_BM, tile_n = tj * TC_BN;
+      // this CTA's part of the tile's writes: column groups g_lo .. g_hi - 1 of every warp
+      const int share = u - t * g.split;
+      const int g_lo = share * (4 / g.split), g_hi = g_lo + 4 / g.split;
       const bool mirror = g.sym && ti != tj;
       const bool diag = g.sym && ti == tj;
       const bool transposed = mirror || diag || e.kind == EPI_VT;
@@ -727,18 +741,18 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
           if (diag) m = fmaxf(m, fmaxf(fmaxf(cmax[r], cmax[TC_BN + r]), fmaxf(cmax[2 * TC_BN + r], cmax[3 * TC_BN + r])));
           const float sigma = pow2_ceil_scale(m);
           invr[r] = 1.0f / sigma;
-          if (e.kind != EPI_VT && rv) *tc_scale_ptr(e.C, b, tj, gr) = sigma;
+          if (e.kind != EPI_VT && rv && share == 0) *tc_scale_ptr(e.C, b, tj, gr) = sigma;
         } else if (mirror || e.kind == EPI_VT) {
           const float m = fmaxf(fmaxf(cmax[r], cmax[TC_BN + r]), fmaxf(cmax[2 * TC_BN + r], cmax[3 * TC_BN + r]));
           const float sigma = pow2_ceil_scale(m);
           invc[r] = 1.0f / sigma;
-          if (tile_n + r < g.N) *tc_scale_ptr(e.C, b, ti, tile_n + r) = sigma;
+          if (tile_n + r < g.N && share == 0) *tc_scale_ptr(e.C, b, ti, tile_n + r) = sigma;
         }
         out_bar();
         const float ih = invr[r];
         const long long rbase = (long long)tile_m + oq * 32;
 #pragma unroll 1
-        for (int gi = 0; gi < 4; ++gi) {
+        for (int gi = g_lo; gi < g_hi; ++gi) {
           if (tile_n + cb + 16 * gi >= g.N) break;     // this and later groups lie beyond the output
           float v[16];
           load_row16(sp, 4 * oh + gi, r, v);
@@ -825,7 +839,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
         // (for a fixed column the warp's lanes are consecutive addresses).
         const long long rbase = (long long)tile_m + oq * 32;
 #pragma unroll 1
-        for (int gi = 0; gi < 4; ++gi) {
+        for (int gi = g_lo; gi < g_hi; ++gi) {
           if (tile_n + cb + 16 * gi >= g.N) break;
           float v[16];
           load_row16(sp, 4 * oh + gi, r, v);
@@ -867,7 +881,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
           }
         }
       }
-      if (e.kind == EPI_M && ow == 0) {
+      if (e.kind == EPI_M && ow == 0 && share == 0) {
         double sum = 0.0;
 #pragma unroll
         for (int w = 0; w < OUT_WARPS; ++w) sum += red[w];     // fixed order: deterministic

@@ -106,6 +106,7 @@ struct precond_ctx {
   std::map<std::string, StepPoly> schedules;   // step schedules already computed (keyed by l0, p, fold, degree)
   int step_degree = 2;                 // 2: quadratic step polynomials at p = 4; 1: linear
   int packed = 0;                      // 1: precond_step's EMA state is the packed upper triangle
+  int tile_split = 4;                  // most CTAs that share one tile of a small tcgen05 launch
   double ws_max = 0;
   void* ws = nullptr;
   size_t ws_cap = 0;
@@ -534,7 +535,8 @@ int build_plan(precond_ctx* h, Plan& P, bool step, int count, const int64_t* dim
         most = std::max(most, std::max(tiles(c.m, c.m), std::max(tiles(c.n, c.n), tiles(c.m, c.n))) *
                                   (long long)c.mats.size());
     if (most > 0) {
-      P.scratch_ctas = std::min<long long>(most, h->num_sms);
+      // a launch of fewer tiles may spread each over up to tile_split CTAs (tc_split)
+      P.scratch_ctas = std::min<long long>(most * h->tile_split, h->num_sms);
       P.scratch_slots = 1 + 2 * tc_classes;
       P.scratch_slot_bytes = (size_t)P.scratch_ctas * 2 * TC_BM * TC_BN * sizeof(float);
       P.scratch = L.take(P.scratch_slot_bytes * P.scratch_slots);
@@ -680,6 +682,15 @@ int encode_map(precond_ctx* h, CUtensorMap* map, void* base, const Slab& s, int 
 // Batched product C_b = A_b B_b^T in the engine of the operands.
 // Ins: the slab of the element-wise input (EPI_AFF, EPI_M) of the tcgen05
 // engine, which must be A itself (the epilogue reads it from the operand ring).
+// CTAs per tile of a tcgen05 launch of `work` tiles: the largest of 4, 2, 1 (at most
+// max_split) whose CTAs still fit on the GPU at one per SM.  A lone tile's latency is
+// mostly its output pass, which the split divides; the MMAs it repeats are cheap there.
+int tc_split(long long work, int num_sms, int max_split) {
+  for (int s = 4; s > 1; s >>= 1)
+    if (s <= max_split && work * s <= num_sms) return s;
+  return 1;
+}
+
 int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int K, const int* aidx,
          const int* bidx, const Epi& e0, int batch, bool sym = false, const Slab* Ins = nullptr) {
   Epi e = e0;
@@ -729,7 +740,8 @@ int gemm(const Ctx& c, int eng, const Slab& A, const Slab& B, int M, int N, int 
     const long long tn = (N + TC_BN - 1) / TC_BN;
     const long long tiles = g.sym ? tn * (tn + 1) / 2 : tn * ((M + TC_BM - 1) / TC_BM);
     e.tiles_per_entry = (unsigned int)tiles;
-    dim3 grid((unsigned int)std::min<long long>(tiles * batch, (long long)c.h->num_sms), 1, 1);
+    g.split = tc_split(tiles * batch, c.h->num_sms, c.h->tile_split);
+    dim3 grid((unsigned int)std::min<long long>(tiles * batch * g.split, (long long)c.h->num_sms), 1, 1);
     // every CTA needs its two hand-over slots in the stream's scratch region
     if (c.sslot >= c.P.scratch_slots || (long long)grid.x > c.P.scratch_ctas) return PRECOND_EINVAL;
     const bool timed = c.h->timing == 1 && c.h->events && c.h->in_ns;   // per-launch events: mode 1 only
@@ -1127,7 +1139,7 @@ std::string plan_key(const precond_ctx* h, const Plan& P, float beta, float eps)
   std::ostringstream k;
   k << P.step << ' ' << P.count << ' ' << P.nroots << ' ' << P.p << ' ' << P.dtype << ' ' << P.out_f32 << ' '
     << P.total << ' ' << P.meta << ' ' << P.meta_bytes << ' ' << P.max_tiles << ' ' << beta << ' ' << eps << ' '
-    << h->tol << ' ' << h->min_iter << ' ' << h->timing << ' ' << h->branches << ' ' << h->step_degree << ' ' << h->packed << ' ' << h->ws;
+    << h->tol << ' ' << h->min_iter << ' ' << h->timing << ' ' << h->branches << ' ' << h->step_degree << ' ' << h->packed << ' ' << h->tile_split << ' ' << h->ws;
   for (const auto& r : P.rc) {
     k << " r" << r.d << ',' << r.eng << ',' << r.roots.size() << ',' << r.kmax;
     for (size_t i = 0; i < r.steps.alpha.size(); ++i)
@@ -1328,6 +1340,10 @@ int precond_set_option(precond_t h, int key, double v) {
     case PRECOND_OPT_BRANCHES:
       if (v != 0 && v != 1) return PRECOND_EINVAL;
       h->branches = v != 0;
+      return PRECOND_OK;
+    case PRECOND_OPT_TILE_SPLIT:
+      if (v != 1 && v != 2 && v != 4) return PRECOND_EINVAL;
+      h->tile_split = (int)v;
       return PRECOND_OK;
   }
   return PRECOND_EINVAL;
@@ -1565,7 +1581,8 @@ int precond_gemm_selftest(precond_t h, int engine, int M, int N, int K, const fl
   Slab sa = make_slab(L, eng, 1, M, K), sb = make_slab(L, eng, 1, N, K);
   if (eng == ENGINE_TC) {
     P.scratch_slots = 1;
-    P.scratch_ctas = std::min<long long>((long long)((M + TC_BM - 1) / TC_BM) * ((N + TC_BN - 1) / TC_BN), h->num_sms);
+    P.scratch_ctas = std::min<long long>((long long)((M + TC_BM - 1) / TC_BM) * ((N + TC_BN - 1) / TC_BN) * h->tile_split,
+                                         h->num_sms);
     P.scratch_slot_bytes = (size_t)P.scratch_ctas * 2 * TC_BM * TC_BN * sizeof(float);
     P.scratch = L.take(P.scratch_slot_bytes);
   }

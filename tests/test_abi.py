@@ -143,6 +143,10 @@ def test_options(host):
     assert lib.precond_set_option(host.h, sr.OPT_ENGINE, 3) == sr.EINVAL
     assert lib.precond_set_option(host.h, sr.OPT_ENGINE, 2) == sr.OK
     assert lib.precond_set_option(host.h, sr.OPT_MIN_ITER, 0) == sr.EINVAL
+    for v in (0, 3, 8, 2.5):
+        assert lib.precond_set_option(host.h, sr.OPT_TILE_SPLIT, v) == sr.EINVAL
+    for v in (1, 2, 4):
+        assert lib.precond_set_option(host.h, sr.OPT_TILE_SPLIT, v) == sr.OK
     assert lib.precond_set_option(None, sr.OPT_TOL, 1e-5) == sr.EINVAL
 
 

@@ -436,3 +436,44 @@ def test_timing_modes_give_identical_results():
     assert res[1][4] > 0 and res[2][4] == -1.0
     assert res[1][5] == res[2][5] == res[1][2] > 0
     assert res[1][6] == res[2][6] > 0 and res[1][3] == res[2][3] > 0
+
+
+def test_tile_split_gives_identical_results():
+    """PRECOND_OPT_TILE_SPLIT = 1, 2, 4: small products spread each tile over that
+    many CTAs, each writing a share of its outputs; the update, the roots and
+    the iteration counts are the same bit for bit (full and packed state), and
+    the split run still meets the oracle."""
+    import torch
+    import shampoo_roots_gb300 as sr
+    shapes = [(256, 128), (300, 130), (384, 200)]
+    G = [synth.gradient(m, n, -0.7, synth.rng_for(31, 0, i), synth.F32) for i, (m, n) in enumerate(shapes)]
+    for packed in (0, 1):
+        res = {}
+        for split in (1, 2, 4):
+            pc = sr.Preconditioner(0, tile_split=split, packed_state=packed, engine=2)
+            side = (lambda d: d * (d + 1) // 2) if packed else (lambda d: d * d)
+            L = [torch.zeros(side(m), device="cuda") for m, _ in shapes]
+            R = [torch.zeros(side(n), device="cuda") for _, n in shapes]
+            if not packed:
+                L = [x.view(m, m) for x, (m, _) in zip(L, shapes)]
+                R = [x.view(n, n) for x, (_, n) in zip(R, shapes)]
+            out = [torch.empty((m, n), device="cuda") for m, n in shapes]
+            sr.precond_step(pc.h, [to_dev(g) for g in G], L, R, 0.95, 1e-6, -0.25, out=out)
+            torch.cuda.synchronize()
+            iters = sr.precond_get_stats(pc.h, 2 * len(shapes))[0]
+            roots = []
+            for i, (m, n) in enumerate(shapes):
+                xl, xr = torch.empty((m, m), device="cuda"), torch.empty((n, n), device="cuda")
+                sr.precond_get_root(pc.h, 2 * i, xl)
+                sr.precond_get_root(pc.h, 2 * i + 1, xr)
+                roots += [xl.cpu(), xr.cpu()]
+            res[split] = ([o.cpu() for o in out], [x.cpu() for x in L + R] + roots, list(iters))
+            pc.close()
+        for split in (2, 4):
+            for a, b in zip(res[1][0] + res[1][1], res[split][0] + res[split][1]):
+                assert torch.equal(a, b), (packed, split)
+            assert res[1][2] == res[split][2]
+    st = oracle.OracleState(shapes)
+    Uo, _, _ = oracle.precond_step(st, [g.astype(np.float64) for g in G], 0.95, 1e-6, -0.25)
+    for u, uo in zip(res[4][0], Uo):
+        assert oracle.rel_fro(u.double().numpy(), uo) <= TOL
