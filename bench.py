@@ -69,17 +69,21 @@ def rank_step_seed(rank: int, step: int) -> int:
 # options and the quadratic p = 4 steps (4 products in the first iteration, 5
 # after).
 TRAFFIC_CAPTURES = {
-    1: {"bytes_per_element": {4096: 26.38, 1024: 15.06}, "algorithmic_bytes_per_element": 14.4,
+    1: {"bytes_per_element": {4096: 26.20, 1024: 14.83}, "algorithmic_bytes_per_element": 14.4,
         "power": -0.25,
-        "sources": {"gemm_tc.cuh": "02b32699b597b6a9a831391f9458019225f1f6c7",
+        "sources": {"gemm_tc.cuh": "da925719f6229a3a61f1956dcaae56f682e89ce8",
                     "engine.cuh": "23828dc074daf405d0bc22da5e5d8ffca1abbfdb",
                     "common.cuh": "bde15094817cdd9be373c93fc049db220e42550e"}},
-    4: {"bytes_per_element": {6144: 35.88, 3072: 19.21}, "algorithmic_bytes_per_element": 14.4,
+    4: {"bytes_per_element": {6144: 35.74, 3072: 19.02}, "algorithmic_bytes_per_element": 14.4,
         "power": -0.25,
-        "sources": {"gemm_tc.cuh": "02b32699b597b6a9a831391f9458019225f1f6c7",
+        "sources": {"gemm_tc.cuh": "da925719f6229a3a61f1956dcaae56f682e89ce8",
                     "engine.cuh": "23828dc074daf405d0bc22da5e5d8ffca1abbfdb",
                     "common.cuh": "bde15094817cdd9be373c93fc049db220e42550e"}},
 }
+
+
+# options that change how the products run, not which products run or their operands
+LAUNCH_ONLY_OPTS = ("tile_split", "branches", "use_graph", "packed_state")
 
 
 def captured_traffic(workload: int, power: float, opts, root_dims, root_iters, launches: float):
@@ -110,8 +114,10 @@ def iteration_bytes(power: float, opts, root_dims, root_iters):
     and 6 B written.  p = 4 takes quadratic steps (4 products in the first
     iteration: 3 with one operand and M' with two, 13.5 B per element on
     average; 5 after, 14.4 B); p = 2 takes linear steps (D = M M and M', then X'
-    too: 30 B, then 48 B per element and iteration).  None for other options."""
-    if opts:
+    too: 30 B, then 48 B per element and iteration).  None for options that
+    change the products (engine, step degree, classical steps, tolerances);
+    options that change only how they run leave the bytes as they are."""
+    if any(k not in LAUNCH_ONLY_OPTS for k in opts):
         return None
     total = 0.0
     for d, k in zip(root_dims, root_iters):

@@ -189,6 +189,10 @@ def test_bench_traffic_is_dropped_when_the_kernel_changes(monkeypatch):
     assert t == pytest.approx(29 * (48 * 6144 ** 2 * b[6144] + 16 * 3072 ** 2 * b[3072]) / 92)
     assert bench.captured_traffic(4, -0.5, {}, dims, iters, 92) == (None, None)
     assert bench.captured_traffic(4, -0.25, {"tol": 1e-5}, dims, iters, 92) == (None, None)
+    # the HBM view's algorithmic bytes ignore options that only change how the products run
+    assert bench.iteration_bytes(-0.25, {"tile_split": 1, "branches": 0}, dims, iters) == \
+        bench.iteration_bytes(-0.25, {}, dims, iters) > 0
+    assert bench.iteration_bytes(-0.25, {"step_degree": 1}, dims, iters) is None
     assert bench.captured_traffic(0, -0.25, {}, [256, 128], [6, 6], 96) == (None, None)
     monkeypatch.setitem(bench.TRAFFIC_CAPTURES, 4, dict(cap, sources=dict(current, **{"gemm_tc.cuh": "0" * 40})))
     assert bench.captured_traffic(4, -0.25, {}, dims, iters, 92) == (None, None)
