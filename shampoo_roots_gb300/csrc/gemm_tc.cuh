@@ -376,6 +376,12 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
   const bool need_in = (e.kind == EPI_AFF || e.kind == EPI_M);
   const bool digits_out = (e.kind == EPI_AFF || e.kind == EPI_M || e.kind == EPI_VT);
   if (threadIdx.x == 0) {
+    // fetch the six tensor maps while the barriers and tensor memory are set up
+#pragma unroll
+    for (int p = 0; p < DIGITS; ++p) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.a[p])) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.b[p])) : "memory");
+    }
     for (int s = 0; s < SM::STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);

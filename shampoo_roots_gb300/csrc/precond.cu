@@ -798,8 +798,10 @@ RootArgs root_args(const Ctx& c, const RootClass& r, float eps) {
   return a;
 }
 
-int launch_roots_start(const Ctx& c, float eps) {
-  for (const auto& r : c.P.rc) {
+int launch_roots_start(const Ctx& c0, float eps, bool br) {
+  for (size_t ri = 0; ri < c0.P.rc.size(); ++ri) {
+    const RootClass& r = c0.P.rc[ri];
+    const Ctx c{c0.h, c0.P, c0.ws, br ? c0.h->side[2 * ri] : c0.st};     // one class per branch
     const int nb = (int)r.roots.size();
     RootArgs a = root_args(c, r, eps);
     const int rb = std::min((r.d + 7) / 8, 512);
@@ -838,13 +840,50 @@ int next_event(precond_ctx* h, size_t& used, cudaEvent_t* out) {
   return PRECOND_OK;
 }
 
+// Whether a plan's stages fork onto the handle's side streams: only when no root
+// class's products fill the GPU (fewer 128 x 128 tiles than SMs); with full
+// products the branches would only compete for the same SMs.  Two streams per
+// root class (at least two), created on first use.
+int branch_plan(const Ctx& c, bool* br) {
+  *br = c.h->branches;
+  for (const auto& r : c.P.rc) {
+    const long long tn = (r.d + TC_BN - 1) / TC_BN;
+    if ((long long)r.roots.size() * tn * (tn + 1) / 2 >= c.h->num_sms) *br = false;
+  }
+  if (*br) return side_streams(c.h, std::max<size_t>(2, 2 * c.P.rc.size()));
+  return PRECOND_OK;
+}
+
+// Side streams 0 .. n-1 wait for all work issued so far on the call's stream.
+int fork_sides(const Ctx& c, size_t& used, size_t n, cudaEvent_t* ev = nullptr) {
+  cudaEvent_t f;
+  int rc;
+  if ((rc = next_event(c.h, used, &f))) return rc;
+  CK(cudaEventRecord(f, c.st));
+  for (size_t i = 0; i < n; ++i) CK(cudaStreamWaitEvent(c.h->side[i], f, 0));
+  if (ev) *ev = f;
+  return PRECOND_OK;
+}
+
+// The call's stream waits for all work issued so far on side streams 0 .. n-1.
+int join_sides(const Ctx& c, size_t& used, size_t n) {
+  for (size_t i = 0; i < n; ++i) {
+    cudaEvent_t j;
+    int rc;
+    if ((rc = next_event(c.h, used, &j))) return rc;
+    CK(cudaEventRecord(j, c.h->side[i]));
+    CK(cudaStreamWaitEvent(c.st, j, 0));
+  }
+  return PRECOND_OK;
+}
+
 // Newton-Schulz iterations of every root class.  When the products are too small
 // to fill the GPU, each class runs on two streams of its own: the M chain (D, F, M') and the X chain (X' = X T).  The X
 // update of iteration k waits for M_k (its operand) and the M' product of
 // iteration k waits for that X update, so the X product overlaps D and F, the
 // convergence flags that M' sets are never seen early by an X update, and the
 // classes (different d) overlap one another.
-int launch_iterations(const Ctx& c) {
+int launch_iterations(const Ctx& c, bool br, size_t& used) {
   c.h->in_ns = true;
   c.h->gemm_ev_used = 0;
   struct Guard { precond_ctx* h; ~Guard() { h->in_ns = false; } } guard{c.h};
@@ -853,22 +892,8 @@ int launch_iterations(const Ctx& c) {
   int kall = 0;
   for (const auto& r : c.P.rc) kall = std::max(kall, r.kmax);
   int rcode;
-  // branch only when no class's product fills the GPU (latency-bound plans): with
-  // full products the branches would only compete for the same SMs
-  bool small = true;
-  for (const auto& r : c.P.rc) {
-    const long long tn = (r.d + TC_BN - 1) / TC_BN;
-    if ((long long)r.roots.size() * tn * (tn + 1) / 2 >= c.h->num_sms) small = false;
-  }
-  const bool br = c.h->branches && small;
-  size_t used = 0;
   cudaEvent_t fork = nullptr;
-  if (br) {
-    if ((rcode = side_streams(c.h, 2 * ncls))) return rcode;
-    if ((rcode = next_event(c.h, used, &fork))) return rcode;
-    CK(cudaEventRecord(fork, c.st));
-    for (size_t i = 0; i < 2 * ncls; ++i) CK(cudaStreamWaitEvent(c.h->side[i], fork, 0));
-  }
+  if (br && (rcode = fork_sides(c, used, 2 * ncls, &fork))) return rcode;
   std::vector<cudaEvent_t> mready(ncls, fork);     // per class: M_k sliced
   int64_t n = 0;
   for (int k = 0; k < kall; ++k) {
@@ -990,18 +1015,15 @@ int launch_iterations(const Ctx& c) {
     }
   }
   // join every branch back into the caller's stream
-  for (size_t i = 0; br && i < 2 * ncls; ++i) {
-    cudaEvent_t j;
-    if ((rcode = next_event(c.h, used, &j))) return rcode;
-    CK(cudaEventRecord(j, c.h->side[i]));
-    CK(cudaStreamWaitEvent(c.st, j, 0));
-  }
+  if (br && (rcode = join_sides(c, used, 2 * ncls))) return rcode;
   c.h->ns_launches = n;
   return PRECOND_OK;
 }
 
-int launch_finish(const Ctx& c, float eps) {
-  for (const auto& r : c.P.rc) {
+int launch_finish(const Ctx& c0, float eps, bool br) {
+  for (size_t ri = 0; ri < c0.P.rc.size(); ++ri) {
+    const RootClass& r = c0.P.rc[ri];
+    const Ctx c{c0.h, c0.P, c0.ws, br ? c0.h->side[2 * ri] : c0.st};
     const int nb = (int)r.roots.size();
     RootArgs a = root_args(c, r, eps);
     if (r.eng == ENGINE_F64)
@@ -1019,9 +1041,33 @@ int record(precond_ctx* h, int i, cudaStream_t st) {
   return PRECOND_OK;
 }
 
+// Start, iterations and finish of every root class, between the stage events 1 and 3.
+// With branches each class's start and finish kernels run on its own side stream,
+// joined back into the call's stream at the end of each stage.
+int run_roots(const Ctx& c, float eps, bool br, size_t& used) {
+  const size_t nside = 2 * c.P.rc.size();
+  int rc;
+  if (br && (rc = fork_sides(c, used, nside))) return rc;
+  if ((rc = launch_roots_start(c, eps, br))) return rc;
+  if (br && (rc = join_sides(c, used, nside))) return rc;
+  if ((rc = record(c.h, 2, c.st))) return rc;
+  if ((rc = launch_iterations(c, br, used))) return rc;
+  if ((rc = record(c.h, 3, c.st))) return rc;
+  if (br && (rc = fork_sides(c, used, nside))) return rc;
+  if ((rc = launch_finish(c, eps, br))) return rc;
+  if (br && (rc = join_sides(c, used, nside))) return rc;
+  return PRECOND_OK;
+}
+
 int run_step(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream_t st) {
   Ctx c{h, P, (char*)h->ws, st};
   int rc;
+  bool br;
+  size_t used = 0;
+  if ((rc = branch_plan(c, &br))) return rc;
+  // the Gram products fork by side onto side streams 0 and 1, which own scratch regions 1
+  // and 2 (a tcgen05 Gram implies a tcgen05 root class, hence those regions)
+  const bool gram_br = br && P.scratch_slots >= 3;
   CK(cudaMemsetAsync(c.ws + P.stats, 0, sizeof(RootStat) * P.nroots, st));
   CK(cudaMemsetAsync(c.ws + P.err, 0, 64, st));
   if ((rc = record(h, 0, st))) return rc;
@@ -1048,7 +1094,13 @@ int run_step(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream_t 
     }
     h->launches++;
     CK(cudaGetLastError());
+  }
+  if (gram_br && (rc = fork_sides(c, used, 2))) return rc;
+  for (const auto& s : P.sc) {
+    const int nb = (int)s.mats.size();
+    const bool tc = s.eng == ENGINE_TC;
     for (int side = 0; side < 2; ++side) {
+      const Ctx cg{h, P, c.ws, gram_br ? h->side[side] : st, gram_br ? 1 + side : 0};
       const int dim = side == 0 ? s.m : s.n, K = side == 0 ? s.n : s.m;
       Epi e = base_epi(c, EPI_GRAM, dim, dim);
       e.state = c.at<float* const>(side == 0 ? s.t_L : s.t_R);
@@ -1056,15 +1108,12 @@ int run_step(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream_t 
       e.beta = beta;
       e.nonfinite_of = c.at<const int>(s.t_roots2);
       const Slab& G = tc ? (side == 0 ? s.Gq : s.GTq) : (side == 0 ? s.Gd : s.GTd);
-      if ((rc = gemm(c, s.eng, G, G, dim, dim, K, nullptr, nullptr, e, nb, true))) return rc;
+      if ((rc = gemm(cg, s.eng, G, G, dim, dim, K, nullptr, nullptr, e, nb, true))) return rc;
     }
   }
+  if (gram_br && (rc = join_sides(c, used, 2))) return rc;
   if ((rc = record(h, 1, st))) return rc;
-  if ((rc = launch_roots_start(c, eps))) return rc;
-  if ((rc = record(h, 2, st))) return rc;
-  if ((rc = launch_iterations(c))) return rc;
-  if ((rc = record(h, 3, st))) return rc;
-  if ((rc = launch_finish(c, eps))) return rc;
+  if ((rc = run_roots(c, eps, br, used))) return rc;
   // ---- apply: V = G X_R (stored transposed), U = X_L V
   for (const auto& s : P.sc) {
     const int nb = (int)s.mats.size();
@@ -1091,15 +1140,14 @@ int run_step(precond_ctx* h, const Plan& P, float beta, float eps, cudaStream_t 
 int run_inv_root(precond_ctx* h, const Plan& P, float eps, cudaStream_t st) {
   Ctx c{h, P, (char*)h->ws, st};
   int rc;
+  bool br;
+  size_t used = 0;
+  if ((rc = branch_plan(c, &br))) return rc;
   CK(cudaMemsetAsync(c.ws + P.stats, 0, sizeof(RootStat) * P.nroots, st));
   CK(cudaMemsetAsync(c.ws + P.err, 0, 64, st));
   if ((rc = record(h, 0, st))) return rc;
   if ((rc = record(h, 1, st))) return rc;
-  if ((rc = launch_roots_start(c, eps))) return rc;
-  if ((rc = record(h, 2, st))) return rc;
-  if ((rc = launch_iterations(c))) return rc;
-  if ((rc = record(h, 3, st))) return rc;
-  if ((rc = launch_finish(c, eps))) return rc;
+  if ((rc = run_roots(c, eps, br, used))) return rc;
   if ((rc = record(h, 4, st))) return rc;
   return PRECOND_OK;
 }

@@ -162,7 +162,8 @@ def test_bf16_in_place_output():
 @pytest.mark.parametrize("engine", [1, 2])
 def test_graph_replay_matches_direct_launches(engine):
     """The graph path replays one capture per plan with fresh pointer tables and
-    runs the iteration stage on forked streams: it must give bit-identical
+    runs the Gram, start, iteration and finish stages of these small plans on
+    forked streams (with and without the graph): it must give bit-identical
     results to direct launches on one stream while the caller's tensors move,
     the plan changes and comes back, and the caller uses a non-default stream."""
     import torch
@@ -173,9 +174,9 @@ def test_graph_replay_matches_direct_launches(engine):
     plans = [[(200, 72), (64, 136)], [(96, 40)], [(200, 72), (64, 136)], [(200, 72), (64, 136)],
              [(40, 24)], [(48, 24)], [(56, 24)], [(64, 24)], [(72, 24)], [(200, 72), (64, 136)]]
     results = {}
-    # (graph, branches): direct launches on one stream, graph replay with the iteration
-    # stage on forked streams
-    for use_graph, branches in ((0, 0), (1, 1)):
+    # (graph, branches): direct launches on one stream, graph replay with the stages on
+    # forked streams, and direct launches on forked streams
+    for use_graph, branches in ((0, 0), (1, 1), (0, 1)):
         pc = sr.Preconditioner(0, engine=engine, small_dim=0 if engine == 2 else 512, use_graph=use_graph,
                                branches=branches)
         rng = np.random.default_rng(11)
@@ -195,15 +196,17 @@ def test_graph_replay_matches_direct_launches(engine):
                 sr.precond_step(pc.h, g, L, R, 0.9, 1e-6, -0.25, out=out, stream=side)
                 outs.append([o.cpu() for o in out])
         torch.cuda.synchronize()
-        results[use_graph] = (outs, sr.precond_launch_count(pc.h) - launches0,
-                              sr.precond_get_stats(pc.h, 4))
+        results[(use_graph, branches)] = (outs, sr.precond_launch_count(pc.h) - launches0,
+                                          sr.precond_get_stats(pc.h, 4))
         pc.close()
-    (o0, n0, s0), (o1, n1, s1) = results[0], results[1]
-    assert n0 == n1 > 0
-    for a, b in zip(o0, o1):
-        for x, y in zip(a, b):
-            assert torch.equal(x, y)
-    assert s0[0] == s1[0] and s0[2] == s1[2]
+    o0, n0, s0 = results[(0, 0)]
+    for key in ((1, 1), (0, 1)):
+        o1, n1, s1 = results[key]
+        assert n0 == n1 > 0
+        for a, b in zip(o0, o1):
+            for x, y in zip(a, b):
+                assert torch.equal(x, y)
+        assert s0[0] == s1[0] and s0[2] == s1[2]
 
 
 @pytest.mark.gpu
