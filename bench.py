@@ -69,14 +69,14 @@ def rank_step_seed(rank: int, step: int) -> int:
 # options and the quadratic p = 4 steps (4 products in the first iteration, 5
 # after).
 TRAFFIC_CAPTURES = {
-    1: {"bytes_per_element": {4096: 26.20, 1024: 14.83}, "algorithmic_bytes_per_element": 14.4,
+    1: {"bytes_per_element": {4096: 26.21, 1024: 14.81}, "algorithmic_bytes_per_element": 14.4,
         "power": -0.25,
-        "sources": {"gemm_tc.cuh": "da925719f6229a3a61f1956dcaae56f682e89ce8",
+        "sources": {"gemm_tc.cuh": "a0fc6c16a672c73f06179e4b2462dbd2f9257c2a",
                     "engine.cuh": "23828dc074daf405d0bc22da5e5d8ffca1abbfdb",
                     "common.cuh": "bde15094817cdd9be373c93fc049db220e42550e"}},
-    4: {"bytes_per_element": {6144: 35.74, 3072: 19.02}, "algorithmic_bytes_per_element": 14.4,
+    4: {"bytes_per_element": {6144: 35.74, 3072: 18.95}, "algorithmic_bytes_per_element": 14.4,
         "power": -0.25,
-        "sources": {"gemm_tc.cuh": "da925719f6229a3a61f1956dcaae56f682e89ce8",
+        "sources": {"gemm_tc.cuh": "a0fc6c16a672c73f06179e4b2462dbd2f9257c2a",
                     "engine.cuh": "23828dc074daf405d0bc22da5e5d8ffca1abbfdb",
                     "common.cuh": "bde15094817cdd9be373c93fc049db220e42550e"}},
 }
