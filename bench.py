@@ -69,14 +69,14 @@ def rank_step_seed(rank: int, step: int) -> int:
 # options and the quadratic p = 4 steps (4 products in the first iteration, 5
 # after).
 TRAFFIC_CAPTURES = {
-    1: {"bytes_per_element": {4096: 26.21, 1024: 14.81}, "algorithmic_bytes_per_element": 14.4,
+    1: {"bytes_per_element": {4096: 26.32, 1024: 14.93}, "algorithmic_bytes_per_element": 14.4,
         "power": -0.25,
-        "sources": {"gemm_tc.cuh": "a0fc6c16a672c73f06179e4b2462dbd2f9257c2a",
+        "sources": {"gemm_tc.cuh": "e2e7297b0c5888ec741d4361631d99f23c44111e",
                     "engine.cuh": "23828dc074daf405d0bc22da5e5d8ffca1abbfdb",
                     "common.cuh": "bde15094817cdd9be373c93fc049db220e42550e"}},
-    4: {"bytes_per_element": {6144: 35.74, 3072: 18.95}, "algorithmic_bytes_per_element": 14.4,
+    4: {"bytes_per_element": {6144: 35.82, 3072: 19.06}, "algorithmic_bytes_per_element": 14.4,
         "power": -0.25,
-        "sources": {"gemm_tc.cuh": "a0fc6c16a672c73f06179e4b2462dbd2f9257c2a",
+        "sources": {"gemm_tc.cuh": "e2e7297b0c5888ec741d4361631d99f23c44111e",
                     "engine.cuh": "23828dc074daf405d0bc22da5e5d8ffca1abbfdb",
                     "common.cuh": "bde15094817cdd9be373c93fc049db220e42550e"}},
 }

@@ -81,11 +81,13 @@ struct TcSmem {
   static constexpr int XS_LD = 17;                                      // per-warp scratch row (32-bit words)
   static constexpr int OFF_XS = RING;                                   // per output warp: 32 rows x 17 words
   static constexpr int OFF_SB = OFF_XS + OUT_WARPS * 32 * XS_LD * 4;    // per drain warp: B scales of 2 chunks
-  static constexpr int OFF_RMAX = OFF_SB + EPI_WARPS * 128 * 4;         // [2 column halves][128 rows]
-  static constexpr int OFF_CMAX = OFF_RMAX + 2 * TC_BM * 4;             // [4 row quarters][128 columns]
-  static constexpr int OFF_INV = OFF_CMAX + 4 * TC_BN * 4;              // [128] row and [128] column 1/sigma
-  static constexpr int OFF_RED = OFF_INV + (TC_BM + TC_BN) * 4;         // [8] doubles
-  static constexpr int OFF_BAR = OFF_RED + OUT_WARPS * 8;
+  // per hand-over slot: [2 column halves][128 rows] row maxima, [4 row quarters][128
+  // columns] column maxima, [8] residual parts (doubles)
+  static constexpr int OFF_RMAX = OFF_SB + EPI_WARPS * 128 * 4;
+  static constexpr int OFF_CMAX = OFF_RMAX + 2 * 2 * TC_BM * 4;
+  static constexpr int OFF_INV = OFF_CMAX + 2 * 4 * TC_BN * 4;          // [128] row and [128] column 1/sigma
+  static constexpr int OFF_RED = OFF_INV + (TC_BM + TC_BN) * 4;
+  static constexpr int OFF_BAR = OFF_RED + 2 * EPI_WARPS * 8;
   static constexpr int BAR_BYTES = 256;
   static constexpr int BYTES = 1024 /*align*/ + OFF_BAR + BAR_BYTES;
   static constexpr int TMEM_COLS = 512;                                 // 2 chunk buffers x (S0, S1) x 128
@@ -353,11 +355,11 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
   uint8_t* gbase = smem_raw + (base - raw);
   uint32_t* xs_all = reinterpret_cast<uint32_t*>(gbase + SM::OFF_XS);
   float* sb_all = reinterpret_cast<float*>(gbase + SM::OFF_SB);
-  float* rmax = reinterpret_cast<float*>(gbase + SM::OFF_RMAX);     // [2][128]
-  float* cmax = reinterpret_cast<float*>(gbase + SM::OFF_CMAX);     // [4][128]
+  float* rmax_all = reinterpret_cast<float*>(gbase + SM::OFF_RMAX);     // [2 slots][2][128]
+  float* cmax_all = reinterpret_cast<float*>(gbase + SM::OFF_CMAX);     // [2 slots][4][128]
   float* invr = reinterpret_cast<float*>(gbase + SM::OFF_INV);      // [128] 1 / sigma of the output rows
   float* invc = invr + TC_BM;                                       // [128] of the mirrored tile's rows
-  double* red = reinterpret_cast<double*>(gbase + SM::OFF_RED);
+  double* red_all = reinterpret_cast<double*>(gbase + SM::OFF_RED);   // [2 slots][8]
   uint8_t* tail = gbase + SM::OFF_BAR;
   const uint32_t bars = smem_u32(tail);
   auto full_bar = [&](int s) { return bars + 8u * s; };
@@ -642,7 +644,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       }
       q += (uint32_t)nk;
       if (!ok) break;                        // a role gave up: leave (every other wait does too)
-      // the tile's sums, in the output's units, to the scratch slot: [32 column quads][128 rows][4]
+      // the tile's sums in the output's units
 #pragma unroll
       for (int j = 0; j < 64; ++j) {
         acc[j] *= alpha16;
@@ -651,10 +653,71 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       const uint32_t slot = lt & 1;
       if (lt >= 2 && !mbar_wait(slot_empty(slot), ((lt >> 1) - 1) & 1, g.err, abort_flag)) break;
       float4* sp = reinterpret_cast<float4*>(g.scratch + ((size_t)blockIdx.x * 2 + slot) * (TC_BM * TC_BN));
+      // A split launch (few tiles: its latency is the output pass) takes the maxima of the
+      // finished tile here, one 16-column group at a time while the sums are in registers
+      // (each group is stored right after): row maxima (the direct write's scales), column
+      // maxima by warp butterflies (the mirrored write's) and the residual of an M product.
+      // A diagonal tile counts its upper part (with the diagonal) for the rows and its strict
+      // upper part, mirrored, for the columns.  Launches of many tiles leave this to the
+      // output warps, which have time to spare there, while the drain does not.
+      const bool drain_max = digits_out && g.split > 1;
+      const bool diag = g.sym && ti == tj, mirror = g.sym && ti != tj;
+      const bool want_cmax = drain_max && (mirror || diag || e.kind == EPI_VT);
+      float* cmx = cmax_all + slot * (4 * TC_BN) + qd * TC_BN + own * 64;
+      float part = 0.f, mrow = 0.f;
+      // bounds on this thread's column index j (tile column own * 64 + j): columns inside
+      // the output are j < jn; a diagonal tile counts j >= jr for the rows and j > jr for the
+      // columns (and twice, mirrored, in the residual); jd is the identity's column
+      const int jn = rv ? min(64, g.N - tile_n - own * 64) : 0;
+      const int jr = r - own * 64;
+      const int jlo = diag ? jr : 0, jmlo = diag ? jr + 1 : 0;
+      const int jtwo = mirror ? 0 : (diag ? jr + 1 : 64);
+      const int jd = (int)(gr - tile_n) - own * 64;
 #pragma unroll
-      for (int k4 = 0; k4 < 16; ++k4)
-        __stcg(sp + (own * 16 + k4) * TC_BM + r,
-               make_float4(acc[4 * k4], acc[4 * k4 + 1], acc[4 * k4 + 2], acc[4 * k4 + 3]));
+      for (int gi = 0; gi < 4; ++gi) {
+        if (drain_max) {
+          float m[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int j = 16 * gi + i;
+            const float v = acc[j];
+            const bool valid = j >= jlo && j < jn;
+            if (valid) mrow = fmaxf(mrow, fabsf(v));
+            if (e.kind == EPI_M && valid) {
+              const float rd = v - (j == jd ? 1.0f : 0.0f);
+              part += (j >= jtwo) ? 2.f * (rd * rd) : rd * rd;
+            }
+            m[i] = (j >= jmlo && j < jn) ? fabsf(v) : 0.f;
+          }
+          if (want_cmax) {
+            // after the exchanges lane L holds column L % 16 of the group
+#pragma unroll
+            for (int w = 8; w >= 1; w >>= 1) {
+              const bool up = (lane & w) != 0;
+#pragma unroll
+              for (int i = 0; i < w; ++i) {
+                const float send = up ? m[i] : m[i + w];
+                const float keep = up ? m[i + w] : m[i];
+                m[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, w));
+              }
+            }
+            m[0] = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], 16));
+            if (lane < 16) cmx[16 * gi + lane] = m[0];
+          }
+        }
+        // the group's sums to the scratch slot: [32 column quads][128 rows][4]
+#pragma unroll
+        for (int k4 = 4 * gi; k4 < 4 * gi + 4; ++k4)
+          __stcg(sp + (own * 16 + k4) * TC_BM + r,
+                 make_float4(acc[4 * k4], acc[4 * k4 + 1], acc[4 * k4 + 2], acc[4 * k4 + 3]));
+      }
+      if (drain_max) {
+        rmax_all[slot * (2 * TC_BM) + own * TC_BM + r] = mrow;
+        if (e.kind == EPI_M) {
+          const float pd = warp_sum(part);
+          if (lane == 0) red_all[slot * EPI_WARPS + qd + 4 * own] = (double)pd;   // the output warps' order
+        }
+      }
       __threadfence_block();
       __syncwarp();
       if (lane == 0) mbar_arrive(slot_full(slot));
@@ -693,51 +756,56 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       const bool got = mbar_wait(slot_full(slot), (lt >> 1) & 1, g.err, abort_flag);
       if (out_bar_or(!got || *abort_flag != 0)) break;
       const float4* sp = reinterpret_cast<const float4*>(g.scratch + ((size_t)blockIdx.x * 2 + slot) * (TC_BM * TC_BN));
-      // ---- pass 1: maxima (and the residual of an M product); fp32 results need neither
-      float part = 0.f, mrow = 0.f;
-      const bool want_cmax = transposed && digits_out;
-      float vn[16];
-      if (digits_out) load_row16(sp, 4 * oh, r, vn);
+      float* rmax = rmax_all + slot * (2 * TC_BM);
+      float* cmax = cmax_all + slot * (4 * TC_BN);
+      if (g.split == 1) {
+        // ---- pass 1: maxima (and the residual of an M product); fp32 results need neither.
+        // (A split launch's drain took them; they are visible since slot_full.)
+        float part = 0.f, mrow = 0.f;
+        const bool want_cmax = transposed && digits_out;
+        float vn[16];
+        if (digits_out) load_row16(sp, 4 * oh, r, vn);
 #pragma unroll 1
-      for (int gi = 0; gi < (digits_out ? 4 : 0); ++gi) {
-        float v[16], m[16];
+        for (int gi = 0; gi < (digits_out ? 4 : 0); ++gi) {
+          float v[16], m[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = vn[i];
-        if (gi + 1 < 4) load_row16(sp, 4 * oh + gi + 1, r, vn);     // next group in flight
+          for (int i = 0; i < 16; ++i) v[i] = vn[i];
+          if (gi + 1 < 4) load_row16(sp, 4 * oh + gi + 1, r, vn);     // next group in flight
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int cl = cb + 16 * gi + i;
-          const bool vcol = rv && (tile_n + cl < g.N);
-          const bool valid = vcol && !(diag && cl < r);
-          if (valid) mrow = fmaxf(mrow, fabsf(v[i]));
-          if (e.kind == EPI_M && valid) {
-            const float rd = v[i] - ((tile_n + cl == gr) ? 1.0f : 0.0f);
-            part += (mirror || (diag && cl > r)) ? 2.f * (rd * rd) : rd * rd;
-          }
-          m[i] = (vcol && !(diag && cl <= r)) ? fabsf(v[i]) : 0.f;
-        }
-        if (want_cmax) {
-          // butterfly over the warp: after the exchanges lane L holds column L % 16 of the group
-#pragma unroll
-          for (int w = 8; w >= 1; w >>= 1) {
-            const bool up = (lane & w) != 0;
-#pragma unroll
-            for (int i = 0; i < w; ++i) {
-              const float send = up ? m[i] : m[i + w];
-              const float keep = up ? m[i + w] : m[i];
-              m[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, w));
+          for (int i = 0; i < 16; ++i) {
+            const int cl = cb + 16 * gi + i;
+            const bool vcol = rv && (tile_n + cl < g.N);
+            const bool valid = vcol && !(diag && cl < r);
+            if (valid) mrow = fmaxf(mrow, fabsf(v[i]));
+            if (e.kind == EPI_M && valid) {
+              const float rd = v[i] - ((tile_n + cl == gr) ? 1.0f : 0.0f);
+              part += (mirror || (diag && cl > r)) ? 2.f * (rd * rd) : rd * rd;
             }
+            m[i] = (vcol && !(diag && cl <= r)) ? fabsf(v[i]) : 0.f;
           }
-          m[0] = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], 16));
-          if (lane < 16) cmax[oq * TC_BN + cb + 16 * gi + lane] = m[0];
+          if (want_cmax) {
+            // butterfly over the warp: after the exchanges lane L holds column L % 16 of the group
+#pragma unroll
+            for (int w = 8; w >= 1; w >>= 1) {
+              const bool up = (lane & w) != 0;
+#pragma unroll
+              for (int i = 0; i < w; ++i) {
+                const float send = up ? m[i] : m[i + w];
+                const float keep = up ? m[i + w] : m[i];
+                m[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, w));
+              }
+            }
+            m[0] = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], 16));
+            if (lane < 16) cmax[oq * TC_BN + cb + 16 * gi + lane] = m[0];
+          }
         }
+        rmax[oh * TC_BM + r] = mrow;
+        if (e.kind == EPI_M) {
+          const float pd = warp_sum(part);
+          if (lane == 0) red_all[slot * EPI_WARPS + ow] = (double)pd;
+        }
+        out_bar();                                     // column maxima and residual parts visible
       }
-      rmax[oh * TC_BM + r] = mrow;
-      if (e.kind == EPI_M) {
-        const float pd = warp_sum(part);
-        if (lane == 0) red[ow] = (double)pd;
-      }
-      out_bar();                                       // column maxima and residual parts visible
       if (digits_out) {
         // output scales: the first column half's threads take row r of this tile (and, for a
         // diagonal tile, its lower part mirrored in), the second half's row r of the mirrored
@@ -890,7 +958,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs g, Epi e) {
       if (e.kind == EPI_M && ow == 0 && share == 0) {
         double sum = 0.0;
 #pragma unroll
-        for (int w = 0; w < OUT_WARPS; ++w) sum += red[w];     // fixed order: deterministic
+        for (int w = 0; w < EPI_WARPS; ++w) sum += red_all[slot * EPI_WARPS + w];     // fixed order: deterministic
         epi_m_finish(e, b, sum, g.M, tl);
       }
       // the slot's data is dead: drop its L2 lines without writing them back (the slot is
