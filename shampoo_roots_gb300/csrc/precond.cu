@@ -131,7 +131,7 @@ struct precond_ctx {
   size_t gemm_ev_used = 0;
   EncodeTiledFn encode = nullptr;
   bool tc_attr_set = false;
-  int num_sms = 148;
+  int num_sms = 152;                   // a GB300's; a device handle reads its device's count
   // CUDA graph of the last plan (replayed on an internal stream joined to the caller's by events)
   struct Graph {                       // one captured plan
     std::string key;

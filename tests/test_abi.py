@@ -217,3 +217,28 @@ def test_packed_state_option(host):
     assert sr.precond_set_option(host.h, sr.OPT_PACKED_STATE, 1) is None
     assert host.lib.precond_set_option(host.h, sr.OPT_PACKED_STATE, ctypes.c_double(2.0)) == sr.EINVAL
     assert host.step([(256, 128)]) == sr.ENODEV          # plans and validates with packed state
+
+
+def test_tile_split_sizes_the_hand_over_scratch(host):
+    """A plan of few tiles reserves hand-over slots for up to PRECOND_OPT_TILE_SPLIT
+    CTAs per tile: two 128 x 128 fp32 slots per CTA in each of the plan's scratch
+    regions (the call's stream and the two branch streams of each tcgen05 root
+    class).  The plan bounds a product's tiles by the full square: 2 x 2 for the
+    256^2 products of the single 256x128 gradient, so the split of 4 reserves
+    16 CTAs' slots instead of 4."""
+    slot_bytes = 2 * 128 * 128 * 4
+    regions = 1 + 2 * 2                    # root classes 256 and 128, both on the tcgen05 engine
+    sizes = {}
+    for split in (1, 2, 4):
+        assert sr.precond_set_option(host.h, sr.OPT_TILE_SPLIT, split) is None
+        assert host.step([(256, 128)]) == sr.ENODEV
+        sizes[split] = sr.precond_get_workspace(host.h)[0]
+    assert sizes[2] - sizes[1] == regions * (8 - 4) * slot_bytes
+    assert sizes[4] - sizes[1] == regions * (16 - 4) * slot_bytes
+    # a plan whose products already fill the GPU reserves one CTA per SM whatever the split
+    big = {}
+    for split in (1, 4):
+        sr.precond_set_option(host.h, sr.OPT_TILE_SPLIT, split)
+        assert host.step([(4096, 4096)]) == sr.ENODEV
+        big[split] = sr.precond_get_workspace(host.h)[0]
+    assert big[1] == big[4]
