@@ -91,10 +91,11 @@ typedef struct precond_ctx* precond_t;
 #define PRECOND_OPT_FOLD          10  /* minimax step: the interval's top may not fall below this
                                          fraction of its bottom's factor, T(1) >= fold T(l); [0, 1), default 0.3 */
 #define PRECOND_OPT_BRANCHES      11  /* 1 = when no root class's products fill the GPU (fewer 128 x 128
-                                         tiles than SMs), the iteration stage runs each class's M chain and
-                                         X chain on streams of the handle's own, joined back by events
-                                         (default 1); 0 = everything on the call's stream.  Results are
-                                         identical. */
+                                         tiles than SMs), the stages fork onto streams of the handle's own:
+                                         the two Gram sides, each root class's start and finish kernels,
+                                         and each class's M chain and X chain in the iteration stage, every
+                                         stage joined back into the call's stream by events (default 1);
+                                         0 = everything on the call's stream.  Results are identical. */
 #define PRECOND_OPT_STEP_DEGREE   12  /* degree of the per-step minimax polynomial T_k(M) at p = 4: 2 (default;
                                          T = a I - b M + c M^2, 5 products per iteration, about 7
                                          iterations from l_0 = 1e-6) or 1 (T = a I - b M, 4 products, about
