@@ -191,8 +191,9 @@ int precond_get_timing(precond_t h, double ms[4], int64_t* ns_gemm_launches, dou
  * call's stream; synchronises; -1 in timing mode 2, which records no such
  * events), their number, and the bf16 MMA FLOPs they issued, counted on the
  * device: for every tile actually computed (tiles of converged roots are
- * skipped), 2 x 128 x 128 x 32 per K block and digit product.  Any output
- * pointer may be NULL.
+ * skipped; a tile spread over several CTAs by PRECOND_OPT_TILE_SPLIT counts
+ * once per CTA), 2 x 128 x 128 x 32 per K block and digit product.  Any
+ * output pointer may be NULL.
  */
 int precond_get_gemm_timing(precond_t h, double* ms_total, int64_t* launches, double* issued_flops);
 
