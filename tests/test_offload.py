@@ -1,9 +1,10 @@
 """EMA state kept in host memory and streamed through the device in groups
 ("Online KL Shampoo", zero-delay CPU offload), on CPU: the pages' break-even
-dimension, the grouping, and steps over offloaded state against steps over
+dimension, the grouping, steps over offloaded state against steps over
 resident state, bit for bit, for full and packed layouts and several group
-splits.  The step here is an fp32 EMA with float64-oracle roots; on a GPU it is
-the library's step (``offload.library_step``)."""
+splits, and two gloo ranks whose owners keep their state offloaded against one
+process.  The step here is an fp32 EMA with float64-oracle roots; on a GPU it
+is the library's step (``offload.library_step``)."""
 import math
 
 import numpy as np
@@ -139,3 +140,65 @@ def test_the_tests_see_a_shared_buffer(monkeypatch):
             caught = True
             break
     assert caught
+
+
+def _free_port():
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _local_grads(rank, step):
+    rng = np.random.default_rng([5, rank, step])
+    return [rng.standard_normal(s).astype(np.float32) for s in SHAPES]
+
+
+def _owner_rank(rank, world, port, q):
+    import os
+    import torch.distributed as dist
+    from shampoo_roots_gb300 import sharding
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        plan = sharding.OwnerSharding(SHAPES, rank, world)
+        off = offload.OffloadedState([SHAPES[i] for i in plan.mine], "cpu", packed=True,
+                                     groups=[[j] for j in range(len(plan.mine))])
+        run = off.compute(_ema_step(True))
+        outs = []
+        for step in range(2):
+            grads = [torch.from_numpy(g) for g in _local_grads(rank, step)]
+            outs.append([u.numpy().copy() for u in plan.step(grads, run)])
+        q.put((rank, plan.owners, outs))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_owners_with_offloaded_state_match_a_single_process():
+    """Two gloo ranks, each owner keeping its matrices' packed state offloaded:
+    the same updates as one process stepping every matrix on resident state."""
+    import torch.multiprocessing as mp
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_owner_rank, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=180) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res[0][1] == res[1][1] and set(res[0][1]) == {0, 1}
+    fn = _ema_step(True)
+    L = [torch.zeros(offload.state_numel(m, True)) for m, _ in SHAPES]
+    R = [torch.zeros(offload.state_numel(n, True)) for _, n in SHAPES]
+    for step in range(2):
+        g0, g1 = _local_grads(0, step), _local_grads(1, step)
+        avg = [torch.from_numpy(((a + b) / np.float32(world)).astype(np.float32)) for a, b in zip(g0, g1)]
+        want = fn(list(range(len(SHAPES))), avg, L, R)
+        for rank in range(world):
+            for i, u in enumerate(want):
+                assert np.array_equal(res[rank][2][step][i], u.numpy()), (rank, step, i)
