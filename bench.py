@@ -554,6 +554,8 @@ def main():
         e2e = {"value": job_rate(world, args.steps, t_e2e), "unit": "preconditioner steps/s",
                "ms_per_step": t_e2e / args.steps * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "overlap": "next step's upload and last step's download on copy streams during compute"}
+        if flush is not None:
+            e2e["l2"] = "steps back to back with no L2 flush between them (the device-timed steps flush)"
 
     peaks = load_peaks()
     # dominant kernel: the tcgen05 GEMM of the iteration stage (timed inside a long step -> sustained peak).
